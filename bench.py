@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the sharded RS+AdamW+AG step (FSDP / ZeRO-3 per-step pass) on GB300.
+
+One step = the whole hot path over one synthetic batch of gradients:
+  1. fsdp_reduce_scatter_adamw over every fully_shard group (one launch):
+     N virtual ranks' bf16 gradients summed in fp32 in rank order, divided by
+     N, AdamW on every rank's shard of the fp32 master/moments, bf16 shards
+     written;
+  2. fsdp_all_gather_unpack over every group (one launch): the N shards back
+     into full per-parameter bf16 tensors (n_out replicas, default 1).
+Default workload: the 1.2B Llama-shaped model (24 layers, hidden 2048, FFN
+5632, vocab 32000, untied embeddings) with N = 8 virtual ranks, FSDP2
+per-parameter dim-0 layout, 24 block groups + 1 root group, 1,364,297,728
+parameters.  Every buffer is resident in HBM; the 62.8 GB a step moves are far
+larger than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "sharded RS+AdamW+AG step: params/s and HBM GB/s vs GB300 peak (1 GPU)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="llama_1b2",
+                    choices=["llama_1b2", "llama_block_4096", "probe", "tiny_mlp"])
+    ap.add_argument("--n-out", type=int, default=1, help="all-gather replicas (1 or N)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def make_workload(name: str) -> W.ParamSet:
+    if name == "llama_1b2":
+        return W.llama_1b2()
+    if name == "llama_block_4096":
+        return W.llama_block_4096()
+    if name == "probe":  # one block + small root: a few GB, larger than L2 (profiling case)
+        return W.llama_1b2(layers=1, vocab=4096)
+    return W.tiny_mlp()
+
+
+def step_bytes(N: int, total: int, unpadded: int, n_out: int) -> dict:
+    """Algorithmic bytes: RS+AdamW reads N grads (2 B) + master/m/v (12 B), writes
+    master/m/v (12 B) + the bf16 shard (2 B) for every packed element; the
+    all-gather reads each parameter element's shard (2 B) and writes n_out copies."""
+    rs = (2 * N + 26) * total
+    ag = (2 + 2 * n_out) * unpadded
+    return {"rs_adamw": rs, "all_gather": ag, "step": rs + ag}
+
+
+def workload_config(ps: W.ParamSet, info, n_out: int) -> dict:
+    return {"workload": f"{ps.description}; N={ps.world_size} virtual ranks",
+            "params": int(info["unpadded_numel"]), "packed_numel": int(info["total_numel"]),
+            "world_size": ps.world_size, "groups": len(ps.groups), "tensors": ps.num_params,
+            "layout": W.LAYOUT_NAMES[ps.layout], "n_out": n_out,
+            "storage": "bf16 grads/params, fp32 master/exp_avg/exp_avg_sq",
+            "adamw": {k: v for k, v in W.adamw_hparams().items() if k != "step"},
+            "l2": "no flush: inputs of every step (>= 62 GB at the default workload) exceed L2"}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int, enabled: bool = True):
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        dev = str(local_rank)
+        if vis:
+            parts = [p.strip() for p in vis.split(",") if p.strip()]
+            if local_rank < len(parts):
+                dev = parts[local_rank]
+        self.path = f"/tmp/ss_clocks_{os.getpid()}.csv"
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", dev], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    cols = [c.strip() for c in line.split(",")]
+                    if len(cols) < 9:
+                        continue
+                    try:
+                        sm.append(float(cols[1]))
+                        smax.append(float(cols[2]))
+                        power.append(float(cols[3]))
+                    except ValueError:
+                        continue
+                    for nm, val in zip(names, cols[5:9]):
+                        if val.lower() == "active":
+                            reasons.add(nm)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, local: int):
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return dist
+    torch.cuda.set_device(local)
+    return None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Device buffers and the two C-ABI calls of one step."""
+
+    def __init__(self, ss, ps: W.ParamSet, n_out: int):
+        self.ss = ss
+        self.ps = ps
+        self.N = ps.world_size
+        self.n_out = n_out
+        d0, inner = ps.dim0_inner()
+        eb = 2 if ps.dtype == torch.bfloat16 else 4
+        self.plan = ss.fsdp_plan_create(ps.layout, self.N, eb, d0, inner, group_num_params=ps.groups)
+        self.info = self.plan.info().as_dict()
+        total = self.info["total_numel"]
+        dev = "cuda"
+        # parameters -> shards, fp32 state
+        params = W.make_params(ps, device=dev)
+        self.shards = torch.empty(total, dtype=ps.dtype, device=dev)
+        ss.fsdp_pack(self.plan, params, self.shards)
+        del params
+        self.master = torch.empty(total, dtype=torch.float32, device=dev)
+        self.m = torch.empty_like(self.master)
+        self.v = torch.empty_like(self.master)
+        ss.fsdp_init_master(self.plan, self.shards, self.master, self.m, self.v)
+        # every rank's gradient, generated per parameter then packed (pads zero)
+        self.grads = []
+        for r, rank in enumerate(self._rank_grad_iter(dev)):
+            buf = torch.empty(total, dtype=ps.dtype, device=dev)
+            ss.fsdp_pack(self.plan, rank, buf)
+            self.grads.append(buf)
+            del rank
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        # outputs: n_out replicas, each one flat buffer with 16-byte aligned params
+        numels = ps.numels()
+        offs, pos = [], 0
+        for n in numels:
+            offs.append(pos)
+            pos += (n + 7) // 8 * 8
+        self.out_numel = pos
+        self.out_flat = [torch.empty(pos, dtype=ps.dtype, device=dev) for _ in range(n_out)]
+        self.outs = [o[off:off + n] for o in self.out_flat for off, n in zip(offs, numels)]
+        self.t = 0
+
+    def _rank_grad_iter(self, dev):
+        ps = self.ps
+        g = torch.Generator(device=dev)
+        g.manual_seed(ps.seed * 7919 + 17)
+        for _ in range(self.N):
+            yield [(torch.randn(n, generator=g, device=dev) * ps.grad_std).to(ps.dtype)
+                   for n in ps.numels()]
+
+    def rs_adamw(self, stream=None):
+        self.t += 1
+        hp = self.ss.adamw_params(step=self.t, **{k: v for k, v in W.adamw_hparams().items()
+                                                   if k != "step"})
+        self.ss.fsdp_reduce_scatter_adamw(self.plan, self.grads, self.master, self.m, self.v,
+                                          self.shards, hp, None, -1, stream)
+
+    def all_gather(self, stream=None):
+        self.ss.fsdp_all_gather_unpack(self.plan, self.shards, self.outs, self.n_out, -1, stream)
+
+
+def run_native(args, world, rank, local, dist):
+    import __graft_entry__
+    __graft_entry__.build()
+    import sharded_state_gb300 as ss
+    ps = make_workload(args.workload)
+    st = Step(ss, ps, args.n_out)
+    P = st.info["unpadded_numel"]
+    total = st.info["total_numel"]
+    N = st.N
+    by = step_bytes(N, total, P, args.n_out)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    for _ in range(max(args.warmup, 0)):
+        st.rs_adamw(sp)
+        st.all_gather(sp)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.3 if clocks.proc else 0)  # let the sampler start
+    launches0 = ss.ss_launch_count()
+    e0.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        st.rs_adamw(sp)
+        ev[k][1].record(stream)
+        st.all_gather(sp)
+        ev[k][2].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = ss.ss_launch_count() - launches0
+    clk = clocks.stop()
+    barrier(dist)
+    ms = e0.elapsed_time(e1)
+    rs_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    ag_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    ms_max = max_over_ranks(dist, ms)
+    value = P * K * world / (ms_max / 1e3)
+    hbm = by["step"] * K / (ms / 1e3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    rs_avg = sum(rs_ms) / K
+    rs_gbs = by["rs_adamw"] / (rs_avg / 1e3) / 1e9
+    ag_avg = sum(ag_ms) / K
+    ag_gbs = by["all_gather"] / (ag_avg / 1e3) / 1e9
+
+    out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": K,
+           "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "impl": "native", "config": workload_config(ps, st.info, args.n_out),
+           "hbm_gbs": hbm, "bytes_per_step": by["step"],
+           "frac_of_measured_peak": hbm / peak, "frac_of_nominal_8tbs": hbm / NOMINAL_HBM_GBS,
+           "kernels": {"rs_adamw": {"ms": rs_avg, "ms_min": min(rs_ms), "gbs": rs_gbs,
+                                    "bytes": by["rs_adamw"]},
+                       "all_gather_unpack": {"ms": ag_avg, "ms_min": min(ag_ms), "gbs": ag_gbs,
+                                             "bytes": by["all_gather"]}},
+           "roofline": {"bound": "hbm", "kernel": "rs_adamw", "achieved": rs_gbs, "peak": peak,
+                        "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                        if peak_kind == "measured" else "fallback 6.8 TB/s",
+                        "unit": "GB/s", "frac": rs_gbs / peak, "traffic": None,
+                        "per_unit_bytes": 2 * N + 26, "units_per_launch": total},
+           "gpu_launches": launches, "clocks": clk}
+
+    # e2e: the same step through the C ABI with host buffers
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(st, args, stream, dist)
+    # CPU oracle baseline (rank 0, N=1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(st, ps, args)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(st: Step, args, stream, dist) -> dict:
+    """Per step: pinned host -> device copy of the N gradient buffers, the two
+    C-ABI calls, device -> pinned host copy of the gathered parameters."""
+    total = st.info["total_numel"]
+    N = st.N
+    need = N * total * 2 + st.n_out * st.out_numel * 2
+    try:
+        phys = os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except Exception:
+        phys = 0
+    if phys and need * 2 > phys:
+        return {"value": None, "unit": "params/s", "skipped": f"needs {need / 1e9:.1f} GB pinned host"}
+    host_g = []
+    for r in range(N):
+        h = torch.empty(total, dtype=st.ps.dtype, pin_memory=True)
+        h.copy_(st.grads[r])
+        host_g.append(h)
+    host_out = [torch.empty(st.out_numel, dtype=st.ps.dtype, pin_memory=True)
+                for _ in range(st.n_out)]
+    torch.cuda.synchronize()
+    K = max(args.e2e_steps, 1)
+    P = st.info["unpadded_numel"]
+    sp = stream.cuda_stream
+    # one untimed pass to settle the copy engines
+    for r in range(N):
+        st.grads[r].copy_(host_g[r], non_blocking=True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        for r in range(N):
+            st.grads[r].copy_(host_g[r], non_blocking=True)
+        st.rs_adamw(sp)
+        st.all_gather(sp)
+        for j in range(st.n_out):
+            host_out[j].copy_(st.out_flat[j], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    res = {"value": P * K * world / (ms / 1e3), "unit": "params/s", "steps": K,
+           "ms_per_step": ms / K, "h2d_bytes_per_step": N * total * 2,
+           "d2h_bytes_per_step": st.n_out * st.out_numel * 2}
+    del host_g, host_out
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: baseline leg and reference arm
+# ---------------------------------------------------------------------------
+
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_sample_from_step(st: Step):
+    """Block group 0 of the workload, copied from the device buffers."""
+    import sharded_state_gb300 as ss
+    grp = ss.fsdp_plan_group(st.plan, 0)
+    base, span = grp["base"], st.N * grp["shard_numel"]
+    a, b = grp["first_param"], grp["first_param"] + grp["num_params"]
+    sl = slice(base, base + span)
+    to_u16 = lambda t: t[sl].cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    return {"grads": [to_u16(g) for g in st.grads], "master": st.master[sl].cpu().numpy().copy(),
+            "m": st.m[sl].cpu().numpy().copy(), "v": st.v[sl].cpu().numpy().copy(),
+            "shard_numel": grp["shard_numel"], "params": a, "params_end": b, "span": span}
+
+
+def _oracle_sample_cpu(ps: W.ParamSet):
+    """Block group 0 of the workload, drawn on the host (reference arm)."""
+    import oracle
+    g0 = ps.groups[0]
+    d0, inner = ps.dim0_inner()
+    lay = oracle.layout(ps.layout, ps.world_size, 2, d0[:g0], inner[:g0])
+    span = lay["total_numel"]
+    gen = torch.Generator().manual_seed(ps.seed)
+    params = (torch.randn(span, generator=gen) * ps.param_std).to(ps.dtype)
+    master = params.float().numpy().copy()
+    grads = [(torch.randn(span, generator=gen) * ps.grad_std).to(ps.dtype)
+             .view(torch.int16).numpy().view(np.uint16).copy() for _ in range(ps.world_size)]
+    return {"grads": grads, "master": master, "m": np.zeros(span, np.float32),
+            "v": np.zeros(span, np.float32), "shard_numel": lay["shard_numel"], "params": 0,
+            "params_end": g0, "span": span}
+
+
+def _oracle_step(ps: W.ParamSet, smp: dict, t: int):
+    import oracle
+    hp = W.adamw_hparams(t)
+    d0, inner = ps.dim0_inner()
+    a, b = smp["params"], smp["params_end"]
+    shards, _ = oracle.reduce_scatter_adamw(
+        ps.world_size, smp["shard_numel"], smp["grads"], smp["master"], smp["m"], smp["v"],
+        **{k: hp[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")})
+    oracle.all_gather_unpack(ps.layout, ps.world_size, 2, d0[a:b], inner[a:b], shards)
+    return int(sum(ps.numels()[a:b]))
+
+
+def cpu_baseline(st: Step, ps: W.ParamSet, args) -> dict:
+    import oracle
+    cores = _host_cores()
+    oracle.set_threads(cores)
+    smp = _oracle_sample_from_step(st)
+    used = cores if oracle.has_openmp() else 1
+    t0 = time.perf_counter()
+    reps, params = 0, 0
+    while True:
+        params += _oracle_step(ps, smp, 1000 + reps)
+        reps += 1
+        if time.perf_counter() - t0 >= args.cpu_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": params / dt, "unit": "params/s", "cores": used, "kind": "oracle",
+            "sample": f"block group 0 ({params // reps:,} params, N={ps.world_size}) of the same "
+                      f"workload, {reps} oracle RS+AdamW+AG steps, inputs copied from the device "
+                      f"buffers, {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    ps = make_workload(args.workload)
+    cores = _host_cores()
+    oracle.set_threads(cores)
+    used = cores if oracle.has_openmp() else 1
+    smp = _oracle_sample_cpu(ps)
+    for w in range(max(args.warmup, 0)):
+        _oracle_step(ps, smp, w + 1)
+    t0 = time.perf_counter()
+    params = 0
+    for k in range(args.steps):
+        params += _oracle_step(ps, smp, args.warmup + k + 1)
+    dt = time.perf_counter() - t0
+    d0, inner = ps.dim0_inner()
+    info = {"unpadded_numel": ps.total_unpadded(), "total_numel": ps.total_unpadded()}
+    value = params / dt
+    sample = (f"block group 0 ({params // max(args.steps, 1):,} params, N={ps.world_size}) per "
+              f"step, drawn on the host; {args.steps} timed oracle RS+AdamW+AG steps")
+    out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": dt / max(args.steps, 1) * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "impl": "reference", "config": workload_config(ps, info, args.n_out),
+           "cpu_baseline": {"value": value, "unit": "params/s", "cores": used, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    dist = dist_init(world, local)
+    try:
+        run_native(args, world, rank, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

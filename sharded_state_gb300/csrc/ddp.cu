@@ -1,0 +1,242 @@
+// ddp.cu -- DDP gradient bucketing with a bucketed mean over N virtual ranks.
+//
+// "Scaling data parallel", sections 3-4: a gradient is final as soon as its
+// layer's backward is done, last layer first, so tensors are visited in
+// reverse registration order; gradients accumulate in a bucket and, once the
+// bucket holds at least bucket_cap bytes, it goes out as one all-reduce (sum,
+// then divide by N).  Small buckets pay the fixed per-collective cost many
+// times; a huge cap exposes the last bucket.
+//
+// On one GPU the N ranks' gradients are N sets of tensors in HBM, so one
+// bucket's pack + all-reduce + unpack is a single pass: for each element of
+// each tensor in the bucket, read N bf16 values, sum in fp32 in rank order,
+// divide by N, round to bf16 and write the average (2N + 2 bytes per
+// element).  One kernel launch per bucket keeps the per-collective fixed cost
+// visible.  The per-tensor pointers and the bucket-order prefix sums of the
+// sizes go to the device in a per-call table.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <vector>
+
+#include "device_utils.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// Sum one 8-element vector over ranks (rank order, fp32), divide by N, round.
+template <int NR>
+__device__ __forceinline__ uint4 mean8(const void* const* in, int N, int64_t k) {
+    const int n = NR > 0 ? NR : N;
+    uint4 w0 = ss::ld_stream_u4(static_cast<const uint16_t*>(in[0]) + k);
+    float s[8] = {ss::bf16_lo(w0.x), ss::bf16_hi(w0.x), ss::bf16_lo(w0.y), ss::bf16_hi(w0.y),
+                  ss::bf16_lo(w0.z), ss::bf16_hi(w0.z), ss::bf16_lo(w0.w), ss::bf16_hi(w0.w)};
+    if (NR > 0) {
+        uint4 w[NR > 1 ? NR - 1 : 1];
+#pragma unroll
+        for (int r = 1; r < NR; ++r) w[r - 1] = ss::ld_stream_u4(static_cast<const uint16_t*>(in[r]) + k);
+#pragma unroll
+        for (int r = 1; r < NR; ++r) {
+            s[0] = __fadd_rn(s[0], ss::bf16_lo(w[r - 1].x));
+            s[1] = __fadd_rn(s[1], ss::bf16_hi(w[r - 1].x));
+            s[2] = __fadd_rn(s[2], ss::bf16_lo(w[r - 1].y));
+            s[3] = __fadd_rn(s[3], ss::bf16_hi(w[r - 1].y));
+            s[4] = __fadd_rn(s[4], ss::bf16_lo(w[r - 1].z));
+            s[5] = __fadd_rn(s[5], ss::bf16_hi(w[r - 1].z));
+            s[6] = __fadd_rn(s[6], ss::bf16_lo(w[r - 1].w));
+            s[7] = __fadd_rn(s[7], ss::bf16_hi(w[r - 1].w));
+        }
+    } else {
+        for (int r = 1; r < n; ++r) {
+            uint4 w = ss::ld_stream_u4(static_cast<const uint16_t*>(in[r]) + k);
+            s[0] = __fadd_rn(s[0], ss::bf16_lo(w.x));
+            s[1] = __fadd_rn(s[1], ss::bf16_hi(w.x));
+            s[2] = __fadd_rn(s[2], ss::bf16_lo(w.y));
+            s[3] = __fadd_rn(s[3], ss::bf16_hi(w.y));
+            s[4] = __fadd_rn(s[4], ss::bf16_lo(w.z));
+            s[5] = __fadd_rn(s[5], ss::bf16_hi(w.z));
+            s[6] = __fadd_rn(s[6], ss::bf16_lo(w.w));
+            s[7] = __fadd_rn(s[7], ss::bf16_hi(w.w));
+        }
+    }
+    const float fN = (float)n;
+    uint4 o;
+    o.x = ss::pack_bf16x2(__fdiv_rn(s[0], fN), __fdiv_rn(s[1], fN));
+    o.y = ss::pack_bf16x2(__fdiv_rn(s[2], fN), __fdiv_rn(s[3], fN));
+    o.z = ss::pack_bf16x2(__fdiv_rn(s[4], fN), __fdiv_rn(s[5], fN));
+    o.w = ss::pack_bf16x2(__fdiv_rn(s[6], fN), __fdiv_rn(s[7], fN));
+    return o;
+}
+
+__device__ __forceinline__ uint16_t mean1(const void* const* in, int N, int64_t k) {
+    float s = ss::bf16_to_f32(static_cast<const uint16_t*>(in[0])[k]);
+    for (int r = 1; r < N; ++r) s = __fadd_rn(s, ss::bf16_to_f32(static_cast<const uint16_t*>(in[r])[k]));
+    return ss::f32_to_bf16(__fdiv_rn(s, (float)N));
+}
+
+// Average one tensor piece [k0, k1) of the tensor whose N inputs and one
+// output are ptrs[0..N] (CTA-cooperative).
+template <int NR>
+__device__ __forceinline__ void avg_piece(const void* const* ptrs, int N, int64_t k0, int64_t k1) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(ptrs[N]));
+    // vector path needs every pointer congruent to the output mod 16 bytes
+    const uintptr_t ref = reinterpret_cast<uintptr_t>(out + k0) & 15u;
+    bool vec = true;
+    for (int r = 0; r < N; ++r)
+        vec &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(ptrs[r]) + k0) & 15u) == ref);
+    if (!vec) {
+        for (int64_t k = k0 + tid; k < k1; k += nt) out[k] = mean1(ptrs, N, k);
+        return;
+    }
+    int64_t head = (int64_t)(((16u - ref) & 15u) / 2);
+    if (head > k1 - k0) head = k1 - k0;
+    if (tid < head) out[k0 + tid] = mean1(ptrs, N, k0 + tid);
+    const int64_t vb = k0 + head;
+    const int64_t nvec = (k1 - vb) / 8;
+    for (int64_t q = tid; q < nvec; q += nt) {
+        const int64_t k = vb + 8 * q;
+        ss::st_stream_u4(out + k, mean8<NR>(ptrs, N, k));
+    }
+    const int64_t done = vb + 8 * nvec;
+    if (tid < k1 - done) out[done + tid] = mean1(ptrs, N, done + tid);
+}
+
+// One bucket: tensors [o_lo, o_hi) of the bucket-ordered table; prefix[o] is
+// the element offset of tensor o in bucket order.
+template <int NR>
+__global__ void __launch_bounds__(kThreads)
+ddp_bucket_kernel(const int64_t* __restrict__ prefix, const void* const* __restrict__ ptrs, int N,
+                  int o_lo, int o_hi) {
+    const int64_t u_lo = prefix[o_lo], u_hi = prefix[o_hi];
+    const int64_t span = u_hi - u_lo;
+    int64_t per = (span + gridDim.x - 1) / gridDim.x;
+    per = (per + 63) / 64 * 64;
+    int64_t u = u_lo + per * blockIdx.x;
+    const int64_t u_end = u + per < u_hi ? u + per : u_hi;
+    if (u >= u_end) return;
+    // last tensor in [o_lo, o_hi) whose prefix <= u
+    int lo = o_lo, hi = o_hi;
+    while (hi - lo > 1) {
+        int mid = lo + ((hi - lo) >> 1);
+        if (prefix[mid] <= u) lo = mid;
+        else hi = mid;
+    }
+    int o = lo;
+    while (u < u_end && o < o_hi) {
+        const int64_t t_end = prefix[o + 1];
+        const int64_t piece_end = t_end < u_end ? t_end : u_end;
+        if (piece_end > u)
+            avg_piece<NR>(ptrs + (size_t)o * (N + 1), N, u - prefix[o], piece_end - prefix[o]);
+        u = piece_end > u ? piece_end : u;
+        ++o;
+    }
+}
+
+using DdpKernel = void (*)(const int64_t*, const void* const*, int, int, int);
+
+DdpKernel pick(int N) {
+    switch (N) {
+        case 1: return ddp_bucket_kernel<1>;
+        case 2: return ddp_bucket_kernel<2>;
+        case 3: return ddp_bucket_kernel<3>;
+        case 4: return ddp_bucket_kernel<4>;
+        case 5: return ddp_bucket_kernel<5>;
+        case 6: return ddp_bucket_kernel<6>;
+        case 7: return ddp_bucket_kernel<7>;
+        case 8: return ddp_bucket_kernel<8>;
+        default: return ddp_bucket_kernel<0>;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int ddp_bucket_assign(int num_tensors, const int64_t* numels, int elem_bytes,
+                      size_t bucket_cap_bytes, int* bucket_of) {
+    if (num_tensors < 0 || (num_tensors > 0 && (!numels || !bucket_of))) return SS_EINVAL;
+    if (bucket_cap_bytes == 0 || (elem_bytes != 2 && elem_bytes != 4)) return SS_EINVAL;
+    int bucket = 0;
+    unsigned long long fill = 0;
+    for (int t = num_tensors - 1; t >= 0; --t) {
+        if (numels[t] < 0) return SS_EINVAL;
+        bucket_of[t] = bucket;
+        fill += (unsigned long long)numels[t] * (unsigned long long)elem_bytes;
+        if (fill >= bucket_cap_bytes) {
+            ++bucket;
+            fill = 0;
+        }
+    }
+    return fill > 0 ? bucket + 1 : bucket;
+}
+
+int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* numels,
+                            const void* const* rank_grads, size_t bucket_cap_bytes,
+                            void* const* avg_out, int* num_buckets_out, ss_stream_t stream) {
+    if (world_size < 1 || world_size > SS_MAX_WORLD || num_tensors < 0) return SS_EINVAL;
+    if (num_tensors > 0 && (!numels || !rank_grads || !avg_out)) return SS_EINVAL;
+    if (bucket_cap_bytes == 0) return SS_EINVAL;
+    const int N = world_size, T = num_tensors;
+    for (int t = 0; t < T; ++t) {
+        if (numels[t] < 0 || numels[t] > ((int64_t)1 << 60)) return SS_EINVAL;
+        if (numels[t] == 0) continue;
+        if (!avg_out[t]) return SS_EINVAL;
+        if (!ss::aligned(avg_out[t], 2)) return SS_EALIGN;
+        for (int r = 0; r < N; ++r) {
+            const void* q = rank_grads[(size_t)r * T + t];
+            if (!q) return SS_EINVAL;
+            if (!ss::aligned(q, 2)) return SS_EALIGN;
+        }
+    }
+    std::vector<int> bucket_of((size_t)(T > 0 ? T : 1));
+    const int nb = ddp_bucket_assign(T, numels, 2, bucket_cap_bytes, bucket_of.data());
+    if (nb < 0) return nb;
+    if (num_buckets_out) *num_buckets_out = nb;
+    if (nb == 0) return SS_OK;
+
+    // table in bucket order (reverse registration order): prefix[T+1] then ptrs[T][N+1]
+    const size_t n_prefix = (size_t)T + 1;
+    const size_t n_ptrs = (size_t)T * (size_t)(N + 1);
+    std::vector<unsigned char> host(n_prefix * 8 + n_ptrs * 8);
+    int64_t* prefix = reinterpret_cast<int64_t*>(host.data());
+    const void** ptrs = reinterpret_cast<const void**>(host.data() + n_prefix * 8);
+    std::vector<int> bucket_start((size_t)nb + 1, 0);
+    prefix[0] = 0;
+    for (int o = 0; o < T; ++o) {
+        const int t = T - 1 - o;
+        prefix[o + 1] = prefix[o] + numels[t];
+        for (int r = 0; r < N; ++r) ptrs[(size_t)o * (N + 1) + r] = rank_grads[(size_t)r * T + t];
+        ptrs[(size_t)o * (N + 1) + N] = avg_out[t];
+        if (o == 0 || bucket_of[t] != bucket_of[t + 1]) bucket_start[bucket_of[t]] = o;
+    }
+    bucket_start[nb] = T;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void* d_table = nullptr;
+    cudaError_t e = cudaMallocAsync(&d_table, host.size(), st);
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    e = cudaMemcpyAsync(d_table, host.data(), host.size(), cudaMemcpyHostToDevice, st);
+    int rc = e == cudaSuccess ? SS_OK : ss::cuda_fail(e);
+    const int64_t* d_prefix = static_cast<const int64_t*>(d_table);
+    const void* const* d_ptrs =
+        reinterpret_cast<const void* const*>(static_cast<unsigned char*>(d_table) + n_prefix * 8);
+    DdpKernel fn = pick(N);
+    const int64_t cap = (int64_t)ss::num_sms() * 4;
+    for (int b = 0; rc == SS_OK && b < nb; ++b) {
+        const int o_lo = bucket_start[b], o_hi = bucket_start[b + 1];
+        const int64_t elems = prefix[o_hi] - prefix[o_lo];
+        if (elems == 0) continue;
+        int64_t want = (elems + 4095) / 4096;
+        const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+        fn<<<grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
+        rc = ss::check_launch();
+    }
+    cudaError_t ef = cudaFreeAsync(d_table, st);
+    if (rc == SS_OK && ef != cudaSuccess) rc = ss::cuda_fail(ef);
+    return rc;
+}
+
+}  // extern "C"

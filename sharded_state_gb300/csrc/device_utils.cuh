@@ -1,0 +1,72 @@
+// device_utils.cuh -- small device helpers: bf16 <-> fp32 on packed words and
+// 128-bit global loads/stores with cache hints.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace ss {
+
+// Widen the two bf16 values packed in a 32-bit word (element 2j in the low
+// half, 2j+1 in the high half); exact.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// Round two floats to bf16 (round to nearest even), low half = a.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float a) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(a));
+}
+
+// Read-only streaming 128-bit load: not kept in L1, L2 fetch in 256-byte
+// granules (each element is read once per launch).
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 128-bit load of data this kernel later overwrites (not .nc).
+__device__ __forceinline__ float4 ld_rw_f4(const float* p) {
+    float4 r;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Streaming 128-bit stores (evict-first).
+__device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Index of the last segment in [lo, hi) whose start is <= u (segments sorted by start,
+// the first one starting at or before u).
+template <typename SegT>
+__device__ __forceinline__ int find_seg(const SegT* segs, int lo, int hi, int64_t u) {
+    while (hi - lo > 1) {
+        int mid = lo + ((hi - lo) >> 1);
+        if (segs[mid].start <= u)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+}  // namespace ss

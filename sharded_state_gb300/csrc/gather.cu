@@ -1,0 +1,321 @@
+// gather.cu -- pack (per-parameter tensors -> sharded layout) and all-gather +
+// unpack (rank shards -> full per-parameter tensors).
+//
+// Both walk the plan's data-segment table: each segment is one contiguous run
+// of a parameter inside one rank's shard ("FSDP1 vs FSDP2", section 03: a
+// FlatParameter chunk may hold the tail of one parameter, pad and the head of
+// the next; FSDP2 rank r holds rows [r*c_i, (r+1)*c_i) of every parameter).
+// The segments are ordered by parameter then rank; their lengths define a
+// virtual iteration space U (the unpadded parameters back to back).  The grid
+// splits U into equal contiguous ranges, one per CTA; a CTA finds its first
+// segment by binary search over the segment starts and then walks segments,
+// copying each piece with 128-bit vectors whenever source and destination are
+// congruent mod 16 bytes (scalar element copies otherwise).  Pack also writes
+// zeros over the pad segments.  Pure data movement: HBM-bound, 2 + 2*n_out
+// bytes per bf16 element for the all-gather, 4 for pack (plus pad writes).
+//
+// Per-parameter pointers travel in the kernel parameters (up to kTabBig per
+// launch); more parameters x replicas than that are split into windows of
+// consecutive parameters, whose segments are consecutive in the table.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "device_utils.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTabSmall = 256;
+constexpr int kTabBig = 2048;
+
+template <int CAP>
+struct PtrTab {
+    void* p[CAP];
+};
+
+// Copy `nelem` elements of E bytes from src to the n_dst destinations; every
+// thread of the CTA takes part.  When all destinations are congruent to src
+// mod 16, the body moves in 128-bit vectors (4 per thread in flight).
+template <int E>
+__device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
+                                         const unsigned char* src, int64_t nelem) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const uintptr_t s = reinterpret_cast<uintptr_t>(src);
+    bool vec = true;
+    for (int j = 0; j < n_dst; ++j) vec &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ s) & 15u) == 0;
+    if (!vec) {
+        for (int64_t k = tid; k < nelem; k += nt) {
+            if (E == 2) {
+                uint16_t x = reinterpret_cast<const uint16_t*>(src)[k];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[k] = x;
+            } else {
+                uint32_t x = reinterpret_cast<const uint32_t*>(src)[k];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[k] = x;
+            }
+        }
+        return;
+    }
+    int64_t head = (int64_t)(((16u - (s & 15u)) & 15u) / E);
+    if (head > nelem) head = nelem;
+    if (tid < head) {
+        if (E == 2) {
+            uint16_t x = reinterpret_cast<const uint16_t*>(src)[tid];
+            for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[tid] = x;
+        } else {
+            uint32_t x = reinterpret_cast<const uint32_t*>(src)[tid];
+            for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[tid] = x;
+        }
+    }
+    const int64_t body = nelem - head;
+    const int64_t nvec = body * E / 16;
+    const unsigned char* sv = src + head * E;
+    int64_t q = tid;
+    for (; q + 3 * nt < nvec; q += 4 * nt) {
+        uint4 x0 = ss::ld_stream_u4(sv + 16 * q);
+        uint4 x1 = ss::ld_stream_u4(sv + 16 * (q + nt));
+        uint4 x2 = ss::ld_stream_u4(sv + 16 * (q + 2 * nt));
+        uint4 x3 = ss::ld_stream_u4(sv + 16 * (q + 3 * nt));
+        for (int j = 0; j < n_dst; ++j) {
+            unsigned char* dv = dst[j] + head * E;
+            ss::st_stream_u4(dv + 16 * q, x0);
+            ss::st_stream_u4(dv + 16 * (q + nt), x1);
+            ss::st_stream_u4(dv + 16 * (q + 2 * nt), x2);
+            ss::st_stream_u4(dv + 16 * (q + 3 * nt), x3);
+        }
+    }
+    for (; q < nvec; q += nt) {
+        uint4 x = ss::ld_stream_u4(sv + 16 * q);
+        for (int j = 0; j < n_dst; ++j) ss::st_stream_u4(dst[j] + head * E + 16 * q, x);
+    }
+    const int64_t done = head + nvec * 16 / E;
+    const int64_t tail = nelem - done;
+    if (tid < tail) {
+        const int64_t k = done + tid;
+        if (E == 2) {
+            uint16_t x = reinterpret_cast<const uint16_t*>(src)[k];
+            for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[k] = x;
+        } else {
+            uint32_t x = reinterpret_cast<const uint32_t*>(src)[k];
+            for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[k] = x;
+        }
+    }
+}
+
+// Zero `nelem` elements of E bytes at dst (CTA-cooperative).
+template <int E>
+__device__ __forceinline__ void cta_zero(unsigned char* dst, int64_t nelem) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst);
+    int64_t head = (int64_t)(((16u - (d & 15u)) & 15u) / E);
+    if (head > nelem) head = nelem;
+    for (int64_t k = tid; k < head; k += nt) {
+        if (E == 2) reinterpret_cast<uint16_t*>(dst)[k] = 0;
+        else reinterpret_cast<uint32_t*>(dst)[k] = 0;
+    }
+    const int64_t nvec = (nelem - head) * E / 16;
+    unsigned char* dv = dst + head * E;
+    for (int64_t q = tid; q < nvec; q += nt) ss::st_stream_u4(dv + 16 * q, make_uint4(0, 0, 0, 0));
+    for (int64_t k = head + nvec * 16 / E + tid; k < nelem; k += nt) {
+        if (E == 2) reinterpret_cast<uint16_t*>(dst)[k] = 0;
+        else reinterpret_cast<uint32_t*>(dst)[k] = 0;
+    }
+}
+
+// This CTA's share [u0, u1) of [u_lo, u_hi): equal contiguous ranges, rounded
+// to 64 elements.
+__device__ __forceinline__ void cta_range(int64_t u_lo, int64_t u_hi, int64_t* u0, int64_t* u1) {
+    int64_t span = u_hi - u_lo;
+    int64_t per = (span + gridDim.x - 1) / gridDim.x;
+    per = (per + 63) / 64 * 64;
+    *u0 = u_lo + per * blockIdx.x;
+    *u1 = *u0 + per < u_hi ? *u0 + per : u_hi;
+}
+
+// dir 0: all-gather + unpack (packed -> params, n_out replicas)
+// dir 1: pack (params -> packed)
+template <int E, int CAP, int DIR>
+__global__ void __launch_bounds__(kThreads)
+seg_copy_kernel(const ss::Seg* __restrict__ segs, int s_lo, int s_hi, int64_t u_lo, int64_t u_hi,
+                unsigned char* packed, PtrTab<CAP> tab, int param_base, int ptr_stride,
+                int n_out) {
+    int64_t u, u_end;
+    cta_range(u_lo, u_hi, &u, &u_end);
+    if (u >= u_end) return;
+    int k = ss::find_seg(segs, s_lo, s_hi, u);
+    unsigned char* dsts[DIR == 0 ? 8 : 1];
+    while (u < u_end && k < s_hi) {
+        const ss::Seg sg = segs[k];
+        const int64_t seg_end = sg.start + sg.len;
+        const int64_t piece_end = seg_end < u_end ? seg_end : u_end;
+        const int64_t off = u - sg.start;
+        const int64_t len = piece_end - u;
+        const int slot = sg.param - param_base;
+        if (DIR == 0) {
+            const unsigned char* src = packed + (sg.packed_off + off) * E;
+            // replicas in batches of up to 8 destinations per pass over the source
+            for (int j0 = 0; j0 < n_out; j0 += 8) {
+                int nd = n_out - j0 < 8 ? n_out - j0 : 8;
+                for (int j = 0; j < nd; ++j)
+                    dsts[j] = static_cast<unsigned char*>(tab.p[(j0 + j) * ptr_stride + slot]) +
+                              (sg.param_off + off) * E;
+                cta_copy<E>(dsts, nd, src, len);
+            }
+        } else {
+            const unsigned char* src =
+                static_cast<const unsigned char*>(tab.p[slot]) + (sg.param_off + off) * E;
+            dsts[0] = packed + (sg.packed_off + off) * E;
+            cta_copy<E>(dsts, 1, src, len);
+        }
+        u = piece_end;
+        ++k;
+    }
+}
+
+template <int E>
+__global__ void __launch_bounds__(kThreads)
+zero_fill_kernel(const ss::Seg* __restrict__ segs, int s_lo, int s_hi, int64_t u_lo, int64_t u_hi,
+                 unsigned char* packed) {
+    int64_t u, u_end;
+    cta_range(u_lo, u_hi, &u, &u_end);
+    if (u >= u_end) return;
+    int k = ss::find_seg(segs, s_lo, s_hi, u);
+    while (u < u_end && k < s_hi) {
+        const ss::Seg sg = segs[k];
+        const int64_t seg_end = sg.start + sg.len;
+        const int64_t piece_end = seg_end < u_end ? seg_end : u_end;
+        cta_zero<E>(packed + (sg.packed_off + (u - sg.start)) * E, piece_end - u);
+        u = piece_end;
+        ++k;
+    }
+}
+
+int copy_grid(int64_t elems) {
+    int64_t want = (elems + 4095) / 4096;  // >= 16 KiB of bf16 per CTA
+    int64_t cap = (int64_t)ss::num_sms() * 4;
+    if (want < 1) want = 1;
+    return (int)(want < cap ? want : cap);
+}
+
+template <int CAP>
+int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed,
+                  void* const* ptrs, int n_out, cudaStream_t st) {
+    const int s_lo = p->param_seg[a], s_hi = p->param_seg[b];
+    if (s_hi <= s_lo) return SS_OK;
+    const int64_t u_lo = p->data[s_lo].start;
+    const int64_t u_hi = p->data[s_hi - 1].start + p->data[s_hi - 1].len;
+    PtrTab<CAP> tab;
+    std::memset(&tab, 0, sizeof tab);
+    const int w = b - a;
+    for (int j = 0; j < n_out; ++j)
+        for (int i = a; i < b; ++i) tab.p[j * w + (i - a)] = ptrs[(size_t)j * p->n + i];
+    const int grid = copy_grid(u_hi - u_lo);
+    if (p->eb == 2) {
+        if (dir == 0)
+            seg_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
+                                                                  packed, tab, a, w, n_out);
+        else
+            seg_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
+                                                                  packed, tab, a, w, 1);
+    } else {
+        if (dir == 0)
+            seg_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
+                                                                  packed, tab, a, w, n_out);
+        else
+            seg_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
+                                                                  packed, tab, a, w, 1);
+    }
+    return ss::check_launch();
+}
+
+// Run the segment copy for params [pa, pb), windowing the pointer table.
+int run_segments(const ss_plan* p, int dir, int pa, int pb, unsigned char* packed,
+                 void* const* ptrs, int n_out, cudaStream_t st) {
+    const int n_ptr = (pb - pa) * n_out;
+    if (n_ptr <= kTabSmall) return launch_window<kTabSmall>(p, dir, pa, pb, packed, ptrs, n_out, st);
+    const int w = kTabBig / n_out;
+    for (int a = pa; a < pb; a += w) {
+        int b = a + w < pb ? a + w : pb;
+        int rc = launch_window<kTabBig>(p, dir, a, b, packed, ptrs, n_out, st);
+        if (rc) return rc;
+    }
+    return SS_OK;
+}
+
+int check_param_ptrs(const ss_plan* p, int pa, int pb, void* const* ptrs, int n_out) {
+    for (int j = 0; j < n_out; ++j)
+        for (int i = pa; i < pb; ++i) {
+            const void* q = ptrs[(size_t)j * p->n + i];
+            if (p->numel[i] == 0) continue;
+            if (!q) return SS_EINVAL;
+            if (!ss::aligned(q, (uintptr_t)p->eb)) return SS_EALIGN;
+        }
+    return SS_OK;
+}
+
+void param_range(const ss_plan* p, int group, int* pa, int* pb) {
+    if (group < 0) {
+        *pa = 0;
+        *pb = p->n;
+    } else {
+        *pa = p->gfirst[group];
+        *pb = p->gfirst[group] + p->gnp[group];
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int fsdp_pack(const ss_plan* plan, const void* const* params, void* packed, int group,
+              ss_stream_t stream) {
+    if (!plan || !packed || (plan->n > 0 && !params)) return SS_EINVAL;
+    if (!plan->has_dev) return SS_ENODEVICE;
+    int64_t lo, hi;
+    if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;
+    if (!ss::aligned(packed, 16)) return SS_EALIGN;
+    int pa, pb;
+    param_range(plan, group, &pa, &pb);
+    int rc = check_param_ptrs(plan, pa, pb, const_cast<void* const*>(params), 1);
+    if (rc) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    rc = run_segments(plan, 1, pa, pb, static_cast<unsigned char*>(packed),
+                      const_cast<void* const*>(params), 1, st);
+    if (rc) return rc;
+    // pads of the selected groups
+    const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
+    const int z_lo = plan->group_zero[ga], z_hi = plan->group_zero[gb];
+    if (z_hi > z_lo) {
+        const int64_t u_lo = plan->zero[z_lo].start;
+        const int64_t u_hi = plan->zero[z_hi - 1].start + plan->zero[z_hi - 1].len;
+        const int grid = copy_grid(u_hi - u_lo);
+        if (plan->eb == 2)
+            zero_fill_kernel<2><<<grid, kThreads, 0, st>>>(plan->d_zero, z_lo, z_hi, u_lo, u_hi,
+                                                           static_cast<unsigned char*>(packed));
+        else
+            zero_fill_kernel<4><<<grid, kThreads, 0, st>>>(plan->d_zero, z_lo, z_hi, u_lo, u_hi,
+                                                           static_cast<unsigned char*>(packed));
+        rc = ss::check_launch();
+    }
+    return rc;
+}
+
+int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards, void* const* params_out,
+                           int n_out, int group, ss_stream_t stream) {
+    if (!plan || !param_shards || (plan->n > 0 && !params_out)) return SS_EINVAL;
+    if (n_out < 1 || n_out > SS_MAX_REPLICAS) return SS_EINVAL;
+    if (!plan->has_dev) return SS_ENODEVICE;
+    int64_t lo, hi;
+    if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;
+    if (!ss::aligned(param_shards, 16)) return SS_EALIGN;
+    int pa, pb;
+    param_range(plan, group, &pa, &pb);
+    int rc = check_param_ptrs(plan, pa, pb, params_out, n_out);
+    if (rc) return rc;
+    return run_segments(plan, 0, pa, pb,
+                        static_cast<unsigned char*>(const_cast<void*>(param_shards)), params_out,
+                        n_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// internal.h -- host-side plan object and helpers shared by the library's
+// translation units (never installed; the public ABI is include/shardstate.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "shardstate.h"
+
+namespace ss {
+
+// One contiguous run of parameter elements inside the packed layout.
+//   start       position in the segment table's iteration space (prefix sum
+//               of lengths); a CTA finds its first segment by binary search
+//               on it
+//   len         elements
+//   packed_off  element index in every packed buffer
+//   param_off   element index inside the parameter tensor (-1 param: zero fill)
+//   param       parameter index, or -1 for a pad run
+struct Seg {
+    int64_t start;
+    int64_t len;
+    int64_t packed_off;
+    int64_t param_off;
+    int32_t param;
+    int32_t reserved;
+};
+static_assert(sizeof(Seg) == 40, "Seg layout");
+
+}  // namespace ss
+
+struct ss_plan {
+    int kind = 0;
+    int N = 1;
+    int eb = 2;
+    int n = 0;
+    int G = 0;
+    std::vector<int64_t> dim0, inner, numel, chunk_rows;
+    std::vector<int64_t> offset;        // fsdp_plan_param_offset value
+    std::vector<int> param_group;
+    std::vector<int64_t> gbase, gshard;  // per group: base index, elements per rank
+    std::vector<int> gfirst, gnp;        // per group: first param, param count
+    int64_t shard_total = 0, total = 0, unpadded = 0;
+    // data segments sorted by (param, rank); param_seg[i] = first data segment of param i
+    std::vector<ss::Seg> data;
+    std::vector<int> param_seg;
+    // pad segments sorted by packed offset; group_zero[g] = first pad segment of group g
+    std::vector<ss::Seg> zero;
+    std::vector<int> group_zero;
+    // device copies
+    ss::Seg* d_data = nullptr;
+    ss::Seg* d_zero = nullptr;
+    int device = -1;
+    bool has_dev = false;
+};
+
+namespace ss {
+
+// Record a failed CUDA call for ss_last_cuda_error() and return SS_ECUDA.
+int cuda_fail(cudaError_t e);
+
+// Check the last launch; SS_OK or SS_ECUDA.  Counts the launch.
+int check_launch();
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Element range [lo, hi) of the packed buffers covered by `group` (-1 = all).
+inline bool group_range(const ss_plan* p, int group, int64_t* lo, int64_t* hi) {
+    if (group < 0) {
+        *lo = 0;
+        *hi = p->total;
+        return group == -1;
+    }
+    if (group >= p->G) return false;
+    *lo = p->gbase[group];
+    *hi = p->gbase[group] + (int64_t)p->N * p->gshard[group];
+    return true;
+}
+
+}  // namespace ss

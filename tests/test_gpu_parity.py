@@ -1,0 +1,378 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Layout, pack, all-gather + unpack, the reduce-scatter and the DDP average are
+compared bit for bit; AdamW state within the tolerances in tests/helpers.py
+(1e-6 relative to the operands' magnitude; bf16 parameters within one ulp).
+Small cases span many CTA ranges and ragged tails; the full-size cases run in
+the launch configuration the benchmark times and are checked on sampled
+elements (elementwise steps) or by whole-array comparison / round trip
+(copies).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.gpu_common import Setup, guarded, guards_intact, elem_bytes
+from tests.helpers import (check_adamw_state, check_bf16_within_one_ulp, to_np, from_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ss():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sharded_state_gb300 as ss
+    return ss
+
+
+def _hp_kwargs(step):
+    hp = W.adamw_hparams(step)
+    return {k: hp[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay")}
+
+
+def _small_sets():
+    sets = [("tiny_mlp_flat_true_N2", W.tiny_mlp(2, W.FLAT_ORIG_TRUE))]
+    for N in (3, 5, 7):
+        for dt in (torch.bfloat16, torch.float32):
+            tag = "bf16" if dt == torch.bfloat16 else "f32"
+            sets.append((f"awkward1d_false_N{N}_{tag}", W.awkward_1d(N, W.FLAT_ORIG_FALSE, dt)))
+            sets.append((f"awkward1d_true_N{N}_{tag}", W.awkward_1d(N, W.FLAT_ORIG_TRUE, dt)))
+            sets.append((f"awkward2d_perparam_N{N}_{tag}", W.awkward_2d(N, dtype=dt)))
+    # multi-group model with pads (N=3 does not divide the dims)
+    small_llama = W.llama_1b2(world_size=3, layers=3, hidden=40, ffn=72, vocab=100)
+    sets.append(("small_llama_groups_N3", small_llama))
+    sets.append(("small_llama_groups_N8", W.llama_1b2(world_size=8, layers=2, hidden=48,
+                                                       ffn=136, vocab=96)))
+    ex = W.ParamSet(["p1", "p2"], [(3,), (5,)], [2], 4, W.FLAT_ORIG_TRUE, torch.bfloat16, seed=9)
+    sets.append(("worked_example_3_5", ex))
+    big_n = W.ParamSet([f"p{i}" for i in range(5)], [(130, 3), (64,), (0, 4), (1,), (257, 2)], [5],
+                       64, W.PER_PARAM_DIM0, torch.bfloat16, seed=10)
+    sets.append(("per_param_N64", big_n))
+    return sets
+
+
+SMALL = _small_sets()
+
+
+@pytest.mark.parametrize("name,ps", SMALL, ids=[s[0] for s in SMALL])
+def test_pack_is_bit_exact(ss, name, ps):
+    su = Setup(ss, ps)
+    packed, whole = guarded(su.total, ps.dtype)
+    ss.fsdp_pack(su.plan, su.params, packed)
+    torch.cuda.synchronize()
+    assert guards_intact(whole)
+    want = su.oracle_pack(su.params_np())
+    np.testing.assert_array_equal(to_np(packed).view(np.uint8), want.view(np.uint8))
+
+
+@pytest.mark.parametrize("name,ps", SMALL, ids=[s[0] for s in SMALL])
+def test_all_gather_unpack_is_bit_exact(ss, name, ps):
+    su = Setup(ss, ps)
+    g = torch.Generator().manual_seed(123)
+    if ps.dtype == torch.bfloat16:
+        shards_cpu = torch.randint(-32768, 32767, (su.total,), generator=g,
+                                   dtype=torch.int16).view(torch.bfloat16)
+    else:
+        shards_cpu = torch.randn(su.total, generator=g)
+    shards = shards_cpu.cuda()
+    for n_out in sorted({1, min(ps.world_size, 9)}):
+        outs, wholes = [], []
+        for j in range(n_out):
+            for p in su.params:
+                o, w = guarded(p.numel(), ps.dtype)
+                outs.append(o)
+                wholes.append(w)
+        ss.fsdp_all_gather_unpack(su.plan, shards, outs, n_out=n_out)
+        torch.cuda.synchronize()
+        assert all(guards_intact(w) for w in wholes)
+        want = su.oracle_unpack(to_np(shards_cpu), n_out=n_out)
+        n = len(su.params)
+        for j in range(n_out):
+            for i in range(n):
+                np.testing.assert_array_equal(to_np(outs[j * n + i]).view(np.uint8),
+                                              want[j][i].view(np.uint8))
+
+
+@pytest.mark.parametrize("name,ps", SMALL, ids=[s[0] for s in SMALL])
+def test_reduce_scatter_adamw_three_steps(ss, name, ps):
+    su = Setup(ss, ps)
+    N, total, dt = su.N, su.total, ps.dtype
+    # parameters -> shards (GPU pack, already checked bit-exact) and fp32 state
+    shards = torch.empty(total, dtype=dt, device="cuda")
+    ss.fsdp_pack(su.plan, su.params, shards)
+    master = torch.empty(total, dtype=torch.float32, device="cuda")
+    m = torch.empty_like(master)
+    v = torch.empty_like(master)
+    ss.fsdp_init_master(su.plan, shards, master, m, v)
+    torch.cuda.synchronize()
+    o_master, o_m, o_v = oracle.init_master(to_np(shards))
+    np.testing.assert_array_equal(to_np(master), o_master)
+    assert not to_np(m).any() and not to_np(v).any()
+
+    rank_grads_cpu = W.make_rank_grads(ps)
+    packed = []
+    for r in range(N):
+        buf = torch.empty(total, dtype=dt, device="cuda")
+        ss.fsdp_pack(su.plan, [g.cuda() for g in rank_grads_cpu[r]], buf)
+        packed.append(buf)
+    torch.cuda.synchronize()
+    for r in range(N):
+        want = su.oracle_pack([to_np(g) for g in rank_grads_cpu[r]])
+        np.testing.assert_array_equal(to_np(packed[r]).view(np.uint8), want.view(np.uint8))
+    packed_np = [to_np(b) for b in packed]
+
+    for step in (1, 2, 3):
+        prev_master, prev_m, prev_v = to_np(master), to_np(m), to_np(v)
+        reduced, whole_red = guarded(total, torch.float32)
+        hp = ss.adamw_params(step=step, **_hp_kwargs(step))
+        ss.fsdp_reduce_scatter_adamw(su.plan, packed, master, m, v, shards, hp, reduced)
+        torch.cuda.synchronize()
+        assert guards_intact(whole_red)
+        # oracle on the GPU's previous state (one-step parity)
+        om, omm, ov = prev_master.copy(), prev_m.copy(), prev_v.copy()
+        c = su.info.shard_numel
+        o_params, o_red = oracle.reduce_scatter_adamw(N, c, packed_np, om, omm, ov, step=step,
+                                                      **_hp_kwargs(step))
+        np.testing.assert_array_equal(to_np(reduced), o_red)          # bit-exact RS
+        check_adamw_state(to_np(master), to_np(m), to_np(v), om, omm, ov, prev_master, prev_m,
+                          o_red)
+        if dt == torch.bfloat16:
+            check_bf16_within_one_ulp(to_np(shards), o_params)
+        else:
+            np.testing.assert_array_equal(to_np(shards), to_np(master))
+    # pads still zero after three steps: unpack + pack reproduces the shards exactly
+    outs = [torch.empty_like(p) for p in su.params]
+    ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+    repacked = torch.empty_like(shards)
+    ss.fsdp_pack(su.plan, outs, repacked)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(repacked).view(np.uint8), to_np(shards).view(np.uint8))
+
+
+def test_per_group_calls_equal_whole_plan_calls(ss):
+    ps = W.llama_1b2(world_size=3, layers=4, hidden=40, ffn=72, vocab=100)
+    su = Setup(ss, ps)
+    N, total = su.N, su.total
+    grads = [torch.randn(total, device="cuda").to(torch.bfloat16) for _ in range(N)]
+    base_shards = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+    ss.fsdp_pack(su.plan, su.params, base_shards)
+    results = []
+    for mode in ("whole", "groups"):
+        shards = base_shards.clone()
+        master = torch.empty(total, device="cuda")
+        m = torch.empty_like(master)
+        v = torch.empty_like(master)
+        red = torch.empty_like(master)
+        outs = [torch.empty_like(p) for p in su.params]
+        repacked = torch.empty_like(shards)
+        hp = ss.adamw_params(step=1)
+        if mode == "whole":
+            ss.fsdp_init_master(su.plan, shards, master, m, v)
+            ss.fsdp_reduce_scatter_adamw(su.plan, grads, master, m, v, shards, hp, red)
+            ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+            ss.fsdp_pack(su.plan, outs, repacked)
+        else:
+            for g in range(len(su.groups)):
+                ss.fsdp_init_master(su.plan, shards, master, m, v, group=g)
+                ss.fsdp_reduce_scatter_adamw(su.plan, grads, master, m, v, shards, hp, red, group=g)
+                ss.fsdp_all_gather_unpack(su.plan, shards, outs, group=g)
+                ss.fsdp_pack(su.plan, outs, repacked, group=g)
+        torch.cuda.synchronize()
+        results.append([to_np(t) for t in [shards, master, m, v, red, repacked] + outs])
+    for a, b in zip(*results):
+        np.testing.assert_array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_unaligned_group_ranges_use_scalar_head_and_tail(ss):
+    # groups whose base is not a multiple of 8 elements exercise the scalar head/tail path
+    ps = W.ParamSet([f"p{i}" for i in range(4)], [(5,), (3,), (11,), (2,)], [1, 1, 1, 1], 3,
+                    W.FLAT_ORIG_FALSE, torch.bfloat16, seed=5)
+    su = Setup(ss, ps)
+    N, total = su.N, su.total
+    grads = [torch.randn(total, device="cuda").to(torch.bfloat16) for _ in range(N)]
+    red = torch.zeros(total, device="cuda")
+    for g in range(4):
+        ss.fsdp_reduce_scatter_adamw(su.plan, grads, None, None, None, None, None, red, group=g)
+    torch.cuda.synchronize()
+    want = oracle.reduce_scatter(N, su.info.shard_numel, [to_np(x) for x in grads])
+    # RS is element-wise over the packed index, so per-group RS over all groups == whole RS
+    np.testing.assert_array_equal(to_np(red), want)
+
+
+def test_fp32_shards_equal_master(ss):
+    ps = W.awkward_1d(5, W.FLAT_ORIG_TRUE, torch.float32, count=20, max_len=300)
+    su = Setup(ss, ps)
+    shards = torch.empty(su.total, device="cuda")
+    ss.fsdp_pack(su.plan, su.params, shards)
+    master = torch.empty_like(shards)
+    m = torch.empty_like(shards)
+    v = torch.empty_like(shards)
+    ss.fsdp_init_master(su.plan, shards, master, m, v)
+    grads = [torch.randn(su.total, device="cuda") for _ in range(5)]
+    ss.fsdp_reduce_scatter_adamw(su.plan, grads, master, m, v, shards, ss.adamw_params())
+    torch.cuda.synchronize()
+    assert torch.equal(shards, master)
+
+
+# ---------------------------------------------------------------------------
+# full sizes, launch configuration of the benchmark
+# ---------------------------------------------------------------------------
+
+def _sampled_rs_adamw_check(ss, su, grads, shards, master, m, v, step, samples=1 << 20):
+    """One RS+AdamW step over the whole plan, checked on a random sample of elements
+    (both steps are element-wise over the packed index, so the oracle computes the
+    sampled elements from the gathered inputs exactly as it would in place)."""
+    N, total = su.N, su.total
+    gen = torch.Generator(device="cuda").manual_seed(77)
+    k = (min(samples, total) // N) * N
+    idx = torch.randint(0, total, (k,), device="cuda", generator=gen)
+    in_master = master[idx].cpu().numpy().copy()
+    in_m = m[idx].cpu().numpy().copy()
+    in_v = v[idx].cpu().numpy().copy()
+    in_g = [to_np(gr[idx]) for gr in grads]
+    red = torch.empty(total, device="cuda")
+    hp = ss.adamw_params(step=step)
+    ss.fsdp_reduce_scatter_adamw(su.plan, grads, master, m, v, shards, hp, red)
+    torch.cuda.synchronize()
+    om, omm, ov = in_master.copy(), in_m.copy(), in_v.copy()
+    o_params, o_red = oracle.reduce_scatter_adamw(N, k // N, in_g, om, omm, ov, step=step,
+                                                  **_hp_kwargs(step))
+    np.testing.assert_array_equal(red[idx].cpu().numpy(), o_red)
+    check_adamw_state(master[idx].cpu().numpy(), m[idx].cpu().numpy(), v[idx].cpu().numpy(), om,
+                      omm, ov, in_master, in_m, o_red)
+    check_bf16_within_one_ulp(to_np(shards[idx]), o_params)
+
+
+def _full_size_setup(ss, ps):
+    su = Setup(ss, ps, make_values=False)
+    total, N = su.total, su.N
+    shards = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(ps.seed)
+    shards.copy_((torch.randn(total, device="cuda", generator=gen) * ps.param_std))
+    master = torch.empty(total, device="cuda")
+    m = torch.empty_like(master)
+    v = torch.empty_like(master)
+    ss.fsdp_init_master(su.plan, shards, master, m, v)
+    grads = W.make_packed_rank_grads(N, total, ps.grad_std, ps.seed, device="cuda")
+    return su, shards, master, m, v, grads
+
+
+def test_llama_block_4096_full_size(ss):
+    ps = W.llama_block_4096()
+    su, shards, master, m, v, grads = _full_size_setup(ss, ps)
+    for step in (1, 2):
+        _sampled_rs_adamw_check(ss, su, grads, shards, master, m, v, step)
+    # all-gather + unpack, whole arrays against the oracle
+    outs = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in ps.shapes]
+    ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+    torch.cuda.synchronize()
+    want = su.oracle_unpack(to_np(shards))[0]
+    for o, w in zip(outs, want):
+        np.testing.assert_array_equal(to_np(o), w)
+    del grads
+    torch.cuda.empty_cache()
+
+
+def test_llama_1b2_full_size(ss):
+    ps = W.llama_1b2()
+    su, shards, master, m, v, grads = _full_size_setup(ss, ps)
+    assert su.total == 1_364_297_728
+    _sampled_rs_adamw_check(ss, su, grads, shards, master, m, v, step=1, samples=1 << 21)
+    # all-gather + unpack: round trip at full size, oracle on the root group's small
+    # norm and on one block group in full
+    outs = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in ps.shapes]
+    ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+    repacked = torch.empty_like(shards)
+    ss.fsdp_pack(su.plan, outs, repacked)
+    torch.cuda.synchronize()
+    assert torch.equal(repacked.view(torch.int16), shards.view(torch.int16))
+    g = 5
+    grp = su.groups[g]
+    base, span = grp["base"], su.N * grp["shard_numel"]
+    a, b = grp["first_param"], grp["first_param"] + grp["num_params"]
+    want = oracle.all_gather_unpack(su.kind, su.N, 2, su.d0[a:b], su.inner[a:b],
+                                    to_np(shards[base:base + span]))[0]
+    for i, w in zip(range(a, b), want):
+        np.testing.assert_array_equal(to_np(outs[i]), w)
+    del grads, outs, repacked
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# DDP
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cap", [64 << 10, 1 << 20, 25 << 20, 1 << 30])
+def test_ddp_bucket_average_bit_exact(ss, cap):
+    ds = W.ddp_grads(world_size=8, n_small=70, small=2048, n_large=6, large=65536 + 8, seed=3)
+    grads = W.make_ddp_grads(ds, device="cuda")
+    outs, wholes = [], []
+    for n in ds.numels:
+        o, w = guarded(n, torch.bfloat16)
+        outs.append(o)
+        wholes.append(w)
+    nb = ss.ddp_bucket_pack_average(grads, cap, outs)
+    torch.cuda.synchronize()
+    assert all(guards_intact(w) for w in wholes)
+    assert nb == oracle.ddp_buckets(ds.numels, 2, cap)[1]
+    want = oracle.ddp_average([[to_np(g) for g in rank] for rank in grads])
+    for o, w in zip(outs, want):
+        np.testing.assert_array_equal(to_np(o), w)
+
+
+def test_ddp_misaligned_and_odd_sizes(ss):
+    # views offset by one element: pointers congruent across ranks, and not
+    rng = np.random.default_rng(1)
+    N = 5
+    numels = [1, 7, 9, 300, 0, 1025]
+    bases = [[torch.randn(n + 3, device="cuda").to(torch.bfloat16) for n in numels] for _ in range(N)]
+    grads = [[b[(r + t) % 2: (r + t) % 2 + n] for t, (b, n) in enumerate(zip(bases[r], numels))]
+             for r in range(N)]
+    outs = [torch.empty(n + 1, dtype=torch.bfloat16, device="cuda")[1:] for n in numels]
+    ss.ddp_bucket_pack_average(grads, 100, outs, numels=numels)
+    torch.cuda.synchronize()
+    want = oracle.ddp_average([[to_np(g) for g in rank] for rank in grads])
+    for o, w in zip(outs, want):
+        np.testing.assert_array_equal(to_np(o), w)
+
+
+# ---------------------------------------------------------------------------
+# errors come back as status codes, nothing launched
+# ---------------------------------------------------------------------------
+
+def test_device_argument_errors(ss):
+    ps = W.tiny_mlp()
+    su = Setup(ss, ps)
+    packed = torch.empty(su.total + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ss.ShardStateError) as e:
+        ss.fsdp_pack(su.plan, su.params, packed[1:])
+    assert e.value.status == ss.SS_EALIGN
+    with pytest.raises(ss.ShardStateError) as e:
+        ss.fsdp_pack(su.plan, su.params, packed, group=3)
+    assert e.value.status == ss.SS_EINVAL
+    with pytest.raises(ss.ShardStateError) as e:
+        ss.fsdp_all_gather_unpack(su.plan, packed, su.params, n_out=0)
+    assert e.value.status == ss.SS_EINVAL
+    with pytest.raises(ss.ShardStateError) as e:
+        ss.fsdp_reduce_scatter_adamw(su.plan, [packed, packed], None, None, None, None, None, None)
+    assert e.value.status == ss.SS_EINVAL
+    bad = ss.adamw_params(step=0)
+    f = torch.empty(su.total, device="cuda")
+    with pytest.raises(ss.ShardStateError) as e:
+        ss.fsdp_reduce_scatter_adamw(su.plan, [packed, packed], f, f, f, packed, bad)
+    assert e.value.status == ss.SS_EINVAL
+    torch.cuda.synchronize()
+
+
+def test_empty_plan_is_a_no_op(ss):
+    plan = ss.fsdp_plan_create(ss.SS_PER_PARAM_DIM0, 4, 2, [0, 0], [3, 5])
+    assert plan.info().total_numel == 0
+    x = torch.empty(8, dtype=torch.bfloat16, device="cuda")
+    f = torch.empty(8, device="cuda")
+    ss.fsdp_pack(plan, [x, x], x)
+    ss.fsdp_reduce_scatter_adamw(plan, [x] * 4, f, f, f, x, ss.adamw_params())
+    ss.fsdp_all_gather_unpack(plan, x, [x, x])
+    torch.cuda.synchronize()
