@@ -15,7 +15,7 @@ import torch
 import oracle
 import workloads as W
 from tests.gpu_common import Setup, guarded, guards_intact, elem_bytes
-from tests.helpers import (check_adamw_state, check_bf16_within_one_ulp, to_np, from_np)
+from tests.helpers import check_adamw_state, check_bf16_params, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -140,7 +140,7 @@ def test_reduce_scatter_adamw_three_steps(ss, name, ps):
         check_adamw_state(to_np(master), to_np(m), to_np(v), om, omm, ov, prev_master, prev_m,
                           o_red)
         if dt == torch.bfloat16:
-            check_bf16_within_one_ulp(to_np(shards), o_params)
+            check_bf16_params(to_np(shards), o_params, to_np(master), om, prev_master)
         else:
             np.testing.assert_array_equal(to_np(shards), to_np(master))
     # pads still zero after three steps: unpack + pack reproduces the shards exactly
@@ -243,7 +243,7 @@ def _sampled_rs_adamw_check(ss, su, grads, shards, master, m, v, step, samples=1
     np.testing.assert_array_equal(red[idx].cpu().numpy(), o_red)
     check_adamw_state(master[idx].cpu().numpy(), m[idx].cpu().numpy(), v[idx].cpu().numpy(), om,
                       omm, ov, in_master, in_m, o_red)
-    check_bf16_within_one_ulp(to_np(shards[idx]), o_params)
+    check_bf16_params(to_np(shards[idx]), o_params, master[idx].cpu().numpy(), om, in_master)
 
 
 def _full_size_setup(ss, ps):
