@@ -56,7 +56,8 @@ enum {
     SS_EOVERFLOW = -3, /* a size overflows int64 / the index types */
     SS_ENOMEM = -4,    /* host or device allocation failed */
     SS_ECUDA = -5,     /* a CUDA runtime call failed (ss_last_cuda_error) */
-    SS_ENODEVICE = -6  /* the plan has no device metadata (created host-only) */
+    SS_ENODEVICE = -6, /* the plan has no device metadata (created host-only) */
+    SS_ESCRATCH = -7   /* the call needs more than the library's fixed scratch array */
 };
 
 /* Largest N (virtual ranks) the kernels accept. */
@@ -292,6 +293,38 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards,
 int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* numels,
                             const void* const* rank_grads, size_t bucket_cap_bytes,
                             void* const* avg_out, int* num_buckets_out, ss_stream_t stream);
+
+/*
+ * Allocation-free variant of ddp_bucket_pack_average.  No counterpart on the
+ * pages: it exists for callers that cannot call cudaMalloc or
+ * cudaMallocAsync -- a host framework that owns every byte of device memory
+ * through its own allocator and forbids allocations behind its back, a
+ * latency-critical loop that must not risk an allocation that grows a memory
+ * pool or synchronises, or a process running so close to its device-memory
+ * limit that an allocation could fail in the middle of a step.
+ *
+ * Same arguments, arithmetic, bucket order and launches as
+ * ddp_bucket_pack_average; only the per-call table of pointers and sizes
+ * lives in a fixed array inside the library (a static __device__ array of
+ * SS_DDP_NOALLOC_TABLE_BYTES that every GPU loading the library holds until
+ * the process exits) instead of a cudaMallocAsync allocation.  The table
+ * takes 8 * (num_tensors + 1) + 8 * num_tensors * (world_size + 1) bytes; a
+ * call that needs more returns SS_ESCRATCH before doing anything.
+ *
+ * The call allocates no device memory and calls no allocating library
+ * routine.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call overwrites the whole
+ * table it uses, so nothing has to be cleared between calls, but all calls
+ * share the one array: calls whose work can overlap on the GPU (different
+ * streams without ordering between them, or several host threads) race on
+ * it and must be serialised by the caller.
+ */
+#define SS_DDP_NOALLOC_TABLE_BYTES (256u * 1024u)
+int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors, const int64_t* numels,
+                                    const void* const* rank_grads, size_t bucket_cap_bytes,
+                                    void* const* avg_out, int* num_buckets_out,
+                                    ss_stream_t stream);
 
 /* Bucket assignment only (host, no device work): bucket_of[t] receives
  * tensor t's bucket, numbered in launch order.  Returns the bucket count, or

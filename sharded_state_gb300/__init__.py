@@ -25,6 +25,8 @@ SS_EOVERFLOW = -3
 SS_ENOMEM = -4
 SS_ECUDA = -5
 SS_ENODEVICE = -6
+SS_ESCRATCH = -7
+SS_DDP_NOALLOC_TABLE_BYTES = 256 * 1024
 
 SS_FLAT_ORIG_FALSE = 0
 SS_FLAT_ORIG_TRUE = 1
@@ -38,7 +40,7 @@ EXPORTED = ("fsdp_plan_create", "fsdp_plan_layout", "fsdp_plan_info", "fsdp_plan
             "fsdp_plan_group", "fsdp_plan_destroy", "fsdp_pack", "fsdp_init_master",
             "fsdp_reduce_scatter_adamw", "fsdp_all_gather_unpack", "ddp_bucket_pack_average",
             "ddp_bucket_assign", "ss_strerror", "ss_last_cuda_error", "ss_version",
-            "ss_launch_count")
+            "ss_launch_count", "ddp_bucket_pack_average_noalloc")
 
 
 class ShardStateError(RuntimeError):
@@ -93,6 +95,8 @@ def _load() -> ctypes.CDLL:
         "fsdp_all_gather_unpack": ([vp, vp, vpp, i32, i32, vp], i32),
         "ddp_bucket_pack_average": ([i32, i32, i64p, vpp, ctypes.c_size_t, vpp,
                                      ctypes.POINTER(i32), vp], i32),
+        "ddp_bucket_pack_average_noalloc": ([i32, i32, i64p, vpp, ctypes.c_size_t, vpp,
+                                             ctypes.POINTER(i32), vp], i32),
         "ddp_bucket_assign": ([i32, i64p, i32, ctypes.c_size_t, ctypes.POINTER(i32)], i32),
         "ss_strerror": ([i32], ctypes.c_char_p),
         "ss_last_cuda_error": ([], i32),
@@ -306,6 +310,26 @@ def ddp_bucket_pack_average(rank_grads: Sequence[Sequence], bucket_cap_bytes: in
     flat = [g for rank in rank_grads for g in rank]
     nb = ctypes.c_int()
     _check("ddp_bucket_pack_average", _lib.ddp_bucket_pack_average(
+        N, T, _i64_array(numels), _ptr_array(flat), bucket_cap_bytes, _ptr_array(avg_out),
+        ctypes.byref(nb), _stream(stream)))
+    return nb.value
+
+
+def ddp_bucket_pack_average_noalloc(rank_grads: Sequence[Sequence], bucket_cap_bytes: int,
+                                    avg_out: Sequence, numels: Optional[Sequence[int]] = None,
+                                    stream=None) -> int:
+    """Same as ddp_bucket_pack_average, for callers that cannot allocate device
+    memory: the library's fixed device array holds the per-call table (at most
+    SS_DDP_NOALLOC_TABLE_BYTES; larger requests raise with SS_ESCRATCH).  Calls
+    share that array, so calls that could overlap on the GPU must be ordered by
+    the caller.  Returns the bucket count."""
+    N = len(rank_grads)
+    T = len(avg_out)
+    if numels is None:
+        numels = [int(t.numel()) for t in avg_out]
+    flat = [g for rank in rank_grads for g in rank]
+    nb = ctypes.c_int()
+    _check("ddp_bucket_pack_average_noalloc", _lib.ddp_bucket_pack_average_noalloc(
         N, T, _i64_array(numels), _ptr_array(flat), bucket_cap_bytes, _ptr_array(avg_out),
         ctypes.byref(nb), _stream(stream)))
     return nb.value

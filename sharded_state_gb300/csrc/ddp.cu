@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "device_utils.cuh"
@@ -240,3 +241,108 @@ int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* nume
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// allocation-free variant: the per-call table lives in a fixed device array
+// ---------------------------------------------------------------------------
+
+// Scratch for ddp_bucket_pack_average_noalloc: prefix sums then pointers, as
+// the allocating entry point lays out its table.  Shared by every call.
+static __device__ __align__(256) unsigned char g_ddp_noalloc_table[SS_DDP_NOALLOC_TABLE_BYTES];
+
+namespace {
+
+constexpr int kMaxDevicesNoalloc = 64;
+
+// Device address of the array, looked up once per device (host code cannot use
+// the symbol itself: on the host it names a stand-in, not device memory).
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevicesNoalloc] = {nullptr};
+
+int noalloc_table_address(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return ss::cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevicesNoalloc) return SS_EINVAL;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_ddp_noalloc_table);
+        if (e != cudaSuccess) return ss::cuda_fail(e);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return SS_OK;
+}
+
+}  // namespace
+
+extern "C" int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors,
+                                               const int64_t* numels,
+                                               const void* const* rank_grads,
+                                               size_t bucket_cap_bytes, void* const* avg_out,
+                                               int* num_buckets_out, ss_stream_t stream) {
+    if (world_size < 1 || world_size > SS_MAX_WORLD || num_tensors < 0) return SS_EINVAL;
+    if (num_tensors > 0 && (!numels || !rank_grads || !avg_out)) return SS_EINVAL;
+    if (bucket_cap_bytes == 0) return SS_EINVAL;
+    const int N = world_size, T = num_tensors;
+    const size_t n_prefix = (size_t)T + 1;
+    const size_t n_ptrs = (size_t)T * (size_t)(N + 1);
+    const size_t table_bytes = n_prefix * 8 + n_ptrs * 8;
+    if (table_bytes > SS_DDP_NOALLOC_TABLE_BYTES) return SS_ESCRATCH;
+    for (int t = 0; t < T; ++t) {
+        if (numels[t] < 0 || numels[t] > ((int64_t)1 << 60)) return SS_EINVAL;
+        if (numels[t] == 0) continue;
+        if (!avg_out[t]) return SS_EINVAL;
+        if (!ss::aligned(avg_out[t], 2)) return SS_EALIGN;
+        for (int r = 0; r < N; ++r) {
+            const void* q = rank_grads[(size_t)r * T + t];
+            if (!q) return SS_EINVAL;
+            if (!ss::aligned(q, 2)) return SS_EALIGN;
+        }
+    }
+    void* d_table = nullptr;
+    int rc = noalloc_table_address(&d_table);
+    if (rc) return rc;
+
+    std::vector<int> bucket_of((size_t)(T > 0 ? T : 1));
+    const int nb = ddp_bucket_assign(T, numels, 2, bucket_cap_bytes, bucket_of.data());
+    if (nb < 0) return nb;
+    if (num_buckets_out) *num_buckets_out = nb;
+    if (nb == 0) return SS_OK;
+
+    // table in bucket order (reverse registration order): prefix[T+1] then ptrs[T][N+1]
+    std::vector<unsigned char> host(table_bytes);
+    int64_t* prefix = reinterpret_cast<int64_t*>(host.data());
+    const void** ptrs = reinterpret_cast<const void**>(host.data() + n_prefix * 8);
+    std::vector<int> bucket_start((size_t)nb + 1, 0);
+    prefix[0] = 0;
+    for (int o = 0; o < T; ++o) {
+        const int t = T - 1 - o;
+        prefix[o + 1] = prefix[o] + numels[t];
+        for (int r = 0; r < N; ++r) ptrs[(size_t)o * (N + 1) + r] = rank_grads[(size_t)r * T + t];
+        ptrs[(size_t)o * (N + 1) + N] = avg_out[t];
+        if (o == 0 || bucket_of[t] != bucket_of[t + 1]) bucket_start[bucket_of[t]] = o;
+    }
+    bucket_start[nb] = T;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(d_table, host.data(), table_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return ss::cuda_fail(e);
+    const int64_t* d_prefix = static_cast<const int64_t*>(d_table);
+    const void* const* d_ptrs =
+        reinterpret_cast<const void* const*>(static_cast<unsigned char*>(d_table) + n_prefix * 8);
+    DdpKernel fn = pick(N);
+    const int64_t cap = (int64_t)ss::num_sms() * 4;
+    for (int b = 0; b < nb; ++b) {
+        const int o_lo = bucket_start[b], o_hi = bucket_start[b + 1];
+        const int64_t elems = prefix[o_hi] - prefix[o_lo];
+        if (elems == 0) continue;
+        int64_t want = (elems + 4095) / 4096;
+        const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+        fn<<<grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
+        rc = ss::check_launch();
+        if (rc) return rc;
+    }
+    return SS_OK;
+}

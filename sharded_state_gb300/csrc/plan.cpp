@@ -345,6 +345,7 @@ const char* ss_strerror(int s) {
         case SS_ENOMEM: return "out of memory";
         case SS_ECUDA: return "CUDA runtime error";
         case SS_ENODEVICE: return "plan has no device metadata";
+        case SS_ESCRATCH: return "request exceeds the fixed scratch array";
         default: return "unknown status";
     }
 }
