@@ -12,8 +12,10 @@
 // each tensor in the bucket, read N bf16 values, sum in fp32 in rank order,
 // divide by N, round to bf16 and write the average (2N + 2 bytes per
 // element).  One kernel launch per bucket keeps the per-collective fixed cost
-// visible.  The per-tensor pointers and the bucket-order prefix sums of the
-// sizes go to the device in a per-call table.
+// visible; inside a bucket one CTA averages one 4096-element tile, finding its
+// first tensor with a warp-level search over the bucket-order prefix sums of
+// the tensor sizes.  The per-tensor pointers and those prefix sums go to the
+// device in a per-call table.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -105,27 +107,39 @@ __device__ __forceinline__ void avg_piece(const void* const* ptrs, int N, int64_
     if (tid < k1 - done) out[done + tid] = mean1(ptrs, N, done + tid);
 }
 
+// Last index o in [lo, hi) with prefix[o] <= u (prefix non-decreasing,
+// prefix[lo] <= u), found by one warp with a 32-ary search: each round the 32
+// lanes probe evenly spaced entries and a ballot keeps the last one <= u.
+// Every lane of the warp returns the same index.
+__device__ __forceinline__ int warp_find(const int64_t* __restrict__ prefix, int lo, int hi,
+                                         int64_t u) {
+    const int lane = threadIdx.x & 31;
+    while (hi - lo > 1) {
+        const int stride = (hi - lo + 31) / 32;
+        const int idx = lo + lane * stride;
+        const bool le = idx < hi && prefix[idx] <= u;
+        const unsigned ballot = __ballot_sync(0xFFFFFFFFu, le);
+        const int last = 31 - __clz(ballot);  // lane 0 probes lo, so ballot != 0
+        lo += last * stride;
+        hi = lo + stride < hi ? lo + stride : hi;
+    }
+    return lo;
+}
+
 // One bucket: tensors [o_lo, o_hi) of the bucket-ordered table; prefix[o] is
-// the element offset of tensor o in bucket order.
+// the element offset of tensor o in bucket order.  CTA b averages bucket
+// elements [b*T, (b+1)*T) (T = kTile), walking the tensors that cover them.
+constexpr int64_t kTile = 4096;
+
 template <int NR>
 __global__ void __launch_bounds__(kThreads)
 ddp_bucket_kernel(const int64_t* __restrict__ prefix, const void* const* __restrict__ ptrs, int N,
                   int o_lo, int o_hi) {
     const int64_t u_lo = prefix[o_lo], u_hi = prefix[o_hi];
-    const int64_t span = u_hi - u_lo;
-    int64_t per = (span + gridDim.x - 1) / gridDim.x;
-    per = (per + 63) / 64 * 64;
-    int64_t u = u_lo + per * blockIdx.x;
-    const int64_t u_end = u + per < u_hi ? u + per : u_hi;
+    int64_t u = u_lo + (int64_t)blockIdx.x * kTile;
+    const int64_t u_end = u + kTile < u_hi ? u + kTile : u_hi;
     if (u >= u_end) return;
-    // last tensor in [o_lo, o_hi) whose prefix <= u
-    int lo = o_lo, hi = o_hi;
-    while (hi - lo > 1) {
-        int mid = lo + ((hi - lo) >> 1);
-        if (prefix[mid] <= u) lo = mid;
-        else hi = mid;
-    }
-    int o = lo;
+    int o = warp_find(prefix, o_lo, o_hi, u);
     while (u < u_end && o < o_hi) {
         const int64_t t_end = prefix[o + 1];
         const int64_t piece_end = t_end < u_end ? t_end : u_end;
@@ -225,14 +239,16 @@ int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* nume
     const void* const* d_ptrs =
         reinterpret_cast<const void* const*>(static_cast<unsigned char*>(d_table) + n_prefix * 8);
     DdpKernel fn = pick(N);
-    const int64_t cap = (int64_t)ss::num_sms() * 4;
     for (int b = 0; rc == SS_OK && b < nb; ++b) {
         const int o_lo = bucket_start[b], o_hi = bucket_start[b + 1];
         const int64_t elems = prefix[o_hi] - prefix[o_lo];
         if (elems == 0) continue;
-        int64_t want = (elems + 4095) / 4096;
-        const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-        fn<<<grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
+        const int64_t grid = (elems + kTile - 1) / kTile;
+        if (grid > 0x7FFFFFFF) {
+            rc = SS_EOVERFLOW;
+            break;
+        }
+        fn<<<(unsigned)grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
         rc = ss::check_launch();
     }
     cudaError_t ef = cudaFreeAsync(d_table, st);
@@ -333,14 +349,13 @@ extern "C" int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors,
     const void* const* d_ptrs =
         reinterpret_cast<const void* const*>(static_cast<unsigned char*>(d_table) + n_prefix * 8);
     DdpKernel fn = pick(N);
-    const int64_t cap = (int64_t)ss::num_sms() * 4;
     for (int b = 0; b < nb; ++b) {
         const int o_lo = bucket_start[b], o_hi = bucket_start[b + 1];
         const int64_t elems = prefix[o_hi] - prefix[o_lo];
         if (elems == 0) continue;
-        int64_t want = (elems + 4095) / 4096;
-        const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-        fn<<<grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
+        const int64_t grid = (elems + kTile - 1) / kTile;
+        if (grid > 0x7FFFFFFF) return SS_EOVERFLOW;
+        fn<<<(unsigned)grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
         rc = ss::check_launch();
         if (rc) return rc;
     }

@@ -1,18 +1,18 @@
 // gather.cu -- pack (per-parameter tensors -> sharded layout) and all-gather +
 // unpack (rank shards -> full per-parameter tensors).
 //
-// Both walk the plan's data-segment table: each segment is one contiguous run
+// Both use the plan's data-segment table: each segment is one contiguous run
 // of a parameter inside one rank's shard ("FSDP1 vs FSDP2", section 03: a
 // FlatParameter chunk may hold the tail of one parameter, pad and the head of
 // the next; FSDP2 rank r holds rows [r*c_i, (r+1)*c_i) of every parameter).
-// The segments are ordered by parameter then rank; their lengths define a
-// virtual iteration space U (the unpadded parameters back to back).  The grid
-// splits U into equal contiguous ranges, one per CTA; a CTA finds its first
-// segment by binary search over the segment starts and then walks segments,
-// copying each piece with 128-bit vectors whenever source and destination are
-// congruent mod 16 bytes (scalar element copies otherwise).  Pack also writes
-// zeros over the pad segments.  Pure data movement: HBM-bound, 2 + 2*n_out
-// bytes per bf16 element for the all-gather, 4 for pack (plus pad writes).
+// The planner splits every segment into 16 KiB tiles; one short-lived CTA
+// copies one tile (two dependent metadata loads, then 4 x 128-bit vectors per
+// thread in flight), and the grid is one CTA per tile, so all SMs stream
+// through a narrow, advancing window of HBM.  A piece moves in 128-bit vectors
+// whenever source and destination are congruent mod 16 bytes, element by
+// element otherwise.  Pack also writes zeros over the pad segments' tiles.
+// Pure data movement: HBM-bound, 2 + 2*n_out bytes per bf16 element for the
+// all-gather, 4 for pack (plus pad writes).
 //
 // Per-parameter pointers travel in the kernel parameters (up to kTabBig per
 // launch); more parameters x replicas than that are split into windows of
@@ -123,79 +123,63 @@ __device__ __forceinline__ void cta_zero(unsigned char* dst, int64_t nelem) {
     }
 }
 
-// This CTA's share [u0, u1) of [u_lo, u_hi): equal contiguous ranges, rounded
-// to 64 elements.
-__device__ __forceinline__ void cta_range(int64_t u_lo, int64_t u_hi, int64_t* u0, int64_t* u1) {
-    int64_t span = u_hi - u_lo;
-    int64_t per = (span + gridDim.x - 1) / gridDim.x;
-    per = (per + 63) / 64 * 64;
-    *u0 = u_lo + per * blockIdx.x;
-    *u1 = *u0 + per < u_hi ? *u0 + per : u_hi;
-}
-
-// dir 0: all-gather + unpack (packed -> params, n_out replicas)
-// dir 1: pack (params -> packed)
+// DIR 0: all-gather + unpack (packed -> params); DIR 1: pack (params -> packed).
+// DIR 2: all-gather + unpack with n_out > 1 replicas.
 template <int E, int CAP, int DIR>
 __global__ void __launch_bounds__(kThreads)
-seg_copy_kernel(const ss::Seg* __restrict__ segs, int s_lo, int s_hi, int64_t u_lo, int64_t u_hi,
-                unsigned char* packed, PtrTab<CAP> tab, int param_base, int ptr_stride,
-                int n_out) {
-    int64_t u, u_end;
-    cta_range(u_lo, u_hi, &u, &u_end);
-    if (u >= u_end) return;
-    int k = ss::find_seg(segs, s_lo, s_hi, u);
-    unsigned char* dsts[DIR == 0 ? 8 : 1];
-    while (u < u_end && k < s_hi) {
-        const ss::Seg sg = segs[k];
-        const int64_t seg_end = sg.start + sg.len;
-        const int64_t piece_end = seg_end < u_end ? seg_end : u_end;
-        const int64_t off = u - sg.start;
-        const int64_t len = piece_end - u;
-        const int slot = sg.param - param_base;
-        if (DIR == 0) {
-            const unsigned char* src = packed + (sg.packed_off + off) * E;
-            // replicas in batches of up to 8 destinations per pass over the source
-            for (int j0 = 0; j0 < n_out; j0 += 8) {
-                int nd = n_out - j0 < 8 ? n_out - j0 : 8;
-                for (int j = 0; j < nd; ++j)
-                    dsts[j] = static_cast<unsigned char*>(tab.p[(j0 + j) * ptr_stride + slot]) +
-                              (sg.param_off + off) * E;
-                cta_copy<E>(dsts, nd, src, len);
-            }
-        } else {
-            const unsigned char* src =
-                static_cast<const unsigned char*>(tab.p[slot]) + (sg.param_off + off) * E;
-            dsts[0] = packed + (sg.packed_off + off) * E;
-            cta_copy<E>(dsts, 1, src, len);
+tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
+                 unsigned char* packed, PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out) {
+    constexpr int64_t T = ss::kTileBytes / E;
+    const ss::Tile tl = tiles[t_lo + blockIdx.x];
+    const ss::Seg sg = segs[tl.seg];
+    const int64_t off = (int64_t)tl.idx * T;
+    const int64_t len = sg.len - off < T ? sg.len - off : T;
+    const int slot = sg.param - param_base;
+    if (DIR == 0) {
+        unsigned char* dst = static_cast<unsigned char*>(tab.p[slot]) + (sg.param_off + off) * E;
+        cta_copy<E>(&dst, 1, packed + (sg.packed_off + off) * E, len);
+    } else if (DIR == 2) {
+        unsigned char* dsts[8];
+        const unsigned char* src = packed + (sg.packed_off + off) * E;
+        // replicas in batches of up to 8 destinations per pass over the source
+        for (int j0 = 0; j0 < n_out; j0 += 8) {
+            const int nd = n_out - j0 < 8 ? n_out - j0 : 8;
+            for (int j = 0; j < nd; ++j)
+                dsts[j] = static_cast<unsigned char*>(tab.p[(j0 + j) * ptr_stride + slot]) +
+                          (sg.param_off + off) * E;
+            cta_copy<E>(dsts, nd, src, len);
         }
-        u = piece_end;
-        ++k;
+    } else {
+        unsigned char* dst = packed + (sg.packed_off + off) * E;
+        const unsigned char* src =
+            static_cast<const unsigned char*>(tab.p[slot]) + (sg.param_off + off) * E;
+        cta_copy<E>(&dst, 1, src, len);
     }
 }
 
 template <int E>
 __global__ void __launch_bounds__(kThreads)
-zero_fill_kernel(const ss::Seg* __restrict__ segs, int s_lo, int s_hi, int64_t u_lo, int64_t u_hi,
+zero_tile_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
                  unsigned char* packed) {
-    int64_t u, u_end;
-    cta_range(u_lo, u_hi, &u, &u_end);
-    if (u >= u_end) return;
-    int k = ss::find_seg(segs, s_lo, s_hi, u);
-    while (u < u_end && k < s_hi) {
-        const ss::Seg sg = segs[k];
-        const int64_t seg_end = sg.start + sg.len;
-        const int64_t piece_end = seg_end < u_end ? seg_end : u_end;
-        cta_zero<E>(packed + (sg.packed_off + (u - sg.start)) * E, piece_end - u);
-        u = piece_end;
-        ++k;
-    }
+    constexpr int64_t T = ss::kTileBytes / E;
+    const ss::Tile tl = tiles[t_lo + blockIdx.x];
+    const ss::Seg sg = segs[tl.seg];
+    const int64_t off = (int64_t)tl.idx * T;
+    const int64_t len = sg.len - off < T ? sg.len - off : T;
+    cta_zero<E>(packed + (sg.packed_off + off) * E, len);
 }
 
-int copy_grid(int64_t elems) {
-    int64_t want = (elems + 4095) / 4096;  // >= 16 KiB of bf16 per CTA
-    int64_t cap = (int64_t)ss::num_sms() * 4;
-    if (want < 1) want = 1;
-    return (int)(want < cap ? want : cap);
+// Launch one CTA per tile of [t_lo, t_hi), in chunks that respect the grid limit.
+template <typename Launch>
+int for_tile_chunks(int64_t t_lo, int64_t t_hi, Launch launch) {
+    constexpr int64_t kMaxGrid = (int64_t)1 << 30;
+    for (int64_t t = t_lo; t < t_hi; t += kMaxGrid) {
+        const int64_t n = t_hi - t < kMaxGrid ? t_hi - t : kMaxGrid;
+        launch(t, (unsigned)n);
+        int rc = ss::check_launch();
+        if (rc) return rc;
+    }
+    return SS_OK;
 }
 
 template <int CAP>
@@ -203,30 +187,35 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
                   void* const* ptrs, int n_out, cudaStream_t st) {
     const int s_lo = p->param_seg[a], s_hi = p->param_seg[b];
     if (s_hi <= s_lo) return SS_OK;
-    const int64_t u_lo = p->data[s_lo].start;
-    const int64_t u_hi = p->data[s_hi - 1].start + p->data[s_hi - 1].len;
+    const int64_t t_lo = p->data_seg_tile[s_lo], t_hi = p->data_seg_tile[s_hi];
     PtrTab<CAP> tab;
     std::memset(&tab, 0, sizeof tab);
     const int w = b - a;
     for (int j = 0; j < n_out; ++j)
         for (int i = a; i < b; ++i) tab.p[j * w + (i - a)] = ptrs[(size_t)j * p->n + i];
-    const int grid = copy_grid(u_hi - u_lo);
-    if (p->eb == 2) {
-        if (dir == 0)
-            seg_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
-                                                                  packed, tab, a, w, n_out);
-        else
-            seg_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
-                                                                  packed, tab, a, w, 1);
-    } else {
-        if (dir == 0)
-            seg_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
-                                                                  packed, tab, a, w, n_out);
-        else
-            seg_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data, s_lo, s_hi, u_lo, u_hi,
-                                                                  packed, tab, a, w, 1);
-    }
-    return ss::check_launch();
+    return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
+        if (p->eb == 2) {
+            if (dir == 0 && n_out > 1)
+                tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
+                                                                       packed, tab, a, w, n_out);
+            else if (dir == 0)
+                tile_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
+                                                                       packed, tab, a, w, 1);
+            else
+                tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
+                                                                       packed, tab, a, w, 1);
+        } else {
+            if (dir == 0 && n_out > 1)
+                tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
+                                                                       packed, tab, a, w, n_out);
+            else if (dir == 0)
+                tile_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
+                                                                       packed, tab, a, w, 1);
+            else
+                tile_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
+                                                                       packed, tab, a, w, 1);
+        }
+    });
 }
 
 // Run the segment copy for params [pa, pb), windowing the pointer table.
@@ -287,16 +276,14 @@ int fsdp_pack(const ss_plan* plan, const void* const* params, void* packed, int 
     const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
     const int z_lo = plan->group_zero[ga], z_hi = plan->group_zero[gb];
     if (z_hi > z_lo) {
-        const int64_t u_lo = plan->zero[z_lo].start;
-        const int64_t u_hi = plan->zero[z_hi - 1].start + plan->zero[z_hi - 1].len;
-        const int grid = copy_grid(u_hi - u_lo);
-        if (plan->eb == 2)
-            zero_fill_kernel<2><<<grid, kThreads, 0, st>>>(plan->d_zero, z_lo, z_hi, u_lo, u_hi,
-                                                           static_cast<unsigned char*>(packed));
-        else
-            zero_fill_kernel<4><<<grid, kThreads, 0, st>>>(plan->d_zero, z_lo, z_hi, u_lo, u_hi,
-                                                           static_cast<unsigned char*>(packed));
-        rc = ss::check_launch();
+        const int64_t t_lo = plan->zero_seg_tile[z_lo], t_hi = plan->zero_seg_tile[z_hi];
+        unsigned char* pk = static_cast<unsigned char*>(packed);
+        rc = for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
+            if (plan->eb == 2)
+                zero_tile_kernel<2><<<grid, kThreads, 0, st>>>(plan->d_zero_tiles, t, plan->d_zero, pk);
+            else
+                zero_tile_kernel<4><<<grid, kThreads, 0, st>>>(plan->d_zero_tiles, t, plan->d_zero, pk);
+        });
     }
     return rc;
 }

@@ -29,6 +29,16 @@ struct Seg {
 };
 static_assert(sizeof(Seg) == 40, "Seg layout");
 
+// Work unit of the copy kernels: one CTA moves one tile of kTileBytes inside
+// one segment.  Tile k of segment s covers elements [k*T, min((k+1)*T, len))
+// with T = kTileBytes / elem_bytes.
+constexpr int kTileBytes = 16384;
+struct Tile {
+    int32_t seg;
+    int32_t idx;
+};
+static_assert(sizeof(Tile) == 8, "Tile layout");
+
 }  // namespace ss
 
 struct ss_plan {
@@ -49,9 +59,14 @@ struct ss_plan {
     // pad segments sorted by packed offset; group_zero[g] = first pad segment of group g
     std::vector<ss::Seg> zero;
     std::vector<int> group_zero;
+    // tiles of the data / pad segments; seg_tile[k] = first tile of segment k (size nseg+1)
+    std::vector<ss::Tile> data_tiles, zero_tiles;
+    std::vector<int64_t> data_seg_tile, zero_seg_tile;
     // device copies
     ss::Seg* d_data = nullptr;
     ss::Seg* d_zero = nullptr;
+    ss::Tile* d_data_tiles = nullptr;
+    ss::Tile* d_zero_tiles = nullptr;
     int device = -1;
     bool has_dev = false;
 };

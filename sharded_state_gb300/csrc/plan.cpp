@@ -15,9 +15,9 @@
 // base_g + r * S_g.
 //
 // Besides the offsets the planner emits the two segment tables the copy
-// kernels walk: `data` (every contiguous run of a parameter inside one rank's
+// kernels use: `data` (every contiguous run of a parameter inside one rank's
 // shard, ordered by parameter then rank) and `zero` (every pad run, ordered by
-// packed offset).
+// packed offset), each split into 16 KiB tiles, one CTA per tile.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -142,6 +142,23 @@ void build_segments(ss_plan* p) {
     p->group_zero[p->G] = (int)p->zero.size();
 }
 
+// Split every segment into tiles of kTileBytes; false if a tile index would
+// not fit the 32-bit fields.
+bool build_tiles(const std::vector<ss::Seg>& segs, int eb, std::vector<ss::Tile>* tiles,
+                 std::vector<int64_t>* seg_tile) {
+    const int64_t T = ss::kTileBytes / eb;
+    tiles->clear();
+    seg_tile->assign(segs.size() + 1, 0);
+    for (size_t k = 0; k < segs.size(); ++k) {
+        (*seg_tile)[k] = (int64_t)tiles->size();
+        const int64_t nt = (segs[k].len + T - 1) / T;
+        if (nt > 0x7FFFFFFF || k > 0x7FFFFFFF) return false;
+        for (int64_t j = 0; j < nt; ++j) tiles->push_back(ss::Tile{(int32_t)k, (int32_t)j});
+    }
+    (*seg_tile)[segs.size()] = (int64_t)tiles->size();
+    return true;
+}
+
 int upload(ss_plan* p) {
     cudaError_t e = cudaGetDevice(&p->device);
     if (e != cudaSuccess) return ss::cuda_fail(e);
@@ -157,6 +174,21 @@ int upload(ss_plan* p) {
     }
     if (!p->zero.empty()) {
         e = cudaMemcpy(p->d_zero, p->zero.data(), p->zero.size() * sizeof(ss::Seg),
+                       cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return ss::cuda_fail(e);
+    }
+    size_t ndt = std::max<size_t>(p->data_tiles.size(), 1), nzt = std::max<size_t>(p->zero_tiles.size(), 1);
+    e = cudaMalloc(&p->d_data_tiles, ndt * sizeof(ss::Tile));
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    e = cudaMalloc(&p->d_zero_tiles, nzt * sizeof(ss::Tile));
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    if (!p->data_tiles.empty()) {
+        e = cudaMemcpy(p->d_data_tiles, p->data_tiles.data(), p->data_tiles.size() * sizeof(ss::Tile),
+                       cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return ss::cuda_fail(e);
+    }
+    if (!p->zero_tiles.empty()) {
+        e = cudaMemcpy(p->d_zero_tiles, p->zero_tiles.data(), p->zero_tiles.size() * sizeof(ss::Tile),
                        cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return ss::cuda_fail(e);
     }
@@ -270,6 +302,9 @@ int fsdp_plan_create(const ss_plan_desc* d, ss_plan** out) {
             p->offset = absolute;
             if (p->data.size() > (size_t)0x7FFFFFFF || p->zero.size() > (size_t)0x7FFFFFFF)
                 rc = SS_EOVERFLOW;
+            else if (!build_tiles(p->data, p->eb, &p->data_tiles, &p->data_seg_tile) ||
+                     !build_tiles(p->zero, p->eb, &p->zero_tiles, &p->zero_seg_tile))
+                rc = SS_EOVERFLOW;
         }
         if (rc == SS_OK && !(d->flags & SS_PLAN_HOST_ONLY)) rc = upload(p);
     } catch (const std::bad_alloc&) {
@@ -333,6 +368,8 @@ void fsdp_plan_destroy(ss_plan* p) {
     if (!p) return;
     if (p->d_data) cudaFree(p->d_data);
     if (p->d_zero) cudaFree(p->d_zero);
+    if (p->d_data_tiles) cudaFree(p->d_data_tiles);
+    if (p->d_zero_tiles) cudaFree(p->d_zero_tiles);
     delete p;
 }
 

@@ -14,9 +14,11 @@
 // reads N gradient values and three fp32 state values and writes three fp32
 // state values and one parameter value -- 2N + 26 bytes for bf16.  Nothing is
 // reused, so the kernel is bound by HBM bandwidth: it moves 128-bit vectors
-// (8 bf16 / 4 fp32 elements), keeps N + 6 independent loads in flight per
-// thread, and runs a persistent grid of (SMs x resident CTAs) that strides
-// over the vectors.
+// (8 bf16 / 4 fp32 elements) and keeps N + 6 independent loads in flight per
+// thread.  The grid has one thread per vector: short-lived CTAs retire in
+// address order, so all SMs stream through a narrow, advancing window of HBM,
+// which measured 7-8 % faster on GB300 than a persistent grid-stride loop over
+// the same vectors.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -60,7 +62,7 @@ __device__ __forceinline__ void adamw_elem(float g, float& theta, float& m, floa
 // ---------------------------------------------------------------------------
 
 template <int NR, bool ADAM, bool WRITE_G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 rs_adamw_bf16_kernel(RankPtrs grads, int N, int64_t vbeg, int64_t nvec, float* __restrict__ master,
                      float* __restrict__ exp_avg, float* __restrict__ exp_avg_sq,
                      uint16_t* __restrict__ shards, float* __restrict__ gout, AdamCoef c) {
@@ -151,7 +153,7 @@ rs_adamw_bf16_kernel(RankPtrs grads, int N, int64_t vbeg, int64_t nvec, float* _
 // ---------------------------------------------------------------------------
 
 template <int NR, bool ADAM, bool WRITE_G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 rs_adamw_f32_kernel(RankPtrs grads, int N, int64_t vbeg, int64_t nvec, float* __restrict__ master,
                     float* __restrict__ exp_avg, float* __restrict__ exp_avg_sq,
                     float* __restrict__ shards, float* __restrict__ gout, AdamCoef c) {
@@ -295,13 +297,11 @@ F32Kernel pick_f32(int N) {
     }
 }
 
-int grid_for(const void* fn, int64_t nvec) {
-    int bps = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, kThreads, 0) != cudaSuccess ||
-        bps <= 0)
-        bps = 2;
-    int64_t want = (nvec + kThreads - 1) / kThreads;
-    int64_t cap = (int64_t)ss::num_sms() * bps;
+// One thread per vector (the kernels' grid-stride loop only runs more than
+// once beyond 2^31 - 1 CTAs).
+int grid_for(int64_t nvec) {
+    const int64_t want = (nvec + kThreads - 1) / kThreads;
+    const int64_t cap = 0x7FFFFFFF;
     return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
@@ -369,13 +369,13 @@ int fsdp_reduce_scatter_adamw(const ss_plan* plan, const void* const* rank_grads
         if (plan->eb == 2) {
             BF16Kernel fn = adam ? (wg ? pick_bf16<true, true>(N) : pick_bf16<true, false>(N))
                                  : pick_bf16<false, true>(N);
-            int grid = grid_for((const void*)fn, nvec);
+            int grid = grid_for(nvec);
             fn<<<grid, kThreads, 0, st>>>(rp, N, vbeg, nvec, master, exp_avg, exp_avg_sq,
                                           static_cast<uint16_t*>(param_shards), reduced_grad_out, c);
         } else {
             F32Kernel fn = adam ? (wg ? pick_f32<true, true>(N) : pick_f32<true, false>(N))
                                 : pick_f32<false, true>(N);
-            int grid = grid_for((const void*)fn, nvec);
+            int grid = grid_for(nvec);
             fn<<<grid, kThreads, 0, st>>>(rp, N, vbeg, nvec, master, exp_avg, exp_avg_sq,
                                           static_cast<float*>(param_shards), reduced_grad_out, c);
         }
