@@ -56,6 +56,12 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--mode", choices=["step", "rows"], default="step",
+                    help="step: the one-line headline; rows: one JSON line per hot-path row")
+    ap.add_argument("--rows", default="all",
+                    help="rows mode: comma list of llama,block4096,tiny,awkward,ddp (default all)")
+    ap.add_argument("--ddp-large", type=int, default=600,
+                    help="rows mode: number of 4M-element DDP tensors (600 = the full list)")
     return ap.parse_args()
 
 
@@ -240,6 +246,9 @@ class Step:
         self.out_numel = pos
         self.out_flat = [torch.empty(pos, dtype=ps.dtype, device=dev) for _ in range(n_out)]
         self.outs = [o[off:off + n] for o in self.out_flat for off, n in zip(offs, numels)]
+        # pointer arrays marshalled once; the timed calls pass them straight through
+        self._grads_arr = ss.ptr_array(self.grads)
+        self._outs_arr = ss.ptr_array(self.outs)
         self.t = 0
 
     def _rank_grad_iter(self, dev):
@@ -251,14 +260,16 @@ class Step:
                    for n in ps.numels()]
 
     def rs_adamw(self, stream=None):
+        """One fused reduce-scatter + AdamW call over every group (next AdamW step)."""
         self.t += 1
         hp = self.ss.adamw_params(step=self.t, **{k: v for k, v in W.adamw_hparams().items()
                                                    if k != "step"})
-        self.ss.fsdp_reduce_scatter_adamw(self.plan, self.grads, self.master, self.m, self.v,
+        self.ss.fsdp_reduce_scatter_adamw(self.plan, self._grads_arr, self.master, self.m, self.v,
                                           self.shards, hp, None, -1, stream)
 
     def all_gather(self, stream=None):
-        self.ss.fsdp_all_gather_unpack(self.plan, self.shards, self.outs, self.n_out, -1, stream)
+        self.ss.fsdp_all_gather_unpack(self.plan, self.shards, self._outs_arr, self.n_out, -1,
+                                       stream)
 
 
 def run_native(args, world, rank, local, dist):
@@ -495,11 +506,206 @@ def run_reference(args, world, rank):
     print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# per-row measurements (--mode rows): every hot-path row on its own workload
+# ---------------------------------------------------------------------------
+
+def _time_stream(fn, K: int, warmup: int = 3):
+    """Mean / min CUDA-event time (ms) of fn() on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(K):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ts]
+    return sum(ms) / len(ms), min(ms)
+
+
+def _time_cpu(fn, seconds: float):
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        fn()
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return (time.perf_counter() - t0) / reps, reps
+
+
+def _row(name, unit_count, unit, ms, ms_min, nbytes, peak, cpu=None, extra=None):
+    gbs = nbytes / (ms / 1e3) / 1e9
+    d = {"row": name, "value": unit_count / (ms / 1e3), "unit": unit, "ms": ms, "ms_min": ms_min,
+         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                      "frac": gbs / peak, "algorithmic_bytes": nbytes}}
+    if cpu is not None:
+        d["cpu_baseline"] = cpu
+    if extra:
+        d.update(extra)
+    print(json.dumps(d), flush=True)
+
+
+def run_rows(args):
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    import sharded_state_gb300 as ss
+    torch.cuda.set_device(0)
+    peak, _ = measured_peak()
+    cores = _host_cores()
+    oracle.set_threads(cores)
+    used = cores if oracle.has_openmp() else 1
+    K = max(args.steps, 5)
+    bits = lambda t: t.reshape(-1).cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    want = set(args.rows.split(",")) if args.rows != "all" else {"llama", "block4096", "tiny",
+                                                                 "awkward", "ddp"}
+    if "llama" in want:
+        _rows_llama(args, ss, oracle, peak, used, K, bits)
+    if "block4096" in want:
+        _rows_block4096(ss, peak, K)
+    if "tiny" in want or "awkward" in want:
+        _rows_small(ss, peak, want)
+    if "ddp" in want:
+        _rows_ddp(args, ss, oracle, peak, used, K, bits)
+
+
+def _rows_llama(args, ss, oracle, peak, used, K, bits):
+    # -- a1/a2/a3/a4 on the 1.2B model ---------------------------------------
+    ps = W.llama_1b2()
+    st = Step(ss, ps, 1)
+    P, total, N = st.info["unpadded_numel"], st.info["total_numel"], st.N
+    d0, inner = ps.dim0_inner()
+    grad_params = next(st._rank_grad_iter("cuda"))
+    packed = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+    ms, mn = _time_stream(lambda: ss.fsdp_pack(st.plan, grad_params, packed), K)
+    # oracle: pack of block group 0 of one rank
+    g0 = ps.groups[0]
+    sample = [bits(t) for t in grad_params[:g0]]
+    t_cpu, reps = _time_cpu(lambda: oracle.pack(ps.layout, N, 2, d0[:g0], inner[:g0], sample),
+                            args.cpu_seconds / 4)
+    p0 = sum(ps.numels()[:g0])
+    _row("a2 pack (one rank's gradients, 1.2B model, N=8)", P, "params/s", ms, mn, 4 * P, peak,
+         {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
+          "sample": f"block group 0 ({p0:,} params), {reps} packs"})
+    del grad_params
+
+    del packed
+    rs_ms, rs_mn = _time_stream(lambda: st.rs_adamw(), K)
+    smp = _oracle_sample_from_step(st)
+    t_cpu, reps = _time_cpu(lambda: _oracle_step(ps, smp, 10_000), args.cpu_seconds / 2)
+    _row("a3 reduce-scatter + AdamW (1.2B model, N=8)", P, "params/s", rs_ms, rs_mn,
+         (2 * N + 26) * total, peak,
+         {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
+          "sample": f"block group 0, {reps} oracle RS+AdamW+AG steps"})
+    ag_ms, ag_mn = _time_stream(lambda: st.all_gather(), K)
+    _row("a4 all-gather + unpack, n_out=1 (1.2B model, N=8)", P, "params/s", ag_ms, ag_mn, 4 * P,
+         peak)
+    st8 = st
+    outs8 = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for _ in range(N)
+             for s in ps.shapes]
+    ms, mn = _time_stream(lambda: ss.fsdp_all_gather_unpack(st8.plan, st8.shards, outs8, N), K)
+    _row("a4 all-gather + unpack, n_out=N=8 (every rank's copy)", P, "params/s", ms, mn,
+         (2 + 2 * N) * P, peak)
+    del outs8, st, st8
+    torch.cuda.empty_cache()
+
+
+def _rows_block4096(ss, peak, K):
+    # -- config 2: one 4096 block ---------------------------------------------
+    ps2 = W.llama_block_4096()
+    st2 = Step(ss, ps2, 1)
+    P2, total2 = st2.info["unpadded_numel"], st2.info["total_numel"]
+
+    def step2():
+        st2.rs_adamw()
+        st2.all_gather()
+    ms, mn = _time_stream(step2, K)
+    by = step_bytes(8, total2, P2, 1)
+    _row("step on one Llama block, hidden 4096 (202M params, N=8)", P2, "params/s", ms, mn,
+         by["step"], peak)
+    del st2
+    torch.cuda.empty_cache()
+
+
+def _rows_small(ss, peak, want):
+    # -- config 1: tiny MLP, launch-bound -------------------------------------
+    ps1 = W.tiny_mlp()
+    st1 = Step(ss, ps1, 1)
+
+    def step1():
+        st1.rs_adamw()
+        st1.all_gather()
+    if "tiny" in want:
+        ms, mn = _time_stream(step1, 200, warmup=20)
+        by = step_bytes(2, st1.info["total_numel"], st1.info["unpadded_numel"], 1)
+        _row("step on the tiny MLP (16,640 params, N=2): latency", st1.info["unpadded_numel"],
+             "params/s", ms, mn, by["step"], peak, extra={"us_per_step": ms * 1e3})
+
+    # -- config 3: awkward sizes, N=7 ------------------------------------------
+    for kind in ((W.FLAT_ORIG_FALSE, W.FLAT_ORIG_TRUE) if "awkward" in want else ()):
+        ps3 = W.awkward_1d(7, kind, torch.bfloat16)
+        st3 = Step(ss, ps3, 1)
+
+        def step3():
+            st3.rs_adamw()
+            st3.all_gather()
+        ms, mn = _time_stream(step3, 100, warmup=10)
+        by = step_bytes(7, st3.info["total_numel"], st3.info["unpadded_numel"], 1)
+        _row(f"step on 200 awkward params ({W.LAYOUT_NAMES[kind]}, N=7)",
+             st3.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
+             extra={"us_per_step": ms * 1e3})
+
+
+
+def _rows_ddp(args, ss, oracle, peak, used, K, bits):
+    # -- a5: DDP bucketed average, cap sweep (config 4) -----------------------
+    ds = W.ddp_grads(n_large=args.ddp_large)
+    grads = W.make_ddp_grads(ds, device="cuda")
+    outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for n in ds.numels]
+    Pd = sum(ds.numels)
+    small = [[bits(grads[r][t]) for t in range(40)] for r in range(ds.world_size)]
+    t_cpu, reps = _time_cpu(lambda: oracle.ddp_average(small), args.cpu_seconds / 4)
+    psmall = sum(ds.numels[:40])
+    cpu = {"value": psmall / t_cpu, "unit": "elements/s", "cores": used, "kind": "oracle",
+           "sample": f"first 40 tensors ({psmall:,} elements, N=8), {reps} averages"}
+    import ctypes
+    T = len(ds.numels)
+    flat_arr = ss.ptr_array([g for rank in grads for g in rank])
+    outs_arr = ss.ptr_array(outs)
+    numels_arr = (ctypes.c_int64 * T)(*ds.numels)
+    nb_out = ctypes.c_int()
+    sp = torch.cuda.current_stream().cuda_stream
+
+    def ddp_call(cap):
+        st_ = ss.lib().ddp_bucket_pack_average(ds.world_size, T, numels_arr, flat_arr, cap,
+                                               outs_arr, ctypes.byref(nb_out), sp)
+        if st_ != 0:
+            raise RuntimeError(f"ddp_bucket_pack_average: {ss.ss_strerror(st_)}")
+    for cap in W.DDP_BUCKET_CAPS:
+        nb = ss.ddp_bucket_assign(ds.numels, 2, cap)[1]
+        ms, mn = _time_stream(lambda: ddp_call(cap), max(K // 10, 5))
+        _row(f"a5 DDP bucketed average, cap {cap} B ({len(ds.numels)} grads, "
+             f"{2 * Pd / 1e9:.2f} GB/rank, N=8)", Pd,
+             "elements/s", ms, mn, (2 * ds.world_size + 2) * Pd, peak, cpu,
+             extra={"bucket_cap_bytes": cap, "buckets": nb})
+        cpu = None
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.mode == "rows":
+        run_rows(args)
         return
     dist = dist_init(world, local)
     try:

@@ -150,7 +150,15 @@ def _addr(x) -> Optional[int]:
     return int(x.data_ptr())
 
 
+def ptr_array(xs: Sequence) -> ctypes.Array:
+    """A host array of device pointers, built once and reusable across calls
+    (every call that takes a list of tensors also accepts one of these)."""
+    return _ptr_array(xs)
+
+
 def _ptr_array(xs: Sequence) -> ctypes.Array:
+    if isinstance(xs, ctypes.Array):
+        return xs
     arr = (ctypes.c_void_p * max(1, len(xs)))()
     for k, x in enumerate(xs):
         arr[k] = _addr(x)
