@@ -267,6 +267,20 @@ class Step:
         self.ss.fsdp_reduce_scatter_adamw(self.plan, self._grads_arr, self.master, self.m, self.v,
                                           self.shards, hp, None, -1, stream)
 
+    def fused_step(self, stream=None, param_grads=None):
+        """fsdp_sharded_step: RS+AdamW with the all-gather written in the same pass."""
+        self.t += 1
+        hp = self.ss.adamw_params(step=self.t, **{k: v for k, v in W.adamw_hparams().items()
+                                                   if k != "step"})
+        if param_grads is None:
+            self.ss.fsdp_sharded_step(self.plan, self.master, self.m, self.v, self.shards, hp,
+                                      rank_grads=self._grads_arr, params_out=self._outs_arr,
+                                      n_out=self.n_out, stream=stream)
+        else:
+            self.ss.fsdp_sharded_step(self.plan, self.master, self.m, self.v, self.shards, hp,
+                                      rank_param_grads=param_grads, params_out=self._outs_arr,
+                                      n_out=self.n_out, stream=stream)
+
     def all_gather(self, stream=None):
         self.ss.fsdp_all_gather_unpack(self.plan, self.shards, self._outs_arr, self.n_out, -1,
                                        stream)
@@ -607,6 +621,15 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     ag_ms, ag_mn = _time_stream(lambda: st.all_gather(), K)
     _row("a4 all-gather + unpack, n_out=1 (1.2B model, N=8)", P, "params/s", ag_ms, ag_mn, 4 * P,
          peak)
+    ms, mn = _time_stream(lambda: st.fused_step(), K)
+    _row("one-pass step: packed grads -> RS+AdamW -> shards + unpacked params (1.2B, N=8)", P,
+         "params/s", ms, mn, (2 * N + 28) * P, peak)
+    rank_sets = list(st._rank_grad_iter("cuda"))  # N distinct per-parameter gradient sets
+    flat_pg = ss.ptr_array([g for rank in rank_sets for g in rank])
+    ms, mn = _time_stream(lambda: st.fused_step(param_grads=flat_pg), K)
+    _row("one-pass step with fused copy-in: N per-parameter grad sets -> RS+AdamW -> shards + "
+         "unpacked params (1.2B, N=8)", P, "params/s", ms, mn, (2 * N + 28) * P, peak)
+    del rank_sets, flat_pg
     st8 = st
     outs8 = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for _ in range(N)
              for s in ps.shapes]

@@ -269,6 +269,45 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards,
                            void* const* params_out, int n_out, int group, ss_stream_t stream);
 
 /*
+ * The whole sharded step in one pass over the parameters: (copy-in) +
+ * reduce-scatter + AdamW + (all-gather + unpack).  Same arithmetic as
+ * fsdp_reduce_scatter_adamw followed by fsdp_all_gather_unpack, but the
+ * kernel walks the plan's data tiles (runs of one parameter inside one rank's
+ * shard), so in one pass it can
+ *   - read rank r's gradient either from its packed buffer (rank_grads[r],
+ *     as fsdp_pack writes it) or straight from rank r's per-parameter
+ *     gradient tensors (rank_param_grads[r*num_params + i]), fusing away the
+ *     copy-in that FSDP does before its reduce-scatter ("FSDP1 vs FSDP2",
+ *     section 04: a group's gradients are concatenated into one
+ *     reduce-scatter buffer);
+ *   - write each new bf16 parameter value both to its shard and to the n_out
+ *     per-parameter outputs (the all-gather + unpack, no second pass over the
+ *     shards).
+ * Pad elements are not read or written (they stay as fsdp_pack /
+ * fsdp_init_master left them: zero).  bf16 plans only.
+ */
+typedef struct {
+    const void* const* rank_grads;        /* HOST [N] packed buffers (16-byte aligned), or NULL */
+    const void* const* rank_param_grads;  /* HOST [N * num_params] per-parameter gradients, or NULL;
+                                             exactly one of the two is non-NULL */
+    float* master;                        /* total_numel floats, updated in place */
+    float* exp_avg;
+    float* exp_avg_sq;
+    void* param_shards;                   /* total_numel bf16, written */
+    const ss_adamw* hp;                   /* required */
+    float* reduced_grad_out;              /* nullable: total_numel floats (pads not written) */
+    void* const* params_out;              /* HOST [n_out * num_params] outputs, or NULL if n_out == 0 */
+    int n_out;                            /* 0..SS_MAX_REPLICAS; 0 = no all-gather */
+} ss_step;
+
+/* Per launch the pointer table holds (N if rank_param_grads else 0) + n_out
+ * entries per parameter within 2048 slots; more parameters are split into
+ * launches over consecutive parameters.  Errors: SS_EINVAL (including both or
+ * neither gradient source, fp32 plans, (N + n_out) > 2048), SS_EALIGN,
+ * SS_ENODEVICE, SS_ECUDA. */
+int fsdp_sharded_step(const ss_plan* plan, const ss_step* step, int group, ss_stream_t stream);
+
+/*
  * DDP bucketed gradient average ("Scaling data parallel", sections 3-4:
  * gradients become final last layer first, so tensors are taken in reverse
  * registration order; each joins the open bucket, and a bucket that holds at

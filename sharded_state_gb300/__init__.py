@@ -40,7 +40,7 @@ EXPORTED = ("fsdp_plan_create", "fsdp_plan_layout", "fsdp_plan_info", "fsdp_plan
             "fsdp_plan_group", "fsdp_plan_destroy", "fsdp_pack", "fsdp_init_master",
             "fsdp_reduce_scatter_adamw", "fsdp_all_gather_unpack", "ddp_bucket_pack_average",
             "ddp_bucket_assign", "ss_strerror", "ss_last_cuda_error", "ss_version",
-            "ss_launch_count", "ddp_bucket_pack_average_noalloc")
+            "ss_launch_count", "ddp_bucket_pack_average_noalloc", "fsdp_sharded_step")
 
 
 class ShardStateError(RuntimeError):
@@ -73,6 +73,14 @@ class AdamW(ctypes.Structure):
                 ("step", ctypes.c_int64)]
 
 
+class _Step(ctypes.Structure):
+    _fields_ = [("rank_grads", ctypes.c_void_p), ("rank_param_grads", ctypes.c_void_p),
+                ("master", ctypes.c_void_p), ("exp_avg", ctypes.c_void_p),
+                ("exp_avg_sq", ctypes.c_void_p), ("param_shards", ctypes.c_void_p),
+                ("hp", ctypes.POINTER(AdamW)), ("reduced_grad_out", ctypes.c_void_p),
+                ("params_out", ctypes.c_void_p), ("n_out", ctypes.c_int)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with `python sharded_state_gb300/build.py` "
@@ -98,6 +106,7 @@ def _load() -> ctypes.CDLL:
         "ddp_bucket_pack_average_noalloc": ([i32, i32, i64p, vpp, ctypes.c_size_t, vpp,
                                              ctypes.POINTER(i32), vp], i32),
         "ddp_bucket_assign": ([i32, i64p, i32, ctypes.c_size_t, ctypes.POINTER(i32)], i32),
+        "fsdp_sharded_step": ([vp, ctypes.POINTER(_Step), i32, vp], i32),
         "ss_strerror": ([i32], ctypes.c_char_p),
         "ss_last_cuda_error": ([], i32),
         "ss_version": ([], ctypes.c_char_p),
@@ -305,6 +314,29 @@ def fsdp_all_gather_unpack(plan: Plan, param_shards, params_out: Sequence, n_out
     """params_out: n_out * num_params tensors, replica-major."""
     _check("fsdp_all_gather_unpack", _lib.fsdp_all_gather_unpack(
         plan, _addr(param_shards), _ptr_array(params_out), n_out, group, _stream(stream)))
+
+
+def fsdp_sharded_step(plan: Plan, master, exp_avg, exp_avg_sq, param_shards, hp: AdamW,
+                      rank_grads: Optional[Sequence] = None,
+                      rank_param_grads: Optional[Sequence] = None, params_out=None,
+                      n_out: int = 0, reduced_grad_out=None, group: int = -1,
+                      stream=None) -> None:
+    """One-pass step: gradients from N packed buffers (rank_grads) or from N
+    per-parameter gradient sets (rank_param_grads, rank-major: rank r's
+    gradient of parameter i at r*num_params + i), reduce-scatter + AdamW, and
+    optionally the n_out per-parameter outputs (replica-major)."""
+    keep = []
+    def arr(xs):
+        if xs is None:
+            return None
+        a = _ptr_array(xs)
+        keep.append(a)
+        return ctypes.cast(a, ctypes.c_void_p)
+    st = _Step(arr(rank_grads), arr(rank_param_grads), _addr(master), _addr(exp_avg),
+               _addr(exp_avg_sq), _addr(param_shards), ctypes.pointer(hp), _addr(reduced_grad_out),
+               arr(params_out) if n_out > 0 else None, n_out)
+    _check("fsdp_sharded_step", _lib.fsdp_sharded_step(plan, ctypes.byref(st), group,
+                                                       _stream(stream)))
 
 
 def ddp_bucket_pack_average(rank_grads: Sequence[Sequence], bucket_cap_bytes: int,

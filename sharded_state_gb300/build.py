@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libshardstate.so")
 
-SOURCES = ["plan.cpp", "rs_adamw.cu", "gather.cu", "ddp.cu"]
+SOURCES = ["plan.cpp", "rs_adamw.cu", "gather.cu", "ddp.cu", "step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
 

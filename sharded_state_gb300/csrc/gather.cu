@@ -29,6 +29,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTabSmall = 256;
 constexpr int kTabBig = 2048;
+// When one pointer table covers the call, tiles could be walked in packed-offset
+// order; parameter order measured slightly faster on GB300 (0.823 vs 0.829 ms
+// for the 1.2B all-gather), so it stays off.
+constexpr bool kPackedOrder = false;
 
 template <int CAP>
 struct PtrTab {
@@ -182,12 +186,17 @@ int for_tile_chunks(int64_t t_lo, int64_t t_hi, Launch launch) {
     return SS_OK;
 }
 
+// Tiles of params [a, b): consecutive in the parameter-ordered table, or, when
+// [a, b) is whole groups [ga, gb), the packed-order table of those groups.
 template <int CAP>
 int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed,
-                  void* const* ptrs, int n_out, cudaStream_t st) {
+                  void* const* ptrs, int n_out, cudaStream_t st, int ga = -1, int gb = -1) {
     const int s_lo = p->param_seg[a], s_hi = p->param_seg[b];
     if (s_hi <= s_lo) return SS_OK;
-    const int64_t t_lo = p->data_seg_tile[s_lo], t_hi = p->data_seg_tile[s_hi];
+    const bool by_offset = kPackedOrder && ga >= 0;
+    const ss::Tile* tiles = by_offset ? p->d_packed_tiles : p->d_data_tiles;
+    const int64_t t_lo = by_offset ? p->group_ptile[ga] : p->data_seg_tile[s_lo];
+    const int64_t t_hi = by_offset ? p->group_ptile[gb] : p->data_seg_tile[s_hi];
     PtrTab<CAP> tab;
     std::memset(&tab, 0, sizeof tab);
     const int w = b - a;
@@ -196,33 +205,37 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
     return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
         if (p->eb == 2) {
             if (dir == 0 && n_out > 1)
-                tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
-                                                                       packed, tab, a, w, n_out);
+                tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, n_out);
             else if (dir == 0)
-                tile_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
-                                                                       packed, tab, a, w, 1);
+                tile_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, 1);
             else
-                tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
-                                                                       packed, tab, a, w, 1);
+                tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, 1);
         } else {
             if (dir == 0 && n_out > 1)
-                tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
-                                                                       packed, tab, a, w, n_out);
+                tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, n_out);
             else if (dir == 0)
-                tile_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
-                                                                       packed, tab, a, w, 1);
+                tile_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, 1);
             else
-                tile_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(p->d_data_tiles, t, p->d_data,
-                                                                       packed, tab, a, w, 1);
+                tile_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, 1);
         }
     });
 }
 
-// Run the segment copy for params [pa, pb), windowing the pointer table.
-int run_segments(const ss_plan* p, int dir, int pa, int pb, unsigned char* packed,
+// Run the segment copy for params [pa, pb) = groups [ga, gb), windowing the
+// pointer table.
+int run_segments(const ss_plan* p, int dir, int pa, int pb, int ga, int gb, unsigned char* packed,
                  void* const* ptrs, int n_out, cudaStream_t st) {
     const int n_ptr = (pb - pa) * n_out;
-    if (n_ptr <= kTabSmall) return launch_window<kTabSmall>(p, dir, pa, pb, packed, ptrs, n_out, st);
+    if (n_ptr <= kTabSmall)
+        return launch_window<kTabSmall>(p, dir, pa, pb, packed, ptrs, n_out, st, ga, gb);
+    if (n_ptr <= kTabBig)
+        return launch_window<kTabBig>(p, dir, pa, pb, packed, ptrs, n_out, st, ga, gb);
     const int w = kTabBig / n_out;
     for (int a = pa; a < pb; a += w) {
         int b = a + w < pb ? a + w : pb;
@@ -269,7 +282,8 @@ int fsdp_pack(const ss_plan* plan, const void* const* params, void* packed, int 
     int rc = check_param_ptrs(plan, pa, pb, const_cast<void* const*>(params), 1);
     if (rc) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = run_segments(plan, 1, pa, pb, static_cast<unsigned char*>(packed),
+    const int ga0 = group < 0 ? 0 : group, gb0 = group < 0 ? plan->G : group + 1;
+    rc = run_segments(plan, 1, pa, pb, ga0, gb0, static_cast<unsigned char*>(packed),
                       const_cast<void* const*>(params), 1, st);
     if (rc) return rc;
     // pads of the selected groups
@@ -300,7 +314,8 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards, void* 
     param_range(plan, group, &pa, &pb);
     int rc = check_param_ptrs(plan, pa, pb, params_out, n_out);
     if (rc) return rc;
-    return run_segments(plan, 0, pa, pb,
+    const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
+    return run_segments(plan, 0, pa, pb, ga, gb,
                         static_cast<unsigned char*>(const_cast<void*>(param_shards)), params_out,
                         n_out, reinterpret_cast<cudaStream_t>(stream));
 }

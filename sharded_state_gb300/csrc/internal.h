@@ -62,11 +62,16 @@ struct ss_plan {
     // tiles of the data / pad segments; seg_tile[k] = first tile of segment k (size nseg+1)
     std::vector<ss::Tile> data_tiles, zero_tiles;
     std::vector<int64_t> data_seg_tile, zero_seg_tile;
+    // the data tiles again, ordered by packed offset; group g's tiles are
+    // [group_ptile[g], group_ptile[g+1])
+    std::vector<ss::Tile> packed_tiles;
+    std::vector<int64_t> group_ptile;
     // device copies
     ss::Seg* d_data = nullptr;
     ss::Seg* d_zero = nullptr;
     ss::Tile* d_data_tiles = nullptr;
     ss::Tile* d_zero_tiles = nullptr;
+    ss::Tile* d_packed_tiles = nullptr;
     int device = -1;
     bool has_dev = false;
 };

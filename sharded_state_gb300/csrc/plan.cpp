@@ -159,6 +159,26 @@ bool build_tiles(const std::vector<ss::Seg>& segs, int eb, std::vector<ss::Tile>
     return true;
 }
 
+// Data tiles in packed-offset order, group by group (segments of one group
+// are disjoint runs of that group's range, so sorting by offset keeps groups
+// contiguous).
+void build_packed_tiles(ss_plan* p) {
+    std::vector<int> order(p->data.size());
+    for (size_t k = 0; k < order.size(); ++k) order[k] = (int)k;
+    std::sort(order.begin(), order.end(),
+              [&](int a, int b) { return p->data[a].packed_off < p->data[b].packed_off; });
+    p->packed_tiles.clear();
+    p->group_ptile.assign(p->G + 1, 0);
+    int g = 0;
+    for (int k : order) {
+        const int pg = p->param_group[p->data[k].param];
+        while (g < pg) p->group_ptile[++g] = (int64_t)p->packed_tiles.size();
+        for (int64_t t = p->data_seg_tile[k]; t < p->data_seg_tile[k + 1]; ++t)
+            p->packed_tiles.push_back(p->data_tiles[t]);
+    }
+    while (g < p->G) p->group_ptile[++g] = (int64_t)p->packed_tiles.size();
+}
+
 int upload(ss_plan* p) {
     cudaError_t e = cudaGetDevice(&p->device);
     if (e != cudaSuccess) return ss::cuda_fail(e);
@@ -190,6 +210,13 @@ int upload(ss_plan* p) {
     if (!p->zero_tiles.empty()) {
         e = cudaMemcpy(p->d_zero_tiles, p->zero_tiles.data(), p->zero_tiles.size() * sizeof(ss::Tile),
                        cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return ss::cuda_fail(e);
+    }
+    e = cudaMalloc(&p->d_packed_tiles, ndt * sizeof(ss::Tile));
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    if (!p->packed_tiles.empty()) {
+        e = cudaMemcpy(p->d_packed_tiles, p->packed_tiles.data(),
+                       p->packed_tiles.size() * sizeof(ss::Tile), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return ss::cuda_fail(e);
     }
     p->has_dev = true;
@@ -305,6 +332,8 @@ int fsdp_plan_create(const ss_plan_desc* d, ss_plan** out) {
             else if (!build_tiles(p->data, p->eb, &p->data_tiles, &p->data_seg_tile) ||
                      !build_tiles(p->zero, p->eb, &p->zero_tiles, &p->zero_seg_tile))
                 rc = SS_EOVERFLOW;
+            else
+                build_packed_tiles(p);
         }
         if (rc == SS_OK && !(d->flags & SS_PLAN_HOST_ONLY)) rc = upload(p);
     } catch (const std::bad_alloc&) {
@@ -370,6 +399,7 @@ void fsdp_plan_destroy(ss_plan* p) {
     if (p->d_zero) cudaFree(p->d_zero);
     if (p->d_data_tiles) cudaFree(p->d_data_tiles);
     if (p->d_zero_tiles) cudaFree(p->d_zero_tiles);
+    if (p->d_packed_tiles) cudaFree(p->d_packed_tiles);
     delete p;
 }
 

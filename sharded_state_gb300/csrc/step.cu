@@ -1,0 +1,349 @@
+// step.cu -- the whole sharded step in one pass over the parameters:
+// (copy-in) + reduce-scatter + AdamW + (all-gather + unpack).
+//
+// fsdp_reduce_scatter_adamw streams the packed index space and
+// fsdp_all_gather_unpack then reads the new shards back to unpack them.  This
+// kernel walks the plan's data tiles instead (one CTA per 16 KiB tile of one
+// parameter's run inside one rank's shard, "FSDP1 vs FSDP2" section 03 / 04),
+// so for every element it knows both its packed index f (gradient buffers,
+// optimizer state, shards) and its place k inside the parameter tensor.  That
+// lets one pass
+//   - read the N gradients either from the packed rank buffers (the
+//     reduce-scatter input FSDP builds by copy-in) or directly from the N
+//     per-parameter gradient sets, which fuses the copy-in away;
+//   - sum them in fp32 in rank order and divide by N (the reduce-scatter,
+//     "Scaling data parallel" sections 9.1-9.3);
+//   - run AdamW on the fp32 master and moments and write the bf16 shard;
+//   - write the same bf16 value into the n_out per-parameter outputs (the
+//     all-gather + unpack, "FSDP1 vs FSDP2" section 04), with no second pass
+//     over the shards.
+// Bytes per parameter element at N ranks: 2N (grads) + 12 + 12 (state) + 2
+// (shard) + 2*n_out, e.g. 44 at N = 8, n_out = 1, against 46 for the two
+// separate calls and 46 + 4N with a separate pack pass.  Pad elements are not
+// touched: they hold zero gradients and zero state, which AdamW leaves zero.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "device_utils.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTab = 2048;
+constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
+
+struct RankPtrs {
+    const void* p[SS_MAX_WORLD];
+};
+struct PtrTab {
+    void* p[kTab];
+};
+struct AdamCoef {
+    float decay, b1, omb1, b2, omb2, step_size, inv_sqrt_bc2, eps;
+};
+
+__device__ __forceinline__ void adamw_elem(float g, float& theta, float& m, float& v,
+                                           const AdamCoef& c) {
+    theta = __fmul_rn(theta, c.decay);
+    m = __fmaf_rn(c.b1, m, __fmul_rn(c.omb1, g));
+    v = __fmaf_rn(c.b2, v, __fmul_rn(c.omb2, __fmul_rn(g, g)));
+    float denom = __fmaf_rn(__fsqrt_rn(v), c.inv_sqrt_bc2, c.eps);
+    theta = __fmaf_rn(-c.step_size, __fdiv_rn(m, denom), theta);
+}
+
+// Kernel arguments that do not change per tile.
+struct StepArgs {
+    RankPtrs packed_grads;  // [N] packed rank buffers (UNPACKED == false)
+    float* master;
+    float* exp_avg;
+    float* exp_avg_sq;
+    uint16_t* shards;
+    float* gout;
+    int N;
+    int n_out;
+    int param_base;  // first parameter of this launch's window
+    int w;           // parameters in the window
+    AdamCoef c;
+};
+
+// Table layout: UNPACKED gradients tab[r*w + slot] for r < N, then outputs
+// tab[goff + j*w + slot] with goff = (UNPACKED ? N*w : 0).
+template <bool UNPACKED>
+__device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const PtrTab& tab, int r,
+                                                    int slot, int64_t f, int64_t k) {
+    if (UNPACKED) return static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k;
+    return static_cast<const uint16_t*>(a.packed_grads.p[r]) + f;
+}
+
+// NR > 0: exactly NR ranks, fully unrolled; NR == 0: any N, the first 8 ranks'
+// loads predicated and kept in flight together, the rest one by one.
+template <int NR, bool UNPACKED, int GATHER, bool WRITE_G>
+__device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, int slot,
+                                         int64_t f, int64_t k) {
+    const int n = NR > 0 ? NR : a.N;
+    uint4 w[kMaxVec];
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r)
+        if (r < n) w[r] = ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
+    const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
+    const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+    const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+    float s[8] = {ss::bf16_lo(w[0].x), ss::bf16_hi(w[0].x), ss::bf16_lo(w[0].y),
+                  ss::bf16_hi(w[0].y), ss::bf16_lo(w[0].z), ss::bf16_hi(w[0].z),
+                  ss::bf16_lo(w[0].w), ss::bf16_hi(w[0].w)};
+#pragma unroll
+    for (int r = 1; r < kMaxVec; ++r) {
+        if (r < n) {
+            s[0] = __fadd_rn(s[0], ss::bf16_lo(w[r].x));
+            s[1] = __fadd_rn(s[1], ss::bf16_hi(w[r].x));
+            s[2] = __fadd_rn(s[2], ss::bf16_lo(w[r].y));
+            s[3] = __fadd_rn(s[3], ss::bf16_hi(w[r].y));
+            s[4] = __fadd_rn(s[4], ss::bf16_lo(w[r].z));
+            s[5] = __fadd_rn(s[5], ss::bf16_hi(w[r].z));
+            s[6] = __fadd_rn(s[6], ss::bf16_lo(w[r].w));
+            s[7] = __fadd_rn(s[7], ss::bf16_hi(w[r].w));
+        }
+    }
+    for (int r = kMaxVec; NR == 0 && r < n; ++r) {  // ranks beyond the first 8
+        const uint4 x = ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
+        s[0] = __fadd_rn(s[0], ss::bf16_lo(x.x));
+        s[1] = __fadd_rn(s[1], ss::bf16_hi(x.x));
+        s[2] = __fadd_rn(s[2], ss::bf16_lo(x.y));
+        s[3] = __fadd_rn(s[3], ss::bf16_hi(x.y));
+        s[4] = __fadd_rn(s[4], ss::bf16_lo(x.z));
+        s[5] = __fadd_rn(s[5], ss::bf16_hi(x.z));
+        s[6] = __fadd_rn(s[6], ss::bf16_lo(x.w));
+        s[7] = __fadd_rn(s[7], ss::bf16_hi(x.w));
+    }
+    const float fN = (float)n;
+    float g[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = __fdiv_rn(s[e], fN);
+    if (WRITE_G) {
+        ss::st_stream_f4(a.gout + f, make_float4(g[0], g[1], g[2], g[3]));
+        ss::st_stream_f4(a.gout + f + 4, make_float4(g[4], g[5], g[6], g[7]));
+    }
+    float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+    float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) adamw_elem(g[e], th[e], mm[e], vv[e], a.c);
+    ss::st_stream_f4(a.master + f, make_float4(th[0], th[1], th[2], th[3]));
+    ss::st_stream_f4(a.master + f + 4, make_float4(th[4], th[5], th[6], th[7]));
+    ss::st_stream_f4(a.exp_avg + f, make_float4(mm[0], mm[1], mm[2], mm[3]));
+    ss::st_stream_f4(a.exp_avg + f + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
+    ss::st_stream_f4(a.exp_avg_sq + f, make_float4(vv[0], vv[1], vv[2], vv[3]));
+    ss::st_stream_f4(a.exp_avg_sq + f + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    uint4 p;
+    p.x = ss::pack_bf16x2(th[0], th[1]);
+    p.y = ss::pack_bf16x2(th[2], th[3]);
+    p.z = ss::pack_bf16x2(th[4], th[5]);
+    p.w = ss::pack_bf16x2(th[6], th[7]);
+    ss::st_stream_u4(a.shards + f, p);
+    if (GATHER) {
+        const int goff = UNPACKED ? n * a.w : 0;
+        for (int j = 0; j < a.n_out; ++j)
+            ss::st_stream_u4(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k, p);
+    }
+}
+
+template <bool UNPACKED, int GATHER, bool WRITE_G>
+__device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab, int slot,
+                                            int64_t f, int64_t k) {
+    const int n = a.N;
+    float s = ss::bf16_to_f32(*grad_ptr<UNPACKED>(a, tab, 0, slot, f, k));
+    for (int r = 1; r < n; ++r) s = __fadd_rn(s, ss::bf16_to_f32(*grad_ptr<UNPACKED>(a, tab, r, slot, f, k)));
+    const float g = __fdiv_rn(s, (float)n);
+    if (WRITE_G) a.gout[f] = g;
+    float th = a.master[f], m = a.exp_avg[f], v = a.exp_avg_sq[f];
+    adamw_elem(g, th, m, v, a.c);
+    a.master[f] = th;
+    a.exp_avg[f] = m;
+    a.exp_avg_sq[f] = v;
+    const uint16_t p = ss::f32_to_bf16(th);
+    a.shards[f] = p;
+    if (GATHER) {
+        const int goff = UNPACKED ? n * a.w : 0;
+        for (int j = 0; j < a.n_out; ++j) static_cast<uint16_t*>(tab.p[goff + j * a.w + slot])[k] = p;
+    }
+}
+
+// kSub CTAs per data tile (blockIdx.y): each takes one 8-element vector per
+// thread of its quarter of the tile, so CTAs stay short-lived like the flat
+// reduce-scatter kernel's.
+constexpr int kSub = ss::kTileBytes / 2 / 8 / kThreads;  // 4 for 16 KiB bf16 tiles
+static_assert(kSub * kThreads * 8 * 2 == ss::kTileBytes, "tile split");
+
+template <int NR, bool UNPACKED, int GATHER, bool WRITE_G>
+__global__ void __launch_bounds__(kThreads, 3)
+fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
+                  StepArgs a, PtrTab tab) {
+    constexpr int64_t T = ss::kTileBytes / 2;
+    const ss::Tile tl = tiles[t_lo + blockIdx.x];
+    const ss::Seg sg = segs[tl.seg];
+    const int64_t off = (int64_t)tl.idx * T;
+    const int64_t len = sg.len - off < T ? sg.len - off : T;
+    constexpr int64_t kPart = T / kSub;  // elements of this CTA's part of the tile
+    const int slot = sg.param - a.param_base;
+    const int64_t f0 = sg.packed_off + off;  // packed index of the tile's first element
+    const int64_t k0 = sg.param_off + off;   // index inside the parameter tensor
+    // vector path: the packed index and every per-parameter pointer 16-byte aligned
+    bool vec = (f0 & 7) == 0;
+    if (UNPACKED)
+        for (int r = 0; r < a.N; ++r)
+            vec &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k0) & 15u) == 0);
+    if (GATHER) {
+        const int goff = UNPACKED ? a.N * a.w : 0;
+        for (int j = 0; j < a.n_out; ++j)
+            vec &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + j * a.w + slot]) + k0) & 15u) == 0);
+    }
+    // this CTA's part [p0, p1) of the tile
+    const int64_t p0 = (int64_t)blockIdx.y * kPart;
+    const int64_t p1 = p0 + kPart < len ? p0 + kPart : len;
+    if (p0 >= p1) return;
+    if (vec) {
+        const int64_t nvec = (p1 - p0) / 8;
+        for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
+            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + p0 + 8 * q, k0 + p0 + 8 * q);
+        for (int64_t e = p0 + 8 * nvec + threadIdx.x; e < p1; e += kThreads)
+            step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
+    } else {
+        for (int64_t e = p0 + threadIdx.x; e < p1; e += kThreads)
+            step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
+    }
+}
+
+using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
+
+template <int NR, bool U>
+Kern pick3(int gather, bool wg) {
+    if (gather == 0) return wg ? fused_step_kernel<NR, U, 0, true> : fused_step_kernel<NR, U, 0, false>;
+    return wg ? fused_step_kernel<NR, U, 1, true> : fused_step_kernel<NR, U, 1, false>;
+}
+
+template <bool U>
+Kern pick2(int N, int gather, bool wg) {
+    return N == 8 ? pick3<8, U>(gather, wg) : pick3<0, U>(gather, wg);
+}
+
+AdamCoef make_coef(const ss_adamw* hp) {
+    AdamCoef c;
+    const double t = (double)hp->step;
+    const double bc1 = 1.0 - std::pow(hp->beta1, t);
+    const double bc2 = 1.0 - std::pow(hp->beta2, t);
+    c.decay = (float)(1.0 - hp->lr * hp->weight_decay);
+    c.b1 = (float)hp->beta1;
+    c.omb1 = (float)(1.0 - hp->beta1);
+    c.b2 = (float)hp->beta2;
+    c.omb2 = (float)(1.0 - hp->beta2);
+    c.step_size = (float)(hp->lr / bc1);
+    c.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    c.eps = (float)hp->eps;
+    return c;
+}
+
+}  // namespace
+
+extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int group,
+                                 ss_stream_t stream) {
+    if (!plan || !s) return SS_EINVAL;
+    if (!plan->has_dev) return SS_ENODEVICE;
+    if (plan->eb != 2) return SS_EINVAL;
+    int64_t lo, hi;
+    if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;
+    const int N = plan->N, n = plan->n;
+    const bool unpacked = s->rank_param_grads != nullptr;
+    if (unpacked == (s->rank_grads != nullptr)) return SS_EINVAL;  // exactly one gradient source
+    if (!s->hp || !s->master || !s->exp_avg || !s->exp_avg_sq || !s->param_shards) return SS_EINVAL;
+    const ss_adamw* hp = s->hp;
+    if (hp->step < 1 || !(hp->beta1 >= 0.0 && hp->beta1 < 1.0) || !(hp->beta2 >= 0.0 && hp->beta2 < 1.0) ||
+        !(hp->eps >= 0.0) || !std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay))
+        return SS_EINVAL;
+    if (s->n_out < 0 || s->n_out > SS_MAX_REPLICAS || (s->n_out > 0 && !s->params_out))
+        return SS_EINVAL;
+    const void* bufs[5] = {s->master, s->exp_avg, s->exp_avg_sq, s->param_shards, s->reduced_grad_out};
+    for (const void* b : bufs)
+        if (b && !ss::aligned(b, 16)) return SS_EALIGN;
+    const int pa = group < 0 ? 0 : plan->gfirst[group];
+    const int pb = group < 0 ? n : plan->gfirst[group] + plan->gnp[group];
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (!unpacked) {
+        for (int r = 0; r < N; ++r) {
+            if (!s->rank_grads[r] && hi > lo) return SS_EINVAL;
+            if (!ss::aligned(s->rank_grads[r], 16)) return SS_EALIGN;
+            a.packed_grads.p[r] = s->rank_grads[r];
+        }
+    }
+    for (int i = pa; i < pb; ++i) {
+        if (plan->numel[i] == 0) continue;
+        for (int r = 0; unpacked && r < N; ++r) {
+            const void* q = s->rank_param_grads[(size_t)r * n + i];
+            if (!q) return SS_EINVAL;
+            if (!ss::aligned(q, 2)) return SS_EALIGN;
+        }
+        for (int j = 0; j < s->n_out; ++j) {
+            const void* q = s->params_out[(size_t)j * n + i];
+            if (!q) return SS_EINVAL;
+            if (!ss::aligned(q, 2)) return SS_EALIGN;
+        }
+    }
+    a.master = s->master;
+    a.exp_avg = s->exp_avg;
+    a.exp_avg_sq = s->exp_avg_sq;
+    a.shards = static_cast<uint16_t*>(s->param_shards);
+    a.gout = s->reduced_grad_out;
+    a.N = N;
+    a.n_out = s->n_out;
+    a.c = make_coef(hp);
+    const int per_param = (unpacked ? N : 0) + s->n_out;
+    if (per_param > kTab) return SS_EINVAL;
+    const int wmax = per_param > 0 ? kTab / per_param : (pb - pa > 0 ? pb - pa : 1);
+    Kern fn = unpacked ? pick2<true>(N, s->n_out > 0, s->reduced_grad_out != nullptr)
+                       : pick2<false>(N, s->n_out > 0, s->reduced_grad_out != nullptr);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    PtrTab tab;
+    constexpr int64_t kMaxGrid = (int64_t)1 << 30;
+    auto launch = [&](const ss::Tile* tiles, int64_t t_lo, int64_t t_hi) -> int {
+        for (int64_t t = t_lo; t < t_hi; t += kMaxGrid) {
+            const int64_t cnt = t_hi - t < kMaxGrid ? t_hi - t : kMaxGrid;
+            fn<<<dim3((unsigned)cnt, kSub), kThreads, 0, st>>>(tiles, t, plan->d_data, a, tab);
+            int rc = ss::check_launch();
+            if (rc) return rc;
+        }
+        return SS_OK;
+    };
+    auto fill = [&](int wa, int wb) {
+        a.param_base = wa;
+        a.w = wb - wa;
+        std::memset(&tab, 0, sizeof tab);
+        for (int i = wa; i < wb; ++i) {
+            for (int r = 0; unpacked && r < N; ++r)
+                tab.p[r * a.w + (i - wa)] = const_cast<void*>(s->rank_param_grads[(size_t)r * n + i]);
+            const int goff = unpacked ? N * a.w : 0;
+            for (int j = 0; j < s->n_out; ++j)
+                tab.p[goff + j * a.w + (i - wa)] = s->params_out[(size_t)j * n + i];
+        }
+    };
+    if (pb - pa <= wmax) {
+        // every parameter's pointers fit one table: walk the tiles in packed
+        // order, so consecutive CTAs stream the gradient / state / shard
+        // buffers front to back
+        fill(pa, pb);
+        const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
+        return launch(plan->d_packed_tiles, plan->group_ptile[ga], plan->group_ptile[gb]);
+    }
+    for (int wa = pa; wa < pb; wa += wmax) {
+        const int wb = wa + wmax < pb ? wa + wmax : pb;
+        const int s_lo = plan->param_seg[wa], s_hi = plan->param_seg[wb];
+        if (s_hi <= s_lo) continue;
+        fill(wa, wb);
+        int rc = launch(plan->d_data_tiles, plan->data_seg_tile[s_lo], plan->data_seg_tile[s_hi]);
+        if (rc) return rc;
+    }
+    return SS_OK;
+}

@@ -1,0 +1,226 @@
+"""GPU parity of the one-pass step (fsdp_sharded_step) through the C ABI.
+
+The fused kernel runs the same fp32 operations in the same order as
+fsdp_reduce_scatter_adamw, so its state and shards must be bit-identical to
+the two-call path, and its per-parameter outputs bit-identical to
+fsdp_all_gather_unpack of its own shards; both are also checked against the
+oracle.  Gradients come either from packed rank buffers or straight from the
+per-parameter gradient tensors (fused copy-in) -- the two must agree bit for
+bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.gpu_common import Setup, guarded, guards_intact
+from tests.helpers import check_adamw_state, check_bf16_params, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ss():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sharded_state_gb300 as ss
+    return ss
+
+
+def _hp(step):
+    hp = W.adamw_hparams(step)
+    return {k: hp[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay")}
+
+
+CASES = [("tiny_mlp", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
+         ("awkward1d_false_N7", W.awkward_1d(7, W.FLAT_ORIG_FALSE, torch.bfloat16)),
+         ("awkward1d_true_N5", W.awkward_1d(5, W.FLAT_ORIG_TRUE, torch.bfloat16)),
+         ("awkward2d_N3", W.awkward_2d(3)),
+         ("small_llama_N3", W.llama_1b2(world_size=3, layers=3, hidden=40, ffn=72, vocab=100)),
+         ("small_llama_N8", W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)),
+         ("per_param_N12", W.ParamSet([f"p{i}" for i in range(4)], [(130, 3), (64,), (0, 4), (257, 8)],
+                                      [4], 12, W.PER_PARAM_DIM0, torch.bfloat16, seed=11))]
+
+
+def _state(ss, su):
+    shards = torch.empty(su.total, dtype=torch.bfloat16, device="cuda")
+    ss.fsdp_pack(su.plan, su.params, shards)
+    master = torch.empty(su.total, device="cuda")
+    m = torch.empty_like(master)
+    v = torch.empty_like(master)
+    ss.fsdp_init_master(su.plan, shards, master, m, v)
+    return shards, master, m, v
+
+
+@pytest.mark.parametrize("name,ps", CASES, ids=[c[0] for c in CASES])
+def test_sharded_step_matches_two_calls_and_oracle(ss, name, ps):
+    su = Setup(ss, ps)
+    N, total, n = su.N, su.total, len(su.params)
+    grads_cpu = W.make_rank_grads(ps)
+    grads_params = [[g.cuda() for g in rank] for rank in grads_cpu]
+    packed = []
+    for r in range(N):
+        b = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+        ss.fsdp_pack(su.plan, grads_params[r], b)
+        packed.append(b)
+    n_out = min(N, 3)
+    # A: two calls
+    sa, ma, mma, va = _state(ss, su)
+    red_a = torch.zeros(total, device="cuda")
+    outs_a = [torch.empty_like(p) for _ in range(n_out) for p in su.params]
+    # B: one pass, packed gradients; C: one pass, per-parameter gradients
+    sb, mb, mmb, vb = _state(ss, su)
+    sc, mc, mmc, vc = _state(ss, su)
+    red_b = torch.zeros(total, device="cuda")
+    outs_b, wholes = [], []
+    for _ in range(n_out):
+        for p in su.params:
+            o, w = guarded(p.numel(), torch.bfloat16)
+            outs_b.append(o)
+            wholes.append(w)
+    outs_c = [torch.empty_like(p) for _ in range(n_out) for p in su.params]
+    flat_param_grads = [g for rank in grads_params for g in rank]
+    torch.cuda.synchronize()
+    for step in (1, 2):
+        hp = ss.adamw_params(step=step, **_hp(step))
+        ss.fsdp_reduce_scatter_adamw(su.plan, packed, ma, mma, va, sa, hp, red_a)
+        ss.fsdp_all_gather_unpack(su.plan, sa, outs_a, n_out=n_out)
+        ss.fsdp_sharded_step(su.plan, mb, mmb, vb, sb, hp, rank_grads=packed, params_out=outs_b,
+                             n_out=n_out, reduced_grad_out=red_b)
+        ss.fsdp_sharded_step(su.plan, mc, mmc, vc, sc, hp, rank_param_grads=flat_param_grads,
+                             params_out=outs_c, n_out=n_out)
+        torch.cuda.synchronize()
+        assert all(guards_intact(w) for w in wholes)
+        for x, y, z in ((sa, sb, sc), (ma, mb, mc), (mma, mmb, mmc), (va, vb, vc)):
+            np.testing.assert_array_equal(to_np(x).view(np.uint8), to_np(y).view(np.uint8))
+            np.testing.assert_array_equal(to_np(x).view(np.uint8), to_np(z).view(np.uint8))
+        for x, y, z in zip(outs_a, outs_b, outs_c):
+            np.testing.assert_array_equal(to_np(x), to_np(y))
+            np.testing.assert_array_equal(to_np(x), to_np(z))
+    # the reduced gradient on parameter elements equals the oracle's reduce-scatter
+    ones = su.oracle_pack([np.full(p.numel(), 0x3F80, np.uint16) for p in su.params])
+    data = ones != 0
+    want = np.concatenate([oracle.reduce_scatter(N, g["shard_numel"],
+                                                 [to_np(b)[g["base"]:g["base"] + N * g["shard_numel"]]
+                                                  for b in packed]) for g in su.groups]) \
+        if su.groups else np.zeros(0, np.float32)
+    np.testing.assert_array_equal(to_np(red_b)[data], want[data])
+    assert not to_np(red_b)[~data].any()          # pads never written
+
+
+def test_sharded_step_windows_and_groups(ss):
+    # N=7 per-parameter grads + 7 outputs: 14 pointers x 200 params > 2048, so the call
+    # splits into parameter windows; group-by-group calls cover the plan in packed order
+    ps = W.awkward_1d(7, W.FLAT_ORIG_FALSE, torch.bfloat16)
+    ps.groups = [50, 0, 75, 75]
+    su = Setup(ss, ps)
+    N = su.N
+    grads = [[g.cuda() for g in rank] for rank in W.make_rank_grads(ps)]
+    flat = [g for rank in grads for g in rank]
+    packed = []
+    for r in range(N):
+        b = torch.empty(su.total, dtype=torch.bfloat16, device="cuda")
+        ss.fsdp_pack(su.plan, grads[r], b)
+        packed.append(b)
+    results = []
+    for mode in ("two_calls", "windows", "groups"):
+        shards, master, m, v = _state(ss, su)
+        outs = [torch.empty_like(p) for _ in range(N) for p in su.params]
+        hp = ss.adamw_params(step=1)
+        if mode == "two_calls":
+            ss.fsdp_reduce_scatter_adamw(su.plan, packed, master, m, v, shards, hp)
+            ss.fsdp_all_gather_unpack(su.plan, shards, outs, n_out=N)
+        elif mode == "windows":
+            ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_param_grads=flat,
+                                 params_out=outs, n_out=N)
+        else:
+            for g in range(len(ps.groups)):
+                ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_grads=packed,
+                                     params_out=outs, n_out=N, group=g)
+        torch.cuda.synchronize()
+        results.append([to_np(t) for t in [shards, master, m, v] + outs])
+    for other in results[1:]:
+        for x, y in zip(results[0], other):
+            np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_sharded_step_state_against_oracle(ss):
+    ps = W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)
+    su = Setup(ss, ps)
+    N, total = su.N, su.total
+    shards, master, m, v = _state(ss, su)
+    grads_cpu = W.make_rank_grads(ps)
+    flat = [g.cuda() for rank in grads_cpu for g in rank]
+    packed_np = [su.oracle_pack([to_np(g) for g in rank]) for rank in grads_cpu]
+    outs = [torch.empty_like(p) for p in su.params]
+    for step in (1, 2, 3):
+        pm, pmm, pv = to_np(master), to_np(m), to_np(v)
+        ss.fsdp_sharded_step(su.plan, master, m, v, shards, ss.adamw_params(step=step, **_hp(step)),
+                             rank_param_grads=flat, params_out=outs, n_out=1)
+        torch.cuda.synchronize()
+        om, omm, ov = pm.copy(), pmm.copy(), pv.copy()
+        o_params, o_red = oracle.reduce_scatter_adamw(N, su.info.shard_numel, packed_np, om, omm, ov,
+                                                      step=step, **_hp(step))
+        check_adamw_state(to_np(master), to_np(m), to_np(v), om, omm, ov, pm, pmm, o_red)
+        check_bf16_params(to_np(shards), o_params, to_np(master), om, pm)
+        want = su.oracle_unpack(to_np(shards))[0]
+        for o, w in zip(outs, want):
+            np.testing.assert_array_equal(to_np(o), w)
+
+
+def test_sharded_step_full_size_equals_two_calls(ss):
+    ps = W.llama_1b2()
+    su = Setup(ss, ps, make_values=False)
+    total, N = su.total, su.N
+    gen = torch.Generator(device="cuda").manual_seed(4)
+    init = (torch.randn(total, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+    grads = W.make_packed_rank_grads(N, total, 1e-3, 4, device="cuda")
+    res = []
+    for mode in ("two_calls", "one_pass"):
+        shards = init.clone()
+        master = torch.empty(total, device="cuda")
+        m = torch.empty_like(master)
+        v = torch.empty_like(master)
+        ss.fsdp_init_master(su.plan, shards, master, m, v)
+        outs = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in ps.shapes]
+        for step in (1, 2):
+            hp = ss.adamw_params(step=step)
+            if mode == "two_calls":
+                ss.fsdp_reduce_scatter_adamw(su.plan, grads, master, m, v, shards, hp)
+                ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+            else:
+                ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_grads=grads,
+                                     params_out=outs, n_out=1)
+        torch.cuda.synchronize()
+        res.append((shards, master, m, v, outs))
+    a, b = res
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    for x, y in zip(a[1:4], b[1:4]):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    for x, y in zip(a[4], b[4]):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    del res, a, b, grads
+    torch.cuda.empty_cache()
+
+
+def test_sharded_step_argument_errors(ss):
+    su = Setup(ss, W.tiny_mlp())
+    shards, master, m, v = _state(ss, su)
+    g = [torch.empty(su.total, dtype=torch.bfloat16, device="cuda")] * 2
+    hp = ss.adamw_params()
+    with pytest.raises(ss.ShardStateError) as e:   # neither gradient source
+        ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp)
+    assert e.value.status == ss.SS_EINVAL
+    with pytest.raises(ss.ShardStateError) as e:   # both
+        ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_grads=g,
+                             rank_param_grads=[p for p in su.params] * 2)
+    assert e.value.status == ss.SS_EINVAL
+    with pytest.raises(ss.ShardStateError) as e:
+        ss.fsdp_sharded_step(su.plan, master[1:], m, v, shards, hp, rank_grads=g)
+    assert e.value.status == ss.SS_EALIGN
+    f32plan = ss.fsdp_plan_create(ss.SS_FLAT_ORIG_TRUE, 2, 4, [16])
+    with pytest.raises(ss.ShardStateError) as e:
+        ss.fsdp_sharded_step(f32plan, master, m, v, master, hp, rank_grads=[master, master])
+    assert e.value.status == ss.SS_EINVAL
+    torch.cuda.synchronize()
