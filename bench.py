@@ -630,6 +630,46 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     _row("one-pass step with fused copy-in: N per-parameter grad sets -> RS+AdamW -> shards + "
          "unpacked params (1.2B, N=8)", P, "params/s", ms, mn, (2 * N + 28) * P, peak)
     del rank_sets, flat_pg
+    # F2: FULL_SHARD gathers the parameters twice per iteration (forward and
+    # backward), SHARD_GRAD_OP once ("FSDP1 vs FSDP2", strategy table)
+    def full_shard():
+        st.all_gather()
+        st.all_gather()
+        st.rs_adamw()
+
+    def shard_grad_op():
+        st.all_gather()
+        st.rs_adamw()
+    for name, fn, nag in (("FULL_SHARD", full_shard, 2), ("SHARD_GRAD_OP", shard_grad_op, 1)):
+        ms, mn = _time_stream(fn, K)
+        _row(f"strategy {name}: {nag} all-gather(s) + RS+AdamW per iteration (1.2B, N=8)", P,
+             "params/s", ms, mn, (2 * N + 26) * total + nag * 4 * P, peak,
+             extra={"all_gathers": nag})
+    # F3: gradient accumulation over 4 micro-batches (same gradients each time)
+    accum = torch.empty(total, device="cuda")
+    kmic = 4
+
+    def accumulate_step():
+        st.t += 1
+        hp = ss.adamw_params(step=st.t)
+        for j in range(kmic):
+            last = j == kmic - 1
+            ss.fsdp_reduce_scatter_accumulate(st.plan, st._grads_arr, accum, j, kmic, st.master,
+                                              st.m, st.v, st.shards, hp if last else None)
+    ms, mn = _time_stream(accumulate_step, max(K // 4, 5))
+    acc_bytes = (2 * N + 4) + 2 * (2 * N + 8) + (2 * N + 30)
+    _row(f"gradient accumulation: {kmic} micro-batches per optimizer step (1.2B, N=8)", P,
+         "params/s", ms, mn, acc_bytes * total, peak, extra={"micro_batches": kmic,
+                                                             "ms_per_micro_batch": ms / kmic})
+    del accum
+    # F4: AdamW without fp32 master weights (bf16 shard updated in place)
+    def no_master():
+        st.t += 1
+        ss.fsdp_reduce_scatter_adamw(st.plan, st._grads_arr, None, st.m, st.v, st.shards,
+                                     ss.adamw_params(step=st.t))
+    ms, mn = _time_stream(no_master, K)
+    _row("RS + AdamW without fp32 master (2 B params + 8 B moments, 1.2B, N=8)", P, "params/s",
+         ms, mn, (2 * N + 20) * total, peak)
     st8 = st
     outs8 = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for _ in range(N)
              for s in ps.shapes]

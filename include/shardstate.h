@@ -237,6 +237,12 @@ int fsdp_init_master(const ss_plan* plan, const void* param_shards, float* maste
  *                     r's packed gradient buffer (total_numel elements of the
  *                     plan dtype, as fsdp_pack writes it).
  *   master, exp_avg, exp_avg_sq   total_numel floats, updated in place.
+ *                     master may be NULL: the recipe without fp32 master
+ *                     weights ("FSDP1 vs FSDP2" ledger: bf16 parameters and
+ *                     gradients plus 8 B of Adam moments per parameter).
+ *                     theta is then the parameter shard itself, widened to
+ *                     fp32, updated, and rounded back in place (2N + 20 bytes
+ *                     per element instead of 2N + 26).
  *   param_shards      total_numel elements of the plan dtype, written.
  *   hp                AdamW hyper-parameters; NULL = reduce-scatter only
  *                     (state and shards untouched; reduced_grad_out required).
@@ -249,6 +255,29 @@ int fsdp_reduce_scatter_adamw(const ss_plan* plan, const void* const* rank_grads
                               float* exp_avg, float* exp_avg_sq, void* param_shards,
                               const ss_adamw* hp, float* reduced_grad_out, int group,
                               ss_stream_t stream);
+
+/*
+ * Reduce-scatter with gradient accumulation over num_micro micro-batches per
+ * optimizer step ("Scaling data parallel", section 5: accumulate gradients
+ * across micro-batches and synchronise once, using their mean; section 9.2:
+ * with fp32 accumulation each rank keeps an fp32 gradient for its own shard
+ * and adds every reduce-scatter result into it).  With RS_j the reduce-scatter
+ * of micro-batch j (as fsdp_reduce_scatter_adamw computes it):
+ *   micro_step 0:                 accum = RS_0
+ *   0 < micro_step < num_micro-1: accum = accum + RS_j       (fp32)
+ *   micro_step = num_micro-1:     g = (accum + RS_j) / num_micro, then AdamW
+ *                                 exactly as fsdp_reduce_scatter_adamw
+ *                                 (reduced_grad_out, if given, receives g)
+ * num_micro = 1 is fsdp_reduce_scatter_adamw.  accum: total_numel floats
+ * (16-byte aligned), left holding acc_{k-1} after the last micro-batch.
+ * master may be NULL (no-master recipe).  bf16 plans only.
+ * Errors: SS_EINVAL, SS_EALIGN, SS_ENODEVICE, SS_ECUDA.
+ */
+int fsdp_reduce_scatter_accumulate(const ss_plan* plan, const void* const* rank_grads,
+                                   float* accum, int micro_step, int num_micro, float* master,
+                                   float* exp_avg, float* exp_avg_sq, void* param_shards,
+                                   const ss_adamw* hp, float* reduced_grad_out, int group,
+                                   ss_stream_t stream);
 
 /*
  * All-gather of the N rank shards followed by unpacking into full

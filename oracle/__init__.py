@@ -73,6 +73,11 @@ def _load():
                                              ctypes.POINTER(vp), vp, vp, vp, vp, vp, dbl, dbl,
                                              dbl, dbl, dbl, ctypes.c_int64]
     lib.sso_reduce_scatter_adamw.restype = None
+    lib.sso_accumulate.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(vp),
+                                   vp, ctypes.c_int]
+    lib.sso_accumulate.restype = None
+    lib.sso_accumulated_grad.argtypes = [ctypes.c_int64, vp, ctypes.c_int, vp]
+    lib.sso_accumulated_grad.restype = None
     lib.sso_init_master.argtypes = [ctypes.c_int64, vp, ctypes.c_int, vp, vp, vp]
     lib.sso_init_master.restype = None
     lib.sso_ddp_buckets.argtypes = [ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int64,
@@ -216,6 +221,30 @@ def adamw(grad: np.ndarray, master: np.ndarray, exp_avg: np.ndarray, exp_avg_sq:
     lib.sso_adamw(grad.size, _vp(grad), _vp(master), _vp(exp_avg), _vp(exp_avg_sq), _vp(out),
                   elem_bytes, lr, beta1, beta2, eps, weight_decay, step)
     return out[:grad.size]
+
+
+def accumulate(world_size: int, shard_numel: int, rank_bufs: Sequence[np.ndarray],
+               accum: Optional[np.ndarray]) -> np.ndarray:
+    """One micro-batch of gradient accumulation: returns acc = RS (accum None)
+    or accum + RS, fp32, all ranks' shards side by side."""
+    lib = _load()
+    eb = 2 if rank_bufs[0].dtype == np.uint16 else 4
+    total = world_size * shard_numel
+    bufs = [np.ascontiguousarray(b) for b in rank_bufs]
+    out = np.empty(max(total, 1), np.float32)
+    if accum is not None:
+        out[:total] = accum
+    lib.sso_accumulate(world_size, shard_numel, eb, _vparr(bufs), _vp(out),
+                       1 if accum is None else 0)
+    return out[:total]
+
+
+def accumulated_grad(accum: np.ndarray, num_micro: int) -> np.ndarray:
+    lib = _load()
+    acc = np.ascontiguousarray(accum, dtype=np.float32)
+    out = np.empty(max(acc.size, 1), np.float32)
+    lib.sso_accumulated_grad(acc.size, _vp(acc), num_micro, _vp(out))
+    return out[:acc.size]
 
 
 def init_master(param_shards: np.ndarray):

@@ -70,6 +70,23 @@ def rank_mean_grads(params, x, t, splits: Sequence[int], token_weighted: bool = 
     return acc
 
 
+def accumulated_dp_grads(params, x, t, world_size: int, micro_batches: int):
+    """Gradient accumulation on top of data parallelism: the batch is split into
+    `micro_batches` consecutive micro-batches, each split evenly over
+    `world_size` ranks; the step's gradient is the mean over micro-batches of
+    the rank-mean gradients ("Scaling data parallel", sections 2.2 and 5:
+    data parallelism is gradient accumulation done in parallel)."""
+    B = x.shape[0]
+    mb = B // micro_batches
+    acc = {k: np.zeros_like(v) for k, v in params.items()}
+    for j in range(micro_batches):
+        xs, ts = x[j * mb:(j + 1) * mb], t[j * mb:(j + 1) * mb]
+        g = rank_mean_grads(params, xs, ts, [mb // world_size] * world_size)
+        for k in acc:
+            acc[k] += g[k] / micro_batches
+    return acc
+
+
 def make_problem(D: int = 64, F: int = 128, B: int = 16, seed: int = 0):
     rng = np.random.default_rng(seed)
     params = {

@@ -417,6 +417,35 @@ void sso_reduce_scatter_adamw(int N, int64_t c, int elem_bytes, const void* cons
 }
 
 /* ------------------------------------------------------------------------ */
+/* gradient accumulation over micro-batches                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Gradient accumulation ("Scaling data parallel", section 5 with section
+ * 9.2): the k micro-batches of one optimizer step each produce a
+ * reduce-scatter; with fp32 accumulation each rank keeps an fp32 buffer for
+ * its own shard and adds every micro-batch's reduce-scatter result into it;
+ * the optimizer uses the average over micro-batches (section 1: in practice
+ * the mean, so the result does not depend on the number of steps).
+ *   acc_1 = RS_1;  acc_j = acc_{j-1} + RS_j  (fp32, in micro-batch order)
+ *   g = acc_k / k  (one IEEE fp32 division)
+ * first != 0 starts a new accumulation (acc = RS), otherwise acc += RS.
+ */
+void sso_accumulate(int N, int64_t c, int elem_bytes, const void* const* rank_bufs, float* accum,
+                    int first) {
+    int64_t total = (int64_t)N * c;
+    float* rs = (float*)malloc((size_t)(total > 0 ? total : 1) * sizeof(float));
+    sso_reduce_scatter(N, c, elem_bytes, rank_bufs, rs);
+    for (int64_t f = 0; f < total; ++f) accum[f] = first ? rs[f] : accum[f] + rs[f];
+    free(rs);
+}
+
+void sso_accumulated_grad(int64_t count, const float* accum, int num_micro, float* grad) {
+    const float k = (float)num_micro;
+    for (int64_t f = 0; f < count; ++f) grad[f] = accum[f] / k;
+}
+
+/* ------------------------------------------------------------------------ */
 /* DDP gradient bucketing                                                    */
 /* ------------------------------------------------------------------------ */
 

@@ -40,7 +40,8 @@ EXPORTED = ("fsdp_plan_create", "fsdp_plan_layout", "fsdp_plan_info", "fsdp_plan
             "fsdp_plan_group", "fsdp_plan_destroy", "fsdp_pack", "fsdp_init_master",
             "fsdp_reduce_scatter_adamw", "fsdp_all_gather_unpack", "ddp_bucket_pack_average",
             "ddp_bucket_assign", "ss_strerror", "ss_last_cuda_error", "ss_version",
-            "ss_launch_count", "ddp_bucket_pack_average_noalloc", "fsdp_sharded_step")
+            "ss_launch_count", "ddp_bucket_pack_average_noalloc", "fsdp_sharded_step",
+            "fsdp_reduce_scatter_accumulate")
 
 
 class ShardStateError(RuntimeError):
@@ -107,6 +108,8 @@ def _load() -> ctypes.CDLL:
                                              ctypes.POINTER(i32), vp], i32),
         "ddp_bucket_assign": ([i32, i64p, i32, ctypes.c_size_t, ctypes.POINTER(i32)], i32),
         "fsdp_sharded_step": ([vp, ctypes.POINTER(_Step), i32, vp], i32),
+        "fsdp_reduce_scatter_accumulate": ([vp, vpp, vp, i32, i32, vp, vp, vp, vp,
+                                            ctypes.POINTER(AdamW), vp, i32, vp], i32),
         "ss_strerror": ([i32], ctypes.c_char_p),
         "ss_last_cuda_error": ([], i32),
         "ss_version": ([], ctypes.c_char_p),
@@ -307,6 +310,19 @@ def fsdp_reduce_scatter_adamw(plan: Plan, rank_grads: Sequence, master, exp_avg,
         plan, _ptr_array(rank_grads), _addr(master), _addr(exp_avg), _addr(exp_avg_sq),
         _addr(param_shards), ctypes.byref(hp) if hp is not None else None, _addr(reduced_grad_out),
         group, _stream(stream)))
+
+
+def fsdp_reduce_scatter_accumulate(plan: Plan, rank_grads: Sequence, accum, micro_step: int,
+                                   num_micro: int, master=None, exp_avg=None, exp_avg_sq=None,
+                                   param_shards=None, hp: Optional[AdamW] = None,
+                                   reduced_grad_out=None, group: int = -1, stream=None) -> None:
+    """Micro-batch `micro_step` of `num_micro`: accumulate the reduce-scatter in
+    fp32, and on the last micro-batch run AdamW on the micro-batch mean."""
+    _check("fsdp_reduce_scatter_accumulate", _lib.fsdp_reduce_scatter_accumulate(
+        plan, _ptr_array(rank_grads), _addr(accum), micro_step, num_micro, _addr(master),
+        _addr(exp_avg), _addr(exp_avg_sq), _addr(param_shards),
+        ctypes.byref(hp) if hp is not None else None, _addr(reduced_grad_out), group,
+        _stream(stream)))
 
 
 def fsdp_all_gather_unpack(plan: Plan, param_shards, params_out: Sequence, n_out: int = 1,

@@ -105,6 +105,14 @@ def check_bf16_params(gpu_bits, ref_bits, gpu_master, ref_master, prev_master):
     import oracle
     gpu_bits = np.asarray(gpu_bits, np.uint16)
     np.testing.assert_array_equal(gpu_bits, oracle.bf16_round(np.asarray(gpu_master, np.float32)))
+    return check_bf16_close(gpu_bits, ref_bits, ref_master, prev_master)
+
+
+def check_bf16_close(gpu_bits, ref_bits, ref_master, prev_master):
+    """Part (b) of check_bf16_params alone (for the recipe without an fp32
+    master, where the GPU keeps no fp32 value to compare the cast against)."""
+    import oracle
+    gpu_bits = np.asarray(gpu_bits, np.uint16)
     d = bf16_ulp_distance(gpu_bits, np.asarray(ref_bits, np.uint16))
     far = d > 1
     if not far.any():

@@ -563,3 +563,52 @@ def test_dp_unequal_split_needs_token_weighting():
     k = "W_in"
     assert np.abs(plain[k] - full[k]).max() > 1e-6 * np.abs(full[k]).max()
     assert np.abs(weighted[k] - full[k]).max() <= 1e-12 * np.abs(full[k]).max()
+
+
+# ---------------------------------------------------------------------------
+# gradient accumulation
+# ---------------------------------------------------------------------------
+
+def test_accumulation_single_micro_batch_is_reduce_scatter():
+    rng = np.random.default_rng(21)
+    N, c = 5, 77
+    bufs = [_bits(torch.from_numpy(rng.normal(0, 1e-2, N * c).astype(np.float32)).to(torch.bfloat16))
+            for _ in range(N)]
+    acc = oracle.accumulate(N, c, bufs, None)
+    np.testing.assert_array_equal(oracle.accumulated_grad(acc, 1), oracle.reduce_scatter(N, c, bufs))
+
+
+def test_accumulation_identical_micro_batches_average_exactly():
+    # acc = RS + RS = 2 RS exactly, and 2 RS / 2 = RS exactly
+    rng = np.random.default_rng(22)
+    N, c = 8, 64
+    bufs = [_bits(torch.from_numpy(rng.normal(0, 1e-3, N * c).astype(np.float32)).to(torch.bfloat16))
+            for _ in range(N)]
+    acc = oracle.accumulate(N, c, bufs, None)
+    acc = oracle.accumulate(N, c, bufs, acc)
+    np.testing.assert_array_equal(oracle.accumulated_grad(acc, 2), oracle.reduce_scatter(N, c, bufs))
+
+
+def test_accumulation_hand_example():
+    # N = 2, k = 3 micro-batches, one element per shard (c = 1): rank values
+    # micro-batch 1: (1, 3) -> mean 2; 2: (4, 8) -> 6; 3: (-2, 2) -> 0
+    # acc = 2 + 6 + 0 = 8, g = 8 / 3 rounded to fp32
+    mbs = [(1.0, 3.0), (4.0, 8.0), (-2.0, 2.0)]
+    acc = None
+    for a, b in mbs:
+        bufs = [_bits(torch.tensor([a, a], dtype=torch.float32).to(torch.bfloat16)),
+                _bits(torch.tensor([b, b], dtype=torch.float32).to(torch.bfloat16))]
+        acc = oracle.accumulate(2, 1, bufs, acc)
+    np.testing.assert_array_equal(acc, np.array([8.0, 8.0], np.float32))
+    np.testing.assert_array_equal(oracle.accumulated_grad(acc, 3),
+                                  np.array([8.0, 8.0], np.float32) / np.float32(3))
+
+
+@pytest.mark.parametrize("N,k", [(2, 2), (4, 2), (2, 4)])
+def test_accumulated_dp_equals_large_batch(N, k):
+    params, x, t = dp_equivalence.make_problem(B=16, seed=N * 10 + k)
+    _, full = dp_equivalence.loss_and_grads(params, x, t)
+    acc = dp_equivalence.accumulated_dp_grads(params, x, t, N, k)
+    for key in full:
+        rel = np.abs(acc[key] - full[key]).max() / max(np.abs(full[key]).max(), 1e-300)
+        assert rel <= 1e-12
