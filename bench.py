@@ -194,11 +194,19 @@ def barrier(dist):
 
 
 def max_over_ranks(dist, x: float) -> float:
+    """Largest value over ranks (the slowest replica's time)."""
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(units_per_rank: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units every replica processed over the slowest
+    replica's time (replicas each run the full workload: weak scaling)."""
+    return units_per_rank * steps * world / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------------------
@@ -329,7 +337,7 @@ def run_native(args, world, rank, local, dist):
     rs_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     ag_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     ms_max = max_over_ranks(dist, ms)
-    value = P * K * world / (ms_max / 1e3)
+    value = job_value(P, K, world, ms_max)
     hbm = by["step"] * K / (ms / 1e3) / 1e9
 
     peak, peak_kind = measured_peak()
@@ -407,7 +415,7 @@ def run_e2e(st: Step, args, stream, dist) -> dict:
     torch.cuda.synchronize()
     ms = max_over_ranks(dist, e0.elapsed_time(e1))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    res = {"value": P * K * world / (ms / 1e3), "unit": "params/s", "steps": K,
+    res = {"value": job_value(P, K, world, ms), "unit": "params/s", "steps": K,
            "ms_per_step": ms / K, "h2d_bytes_per_step": N * total * 2,
            "d2h_bytes_per_step": st.n_out * st.out_numel * 2}
     del host_g, host_out

@@ -1,0 +1,79 @@
+"""bench.py's multi-GPU path, run as world_size-2 gloo ranks on CPU.
+
+With several GPUs bench.py runs one independent replica per rank (the
+sharded step has no data-path collective); the ranks only meet at a barrier
+and in a max over their elapsed times, and rank 0 reports the job-wide
+throughput.  These tests exercise that plumbing with the gloo backend."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(dist)
+        my_ms = 100.0 + 50.0 * rank                 # rank 1 is the slow replica
+        ms_max = bench.max_over_ranks(dist, my_ms)
+        value = bench.job_value(1000, 10, world, ms_max)
+        q.put((rank, ms_max, value, bench.dist_env()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_replica():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms_max, value, env in res:
+        assert ms_max == 150.0                      # every rank sees the max
+        assert value == pytest.approx(1000 * 10 * 2 / 0.150)
+        assert env == (2, rank, rank)
+
+
+def _reference_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import io
+    import contextlib
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.run_reference(None, world, rank)      # ranks other than 0 return without work
+    q.put((rank, buf.getvalue()))
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_reference_worker, args=(1, world, port, q))  # rank 1 of 2
+    p.start()
+    rank, out = q.get(timeout=120)
+    p.join(timeout=60)
+    assert p.exitcode == 0 and rank == 1 and out == ""
+
+
+def test_job_value_single_rank():
+    assert bench.job_value(1_364_297_728, 200, 1, 1752.0) == pytest.approx(
+        1_364_297_728 * 200 / 1.752)
