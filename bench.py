@@ -254,6 +254,7 @@ class Step:
         self.out_numel = pos
         self.out_flat = [torch.empty(pos, dtype=ps.dtype, device=dev) for _ in range(n_out)]
         self.outs = [o[off:off + n] for o in self.out_flat for off, n in zip(offs, numels)]
+        self.out_offs = offs
         # pointer arrays marshalled once; the timed calls pass them straight through
         self._grads_arr = ss.ptr_array(self.grads)
         self._outs_arr = ss.ptr_array(self.outs)
@@ -267,13 +268,19 @@ class Step:
             yield [(torch.randn(n, generator=g, device=dev) * ps.grad_std).to(ps.dtype)
                    for n in ps.numels()]
 
-    def rs_adamw(self, stream=None):
-        """One fused reduce-scatter + AdamW call over every group (next AdamW step)."""
+    def next_hp(self):
+        """AdamW hyper-parameters of the next optimizer step."""
         self.t += 1
-        hp = self.ss.adamw_params(step=self.t, **{k: v for k, v in W.adamw_hparams().items()
-                                                   if k != "step"})
+        return self.ss.adamw_params(step=self.t, **{k: v for k, v in W.adamw_hparams().items()
+                                                     if k != "step"})
+
+    def rs_adamw(self, stream=None, group=-1, hp=None):
+        """One fused reduce-scatter + AdamW call (every group, or one group with
+        the step's shared hyper-parameters)."""
+        if hp is None:
+            hp = self.next_hp()
         self.ss.fsdp_reduce_scatter_adamw(self.plan, self._grads_arr, self.master, self.m, self.v,
-                                          self.shards, hp, None, -1, stream)
+                                          self.shards, hp, None, group, stream)
 
     def fused_step(self, stream=None, param_grads=None):
         """fsdp_sharded_step: RS+AdamW with the all-gather written in the same pass."""
@@ -289,8 +296,8 @@ class Step:
                                       rank_param_grads=param_grads, params_out=self._outs_arr,
                                       n_out=self.n_out, stream=stream)
 
-    def all_gather(self, stream=None):
-        self.ss.fsdp_all_gather_unpack(self.plan, self.shards, self._outs_arr, self.n_out, -1,
+    def all_gather(self, stream=None, group=-1):
+        self.ss.fsdp_all_gather_unpack(self.plan, self.shards, self._outs_arr, self.n_out, group,
                                        stream)
 
 
@@ -374,8 +381,14 @@ def run_native(args, world, rank, local, dist):
 
 
 def run_e2e(st: Step, args, stream, dist) -> dict:
-    """Per step: pinned host -> device copy of the N gradient buffers, the two
-    C-ABI calls, device -> pinned host copy of the gathered parameters."""
+    """The same step end to end through the C ABI with host buffers.  Per step:
+    every rank's gradient buffer comes in from pinned host memory, the two
+    calls run, and the gathered parameters go back to pinned host memory.  The
+    work is pipelined group by group on three streams, as FSDP overlaps
+    communication with compute: group g's reduce-scatter + AdamW + all-gather
+    starts once its gradients have arrived, while group g+1's are still in
+    flight, and group g's parameters leave while later groups compute."""
+    import sharded_state_gb300 as ss
     total = st.info["total_numel"]
     N = st.N
     need = N * total * 2 + st.n_out * st.out_numel * 2
@@ -392,32 +405,61 @@ def run_e2e(st: Step, args, stream, dist) -> dict:
         host_g.append(h)
     host_out = [torch.empty(st.out_numel, dtype=st.ps.dtype, pin_memory=True)
                 for _ in range(st.n_out)]
+    G = len(st.ps.groups)
+    groups = [ss.fsdp_plan_group(st.plan, g) for g in range(G)]
+    numels = st.ps.numels()
+    out_rng = []
+    for grp in groups:
+        a, b = grp["first_param"], grp["first_param"] + grp["num_params"]
+        lo = st.out_offs[a] if b > a else 0
+        hi = st.out_offs[b - 1] + (numels[b - 1] + 7) // 8 * 8 if b > a else 0
+        out_rng.append((lo, hi))
+    h2d = torch.cuda.Stream()
+    d2h = torch.cuda.Stream()
+    sp = stream.cuda_stream
     torch.cuda.synchronize()
     K = max(args.e2e_steps, 1)
     P = st.info["unpadded_numel"]
-    sp = stream.cuda_stream
-    # one untimed pass to settle the copy engines
-    for r in range(N):
-        st.grads[r].copy_(host_g[r], non_blocking=True)
+
+    def one_step():
+        hp = st.next_hp()
+        ev_in = [torch.cuda.Event() for _ in range(G)]
+        ev_done = [torch.cuda.Event() for _ in range(G)]
+        h2d.wait_stream(stream)
+        with torch.cuda.stream(h2d):
+            for g, grp in enumerate(groups):
+                lo, hi = grp["base"], grp["base"] + N * grp["shard_numel"]
+                for r in range(N):
+                    st.grads[r][lo:hi].copy_(host_g[r][lo:hi], non_blocking=True)
+                ev_in[g].record(h2d)
+        for g in range(G):
+            stream.wait_event(ev_in[g])
+            st.rs_adamw(sp, group=g, hp=hp)
+            st.all_gather(sp, group=g)
+            ev_done[g].record(stream)
+            d2h.wait_event(ev_done[g])
+            lo, hi = out_rng[g]
+            with torch.cuda.stream(d2h):
+                for j in range(st.n_out):
+                    host_out[j][lo:hi].copy_(st.out_flat[j][lo:hi], non_blocking=True)
+        stream.wait_stream(d2h)
+
+    one_step()  # untimed pass to settle the copy engines
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(K):
-        for r in range(N):
-            st.grads[r].copy_(host_g[r], non_blocking=True)
-        st.rs_adamw(sp)
-        st.all_gather(sp)
-        for j in range(st.n_out):
-            host_out[j].copy_(st.out_flat[j], non_blocking=True)
+        one_step()
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(dist, e0.elapsed_time(e1))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     res = {"value": job_value(P, K, world, ms), "unit": "params/s", "steps": K,
            "ms_per_step": ms / K, "h2d_bytes_per_step": N * total * 2,
-           "d2h_bytes_per_step": st.n_out * st.out_numel * 2}
+           "d2h_bytes_per_step": st.n_out * st.out_numel * 2,
+           "pipeline": f"{G} groups on 3 streams (H2D / compute / D2H)"}
     del host_g, host_out
     return res
 

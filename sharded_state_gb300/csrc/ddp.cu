@@ -135,6 +135,10 @@ template <int NR>
 __global__ void __launch_bounds__(kThreads)
 ddp_bucket_kernel(const int64_t* __restrict__ prefix, const void* const* __restrict__ ptrs, int N,
                   int o_lo, int o_hi) {
+    // Buckets are independent (disjoint tensors, read-only table), so the next
+    // bucket's launch may start as soon as every CTA of this one is running:
+    // its CTAs then fill SMs while this bucket drains.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t u_lo = prefix[o_lo], u_hi = prefix[o_hi];
     int64_t u = u_lo + (int64_t)blockIdx.x * kTile;
     const int64_t u_end = u + kTile < u_hi ? u + kTile : u_hi;
@@ -151,6 +155,23 @@ ddp_bucket_kernel(const int64_t* __restrict__ prefix, const void* const* __restr
 }
 
 using DdpKernel = void (*)(const int64_t*, const void* const*, int, int, int);
+
+// Launch one bucket with programmatic stream serialisation: it may begin
+// while the previous bucket's kernel on the stream is still finishing.
+cudaError_t launch_bucket(DdpKernel fn, unsigned grid, cudaStream_t st, const int64_t* prefix,
+                          const void* const* ptrs, int N, int o_lo, int o_hi) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, prefix, ptrs, N, o_lo, o_hi);
+}
 
 DdpKernel pick(int N) {
     switch (N) {
@@ -248,8 +269,8 @@ int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* nume
             rc = SS_EOVERFLOW;
             break;
         }
-        fn<<<(unsigned)grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
-        rc = ss::check_launch();
+        cudaError_t le = launch_bucket(fn, (unsigned)grid, st, d_prefix, d_ptrs, N, o_lo, o_hi);
+        rc = le == cudaSuccess ? ss::check_launch() : ss::cuda_fail(le);
     }
     cudaError_t ef = cudaFreeAsync(d_table, st);
     if (rc == SS_OK && ef != cudaSuccess) rc = ss::cuda_fail(ef);
@@ -355,8 +376,8 @@ extern "C" int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors,
         if (elems == 0) continue;
         const int64_t grid = (elems + kTile - 1) / kTile;
         if (grid > 0x7FFFFFFF) return SS_EOVERFLOW;
-        fn<<<(unsigned)grid, kThreads, 0, st>>>(d_prefix, d_ptrs, N, o_lo, o_hi);
-        rc = ss::check_launch();
+        cudaError_t le = launch_bucket(fn, (unsigned)grid, st, d_prefix, d_ptrs, N, o_lo, o_hi);
+        rc = le == cudaSuccess ? ss::check_launch() : ss::cuda_fail(le);
         if (rc) return rc;
     }
     return SS_OK;
