@@ -760,6 +760,23 @@ def _rows_small(ss, peak, want):
         by = step_bytes(2, st1.info["total_numel"], st1.info["unpadded_numel"], 1)
         _row("step on the tiny MLP (16,640 params, N=2): latency", st1.info["unpadded_numel"],
              "params/s", ms, mn, by["step"], peak, extra={"us_per_step": ms * 1e3})
+        # the same two C-ABI calls captured once in a CUDA graph and replayed:
+        # the launch-bound step without host-side call overhead (the AdamW step
+        # count is frozen in the captured arguments, which does not change the
+        # work done)
+        g = torch.cuda.CUDAGraph()
+        s_ = torch.cuda.Stream()
+        s_.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_):
+            step1()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s_):
+                step1()
+        torch.cuda.current_stream().wait_stream(s_)
+        ms, mn = _time_stream(lambda: g.replay(), 500, warmup=20)
+        _row("step on the tiny MLP (16,640 params, N=2): replayed from a CUDA graph",
+             st1.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
+             extra={"us_per_step": ms * 1e3})
 
     # -- config 3: awkward sizes, N=7 ------------------------------------------
     for kind in ((W.FLAT_ORIG_FALSE, W.FLAT_ORIG_TRUE) if "awkward" in want else ()):

@@ -323,6 +323,28 @@ def test_ddp_bucket_average_bit_exact(ss, cap):
         np.testing.assert_array_equal(to_np(o), w)
 
 
+def test_ddp_full_size_sampled(ss):
+    # the full DDP gradient list (1400 x 2048 + 600 x 4,194,304 bf16 per rank, N=8,
+    # 45 GB in and out) at the default 25 MiB cap, in the launch shape the benchmark
+    # times; 24 tensors (small and large) compared whole against the oracle
+    ds = W.ddp_grads()
+    grads = W.make_ddp_grads(ds, device="cuda")
+    outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for n in ds.numels]
+    nb = ss.ddp_bucket_pack_average(grads, 25 << 20, outs)
+    torch.cuda.synchronize()
+    assert nb == oracle.ddp_buckets(ds.numels, 2, 25 << 20)[1]
+    rng = np.random.default_rng(0)
+    small = [t for t, n in enumerate(ds.numels) if n == 2048]
+    large = [t for t, n in enumerate(ds.numels) if n != 2048]
+    pick = list(rng.choice(small, 16, replace=False)) + list(rng.choice(large, 8, replace=False))
+    pick += [0, len(ds.numels) - 1]
+    for t in pick:
+        want = oracle.ddp_average([[to_np(grads[r][t])] for r in range(ds.world_size)])[0]
+        np.testing.assert_array_equal(to_np(outs[t]), want)
+    del grads, outs
+    torch.cuda.empty_cache()
+
+
 def test_ddp_misaligned_and_odd_sizes(ss):
     # views offset by one element: pointers congruent across ranks, and not
     rng = np.random.default_rng(1)
