@@ -161,6 +161,39 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
     }
 }
 
+// Fast path for plans whose every data segment starts and ends on 16-byte
+// boundaries on both sides (plan->vec_aligned) with 16-byte aligned pointers:
+// no head, tail or alignment checks, 4 x 128-bit vectors per thread, few
+// enough registers for 8 resident CTAs per SM.  DIR 0: all-gather, 1: pack.
+template <int E, int CAP, int DIR>
+__global__ void __launch_bounds__(kThreads, 8)
+tile_copy_fast_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo,
+                      const ss::Seg* __restrict__ segs, unsigned char* packed, PtrTab<CAP> tab,
+                      int param_base) {
+    constexpr int64_t T = ss::kTileBytes / E;
+    constexpr int kV = ss::kTileBytes / 16 / kThreads;  // vectors per thread
+    const ss::Tile tl = tiles[t_lo + blockIdx.x];
+    const ss::Seg sg = segs[tl.seg];
+    const int64_t off = (int64_t)tl.idx * T;
+    const int nv = (int)((sg.len - off < T ? sg.len - off : T) * E / 16);
+    unsigned char* pp = static_cast<unsigned char*>(tab.p[sg.param - param_base]) +
+                        (sg.param_off + off) * E;
+    unsigned char* kp = packed + (sg.packed_off + off) * E;
+    const unsigned char* src = DIR == 0 ? kp : pp;
+    unsigned char* dst = DIR == 0 ? pp : kp;
+    uint4 x[kV];
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+        const int q = threadIdx.x + j * kThreads;
+        if (q < nv) x[j] = ss::ld_stream_u4(src + 16 * q);
+    }
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+        const int q = threadIdx.x + j * kThreads;
+        if (q < nv) ss::st_stream_u4(dst + 16 * q, x[j]);
+    }
+}
+
 template <int E>
 __global__ void __launch_bounds__(kThreads)
 zero_tile_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
@@ -200,8 +233,31 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
     PtrTab<CAP> tab;
     std::memset(&tab, 0, sizeof tab);
     const int w = b - a;
+    bool ptrs_aligned = true;
     for (int j = 0; j < n_out; ++j)
-        for (int i = a; i < b; ++i) tab.p[j * w + (i - a)] = ptrs[(size_t)j * p->n + i];
+        for (int i = a; i < b; ++i) {
+            tab.p[j * w + (i - a)] = ptrs[(size_t)j * p->n + i];
+            ptrs_aligned &= p->numel[i] == 0 || ss::aligned(tab.p[j * w + (i - a)], 16);
+        }
+    if (p->vec_aligned && ptrs_aligned && n_out == 1) {
+        return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
+            if (p->eb == 2) {
+                if (dir == 0)
+                    tile_copy_fast_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
+                                                                                packed, tab, a);
+                else
+                    tile_copy_fast_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
+                                                                                packed, tab, a);
+            } else {
+                if (dir == 0)
+                    tile_copy_fast_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
+                                                                                packed, tab, a);
+                else
+                    tile_copy_fast_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
+                                                                                packed, tab, a);
+            }
+        });
+    }
     return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
         if (p->eb == 2) {
             if (dir == 0 && n_out > 1)

@@ -72,6 +72,9 @@ struct ss_plan {
     ss::Tile* d_data_tiles = nullptr;
     ss::Tile* d_zero_tiles = nullptr;
     ss::Tile* d_packed_tiles = nullptr;
+    // every data segment's packed offset, parameter offset and length are
+    // multiples of 16 bytes (enables the copy kernels' fast path)
+    bool vec_aligned = false;
     int device = -1;
     bool has_dev = false;
 };

@@ -334,6 +334,11 @@ int fsdp_plan_create(const ss_plan_desc* d, ss_plan** out) {
                 rc = SS_EOVERFLOW;
             else
                 build_packed_tiles(p);
+            const int64_t per16 = 16 / p->eb;
+            p->vec_aligned = true;
+            for (const ss::Seg& sg : p->data)
+                p->vec_aligned &= sg.packed_off % per16 == 0 && sg.param_off % per16 == 0 &&
+                                  sg.len % per16 == 0;
         }
         if (rc == SS_OK && !(d->flags & SS_PLAN_HOST_ONLY)) rc = upload(p);
     } catch (const std::bad_alloc&) {

@@ -46,6 +46,9 @@ def _small_sets():
     sets.append(("small_llama_groups_N3", small_llama))
     sets.append(("small_llama_groups_N8", W.llama_1b2(world_size=8, layers=2, hidden=48,
                                                        ffn=136, vocab=96)))
+    # every segment a whole number of 16-byte vectors: the copy kernels' fast path
+    sets.append(("small_llama_aligned_N8", W.llama_1b2(world_size=8, layers=2, hidden=64,
+                                                        ffn=128, vocab=64)))
     ex = W.ParamSet(["p1", "p2"], [(3,), (5,)], [2], 4, W.FLAT_ORIG_TRUE, torch.bfloat16, seed=9)
     sets.append(("worked_example_3_5", ex))
     big_n = W.ParamSet([f"p{i}" for i in range(5)], [(130, 3), (64,), (0, 4), (1,), (257, 2)], [5],
