@@ -60,6 +60,9 @@ def parse_args():
                     help="step: the one-line headline; rows: one JSON line per hot-path row")
     ap.add_argument("--rows", default="all",
                     help="rows mode: comma list of llama,block4096,tiny,awkward,ddp (default all)")
+    ap.add_argument("--step-kind", default="two_calls", choices=["two_calls", "fused"],
+                    help="timed step: RS+AdamW then all-gather (two calls), or the one-pass "
+                         "fsdp_sharded_step")
     ap.add_argument("--ddp-large", type=int, default=600,
                     help="rows mode: number of 4M-element DDP tensors (600 = the full list)")
     return ap.parse_args()
@@ -92,6 +95,18 @@ def workload_config(ps: W.ParamSet, info, n_out: int) -> dict:
             "storage": "bf16 grads/params, fp32 master/exp_avg/exp_avg_sq",
             "adamw": {k: v for k, v in W.adamw_hparams().items() if k != "step"},
             "l2": "no flush: inputs of every step (>= 62 GB at the default workload) exceed L2"}
+
+
+def ncu_traffic(kernel: str, units: int):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture
+    (per-element read + write bytes x units), or None if none was taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[kernel]
+        return (d["dram_read_bytes_per_element"] + d["dram_write_bytes_per_element"]) * units
+    except Exception:
+        return None
 
 
 def measured_peak():
@@ -314,9 +329,13 @@ def run_native(args, world, rank, local, dist):
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
+    fused = args.step_kind == "fused"
     for _ in range(max(args.warmup, 0)):
-        st.rs_adamw(sp)
-        st.all_gather(sp)
+        if fused:
+            st.fused_step(sp)
+        else:
+            st.rs_adamw(sp)
+            st.all_gather(sp)
     torch.cuda.synchronize()
 
     K = args.steps
@@ -331,9 +350,13 @@ def run_native(args, world, rank, local, dist):
     e0.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
-        st.rs_adamw(sp)
+        if fused:
+            st.fused_step(sp)
+        else:
+            st.rs_adamw(sp)
         ev[k][1].record(stream)
-        st.all_gather(sp)
+        if not fused:
+            st.all_gather(sp)
         ev[k][2].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -345,29 +368,39 @@ def run_native(args, world, rank, local, dist):
     ag_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     ms_max = max_over_ranks(dist, ms)
     value = job_value(P, K, world, ms_max)
+    if fused:  # one kernel: 2N + 26 bytes per packed element + 2 * n_out per parameter
+        by = {"rs_adamw": (2 * N + 26) * total + 2 * args.n_out * P, "all_gather": 0,
+              "step": (2 * N + 26) * total + 2 * args.n_out * P}
     hbm = by["step"] * K / (ms / 1e3) / 1e9
 
     peak, peak_kind = measured_peak()
     rs_avg = sum(rs_ms) / K
     rs_gbs = by["rs_adamw"] / (rs_avg / 1e3) / 1e9
     ag_avg = sum(ag_ms) / K
-    ag_gbs = by["all_gather"] / (ag_avg / 1e3) / 1e9
+    ag_gbs = by["all_gather"] / (ag_avg / 1e3) / 1e9 if by["all_gather"] else 0.0
 
     out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": K,
            "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-           "impl": "native", "config": workload_config(ps, st.info, args.n_out),
+           "impl": "native", "config": dict(workload_config(ps, st.info, args.n_out),
+                                            step_kind=args.step_kind),
            "hbm_gbs": hbm, "bytes_per_step": by["step"],
            "frac_of_measured_peak": hbm / peak, "frac_of_nominal_8tbs": hbm / NOMINAL_HBM_GBS,
            "kernels": {"rs_adamw": {"ms": rs_avg, "ms_min": min(rs_ms), "gbs": rs_gbs,
                                     "bytes": by["rs_adamw"]},
                        "all_gather_unpack": {"ms": ag_avg, "ms_min": min(ag_ms), "gbs": ag_gbs,
                                              "bytes": by["all_gather"]}},
-           "roofline": {"bound": "hbm", "kernel": "rs_adamw", "achieved": rs_gbs, "peak": peak,
+           "roofline": {"bound": "hbm", "kernel": "fused_step" if fused else "rs_adamw",
+                        "achieved": rs_gbs, "peak": peak,
                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                         if peak_kind == "measured" else "fallback 6.8 TB/s",
-                        "unit": "GB/s", "frac": rs_gbs / peak, "traffic": None,
-                        "per_unit_bytes": 2 * N + 26, "units_per_launch": total},
+                        "unit": "GB/s", "frac": rs_gbs / peak,
+                        "traffic": None if fused or N != 8 else
+                        ncu_traffic("rs_adamw_bf16_kernel<8,1,0,1,0>", total),
+                        "traffic_source": "ncu capture per element x elements per launch "
+                                          "(profiles/ncu_traffic.json)",
+                        "per_unit_bytes": 2 * N + 26 + (2 * args.n_out if fused else 0),
+                        "units_per_launch": total},
            "gpu_launches": launches, "clocks": clk}
 
     # e2e: the same step through the C ABI with host buffers
@@ -643,6 +676,24 @@ def run_rows(args):
 def _rows_llama(args, ss, oracle, peak, used, K, bits):
     # -- a1/a2/a3/a4 on the 1.2B model ---------------------------------------
     ps = W.llama_1b2()
+    d0_, inner_ = ps.dim0_inner()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        plan_ = ss.fsdp_plan_create(ps.layout, ps.world_size, 2, d0_, inner_,
+                                    group_num_params=ps.groups)
+        plan_.destroy()
+    t_plan = (time.perf_counter() - t0) / 5
+    t_cpu, reps = _time_cpu(lambda: [oracle.layout(ps.layout, ps.world_size, 2, d0_[a:a + g],
+                                                   inner_[a:a + g])
+                                     for a, g in zip(np.cumsum([0] + ps.groups[:-1]), ps.groups)],
+                            1.0)
+    print(json.dumps({"row": "a1 plan: layout, segment and tile tables + device upload "
+                             "(1.2B model, 219 params, 25 groups, N=8)",
+                      "value": 1.0 / t_plan, "unit": "plans/s", "ms": t_plan * 1e3,
+                      "host_only": "runs once per model; not on the per-step path",
+                      "cpu_baseline": {"value": 1.0 / t_cpu, "unit": "layouts/s", "cores": 1,
+                                       "kind": "oracle", "sample": f"the 25 group layouts, {reps} reps"}}),
+          flush=True)
     st = Step(ss, ps, 1)
     P, total, N = st.info["unpadded_numel"], st.info["total_numel"], st.N
     d0, inner = ps.dim0_inner()
@@ -669,8 +720,14 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
          {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
           "sample": f"block group 0, {reps} oracle RS+AdamW+AG steps"})
     ag_ms, ag_mn = _time_stream(lambda: st.all_gather(), K)
+    g0p = ps.groups[0]
+    shards0 = bits(st.shards[:N * ss.fsdp_plan_group(st.plan, 0)["shard_numel"]])
+    t_cpu, reps = _time_cpu(lambda: oracle.all_gather_unpack(ps.layout, N, 2, d0[:g0p],
+                                                             inner[:g0p], shards0),
+                            args.cpu_seconds / 4)
     _row("a4 all-gather + unpack, n_out=1 (1.2B model, N=8)", P, "params/s", ag_ms, ag_mn, 4 * P,
-         peak)
+         peak, {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
+                "sample": f"block group 0, {reps} oracle unpacks"})
     ms, mn = _time_stream(lambda: st.fused_step(), K)
     _row("one-pass step: packed grads -> RS+AdamW -> shards + unpacked params (1.2B, N=8)", P,
          "params/s", ms, mn, (2 * N + 28) * P, peak)
@@ -708,9 +765,20 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
                                               st.m, st.v, st.shards, hp if last else None)
     ms, mn = _time_stream(accumulate_step, max(K // 4, 5))
     acc_bytes = (2 * N + 4) + 2 * (2 * N + 8) + (2 * N + 30)
+
+    def oracle_accumulate():
+        acc = None
+        for _ in range(kmic):
+            acc = oracle.accumulate(N, smp["shard_numel"], smp["grads"], acc)
+        g = oracle.accumulated_grad(acc, kmic)
+        oracle.adamw(g, smp["master"], smp["m"], smp["v"], lr=1e-3, beta1=0.9, beta2=0.999,
+                     eps=1e-8, weight_decay=0.01, step=20_000)
+    t_cpu, reps = _time_cpu(oracle_accumulate, args.cpu_seconds / 4)
     _row(f"gradient accumulation: {kmic} micro-batches per optimizer step (1.2B, N=8)", P,
-         "params/s", ms, mn, acc_bytes * total, peak, extra={"micro_batches": kmic,
-                                                             "ms_per_micro_batch": ms / kmic})
+         "params/s", ms, mn, acc_bytes * total, peak,
+         {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
+          "sample": f"block group 0, {reps} oracle optimizer steps of {kmic} micro-batches"},
+         extra={"micro_batches": kmic, "ms_per_micro_batch": ms / kmic})
     del accum
     # F4: AdamW without fp32 master weights (bf16 shard updated in place)
     def no_master():
