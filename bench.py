@@ -454,18 +454,21 @@ def run_e2e(st: Step, args, stream, dist) -> dict:
     K = max(args.e2e_steps, 1)
     P = st.info["unpadded_numel"]
 
+    order = list(range(G))  # registration order (largest-group-in-the-middle measured slower)
+
     def one_step():
         hp = st.next_hp()
         ev_in = [torch.cuda.Event() for _ in range(G)]
         ev_done = [torch.cuda.Event() for _ in range(G)]
         h2d.wait_stream(stream)
         with torch.cuda.stream(h2d):
-            for g, grp in enumerate(groups):
+            for g in order:
+                grp = groups[g]
                 lo, hi = grp["base"], grp["base"] + N * grp["shard_numel"]
                 for r in range(N):
                     st.grads[r][lo:hi].copy_(host_g[r][lo:hi], non_blocking=True)
                 ev_in[g].record(h2d)
-        for g in range(G):
+        for g in order:
             stream.wait_event(ev_in[g])
             st.rs_adamw(sp, group=g, hp=hp)
             st.all_gather(sp, group=g)

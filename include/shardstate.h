@@ -23,6 +23,9 @@
  *     SS_ECUDA means a CUDA runtime call failed; ss_last_cuda_error() returns
  *     that cudaError_t value for the calling thread.
  *   - Device pointers are plain device addresses on the current CUDA device.
+ *     A plan's metadata lives on the device that was current when it was
+ *     created; launching calls made with another device current return
+ *     SS_EINVAL.
  *     The caller owns all of them; the library never frees or keeps them.
  *   - Launches are asynchronous on the caller's stream (NULL = the legacy
  *     default stream).  Nothing synchronises except plan creation, which

@@ -330,6 +330,7 @@ int fsdp_pack(const ss_plan* plan, const void* const* params, void* packed, int 
               ss_stream_t stream) {
     if (!plan || !packed || (plan->n > 0 && !params)) return SS_EINVAL;
     if (!plan->has_dev) return SS_ENODEVICE;
+    if (int drc = ss::check_device(plan)) return drc;
     int64_t lo, hi;
     if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;
     if (!ss::aligned(packed, 16)) return SS_EALIGN;
@@ -363,6 +364,7 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards, void* 
     if (!plan || !param_shards || (plan->n > 0 && !params_out)) return SS_EINVAL;
     if (n_out < 1 || n_out > SS_MAX_REPLICAS) return SS_EINVAL;
     if (!plan->has_dev) return SS_ENODEVICE;
+    if (int drc = ss::check_device(plan)) return drc;
     int64_t lo, hi;
     if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;
     if (!ss::aligned(param_shards, 16)) return SS_EALIGN;

@@ -92,6 +92,13 @@ int num_sms();
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// SS_OK if the current device is the one the plan's metadata lives on.
+inline int check_device(const ss_plan* p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ECUDA;
+    return dev == p->device ? SS_OK : SS_EINVAL;
+}
+
 // Element range [lo, hi) of the packed buffers covered by `group` (-1 = all).
 inline bool group_range(const ss_plan* p, int group, int64_t* lo, int64_t* hi) {
     if (group < 0) {

@@ -363,6 +363,7 @@ int fsdp_reduce_scatter_adamw(const ss_plan* plan, const void* const* rank_grads
                               ss_stream_t stream) {
     if (!plan || !rank_grads) return SS_EINVAL;
     if (!plan->has_dev) return SS_ENODEVICE;
+    if (int drc = ss::check_device(plan)) return drc;
     int64_t lo, hi;
     if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;
     const int N = plan->N;
@@ -439,6 +440,7 @@ int fsdp_init_master(const ss_plan* plan, const void* param_shards, float* maste
                      float* exp_avg_sq, int group, ss_stream_t stream) {
     if (!plan || !param_shards || !master || !exp_avg || !exp_avg_sq) return SS_EINVAL;
     if (!plan->has_dev) return SS_ENODEVICE;
+    if (int drc = ss::check_device(plan)) return drc;
     int64_t lo, hi;
     if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;
     const void* bufs[4] = {param_shards, master, exp_avg, exp_avg_sq};
@@ -589,6 +591,7 @@ extern "C" int fsdp_reduce_scatter_accumulate(const ss_plan* plan, const void* c
                                               ss_stream_t stream) {
     if (!plan || !rank_grads) return SS_EINVAL;
     if (!plan->has_dev) return SS_ENODEVICE;
+    if (int drc = ss::check_device(plan)) return drc;
     if (plan->eb != 2) return SS_EINVAL;
     if (num_micro < 1 || micro_step < 0 || micro_step >= num_micro) return SS_EINVAL;
     const bool last = micro_step == num_micro - 1;

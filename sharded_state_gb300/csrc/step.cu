@@ -252,6 +252,7 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                                  ss_stream_t stream) {
     if (!plan || !s) return SS_EINVAL;
     if (!plan->has_dev) return SS_ENODEVICE;
+    if (int drc = ss::check_device(plan)) return drc;
     if (plan->eb != 2) return SS_EINVAL;
     int64_t lo, hi;
     if (!ss::group_range(plan, group, &lo, &hi)) return SS_EINVAL;

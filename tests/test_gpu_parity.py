@@ -401,3 +401,51 @@ def test_empty_plan_is_a_no_op(ss):
     ss.fsdp_reduce_scatter_adamw(plan, [x] * 4, f, f, f, x, ss.adamw_params())
     ss.fsdp_all_gather_unpack(plan, x, [x, x])
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# pointer-table windows, maximum replica count, the one-group shorthand
+# ---------------------------------------------------------------------------
+
+def test_all_gather_windows_and_max_replicas(ss):
+    # 200 params x 11 replicas = 2200 pointers > 2048: the call splits into windows
+    ps = W.awkward_1d(5, W.FLAT_ORIG_TRUE, torch.bfloat16)
+    su = Setup(ss, ps)
+    g = torch.Generator().manual_seed(5)
+    shards_cpu = torch.randint(-32768, 32767, (su.total,), generator=g,
+                               dtype=torch.int16).view(torch.bfloat16)
+    shards = shards_cpu.cuda()
+    want = su.oracle_unpack(to_np(shards_cpu), n_out=1)[0]
+    for n_out in (11, ss.SS_MAX_REPLICAS):
+        outs = [torch.empty_like(p) for _ in range(n_out) for p in su.params]
+        ss.fsdp_all_gather_unpack(su.plan, shards, outs, n_out=n_out)
+        torch.cuda.synchronize()
+        n = len(su.params)
+        for j in (0, n_out // 2, n_out - 1):
+            for i in range(n):
+                np.testing.assert_array_equal(to_np(outs[j * n + i]), want[i])
+    with pytest.raises(ss.ShardStateError):
+        ss.fsdp_all_gather_unpack(su.plan, shards, outs, n_out=ss.SS_MAX_REPLICAS + 1)
+
+
+def test_pack_more_than_2048_params(ss):
+    ps = W.awkward_1d(3, W.FLAT_ORIG_FALSE, torch.bfloat16, count=2300, max_len=40, seed=8)
+    su = Setup(ss, ps)
+    packed = torch.empty(su.total, dtype=torch.bfloat16, device="cuda")
+    ss.fsdp_pack(su.plan, su.params, packed)
+    outs = [torch.empty_like(p) for p in su.params]
+    ss.fsdp_all_gather_unpack(su.plan, packed, outs)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(packed), su.oracle_pack(su.params_np()))
+    for o, p in zip(outs, su.params_np()):
+        np.testing.assert_array_equal(to_np(o), p)
+
+
+def test_one_group_shorthand_matches_create(ss):
+    ps = W.awkward_2d(5)
+    d0, inner = ps.dim0_inner()
+    a = ss.fsdp_plan_layout(ss.SS_PER_PARAM_DIM0, 5, 2, d0, inner)
+    b = ss.fsdp_plan_create(ss.SS_PER_PARAM_DIM0, 5, 2, d0, inner)
+    assert a.info().as_dict() == b.info().as_dict()
+    for i in (0, 57, 199):
+        assert ss.fsdp_plan_param_offset(a, i) == ss.fsdp_plan_param_offset(b, i)
