@@ -182,6 +182,14 @@ int fsdp_plan_param_offset(const ss_plan* plan, int param, int64_t* offset_out,
 int fsdp_plan_group(const ss_plan* plan, int group, int64_t* base_out, int64_t* shard_numel_out,
                     int* first_param_out, int* num_params_out);
 
+/* Self-check of a plan's host tables: every data run lies inside its
+ * parameter and its group, the runs cover each parameter element exactly once,
+ * data and pad runs tile every packed buffer [0, total_numel) with no gap or
+ * overlap, and the tile tables split every run exactly.  The kernels index
+ * device memory only through these tables, so a plan that passes keeps every
+ * access in bounds.  SS_OK or SS_EINVAL. */
+int fsdp_plan_validate(const ss_plan* plan);
+
 /* Free a plan and its device metadata (NULL is a no-op).  The caller makes
  * sure no launch that uses the plan is still pending. */
 void fsdp_plan_destroy(ss_plan* plan);

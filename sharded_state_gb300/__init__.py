@@ -41,7 +41,7 @@ EXPORTED = ("fsdp_plan_create", "fsdp_plan_layout", "fsdp_plan_info", "fsdp_plan
             "fsdp_reduce_scatter_adamw", "fsdp_all_gather_unpack", "ddp_bucket_pack_average",
             "ddp_bucket_assign", "ss_strerror", "ss_last_cuda_error", "ss_version",
             "ss_launch_count", "ddp_bucket_pack_average_noalloc", "fsdp_sharded_step",
-            "fsdp_reduce_scatter_accumulate")
+            "fsdp_reduce_scatter_accumulate", "fsdp_plan_validate")
 
 
 class ShardStateError(RuntimeError):
@@ -97,6 +97,7 @@ def _load() -> ctypes.CDLL:
         "fsdp_plan_param_offset": ([vp, i32, i64p, i64p], i32),
         "fsdp_plan_group": ([vp, i32, i64p, i64p, ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "fsdp_plan_destroy": ([vp], None),
+        "fsdp_plan_validate": ([vp], i32),
         "fsdp_pack": ([vp, vpp, vp, i32, vp], i32),
         "fsdp_init_master": ([vp, vp, vp, vp, vp, i32, vp], i32),
         "fsdp_reduce_scatter_adamw": ([vp, vpp, vp, vp, vp, vp, ctypes.POINTER(AdamW), vp, i32, vp],
@@ -277,6 +278,10 @@ def fsdp_plan_group(plan: Plan, group: int):
                                                    ctypes.byref(count)))
     return {"base": base.value, "shard_numel": shard.value, "first_param": first.value,
             "num_params": count.value}
+
+
+def fsdp_plan_validate(plan: Plan) -> None:
+    _check("fsdp_plan_validate", _lib.fsdp_plan_validate(plan))
 
 
 def fsdp_plan_destroy(plan: Plan) -> None:

@@ -408,6 +408,71 @@ void fsdp_plan_destroy(ss_plan* p) {
     delete p;
 }
 
+int fsdp_plan_validate(const ss_plan* p) {
+    if (!p) return SS_EINVAL;
+    // data segments: inside their group's range and their parameter, ordered
+    // by parameter, consecutive starts
+    std::vector<std::pair<int64_t, int64_t>> cover;  // (packed_off, len) of data and pads
+    int64_t u = 0;
+    for (size_t k = 0; k < p->data.size(); ++k) {
+        const ss::Seg& s = p->data[k];
+        if (s.param < 0 || s.param >= p->n || s.len <= 0 || s.start != u) return SS_EINVAL;
+        if (s.param_off < 0 || s.param_off + s.len > p->numel[s.param]) return SS_EINVAL;
+        const int g = p->param_group[s.param];
+        const int64_t glo = p->gbase[g], ghi = glo + (int64_t)p->N * p->gshard[g];
+        if (s.packed_off < glo || s.packed_off + s.len > ghi) return SS_EINVAL;
+        if (k > 0 && p->data[k - 1].param > s.param) return SS_EINVAL;
+        u += s.len;
+        cover.emplace_back(s.packed_off, s.len);
+    }
+    if (u != p->unpadded) return SS_EINVAL;  // every parameter element exactly once
+    int64_t uz = 0;
+    for (const ss::Seg& s : p->zero) {
+        if (s.param != -1 || s.len <= 0 || s.start != uz) return SS_EINVAL;
+        uz += s.len;
+        cover.emplace_back(s.packed_off, s.len);
+    }
+    // data + pads tile [0, total) with no gap and no overlap
+    std::sort(cover.begin(), cover.end());
+    int64_t pos = 0;
+    for (auto& c : cover) {
+        if (c.first != pos) return SS_EINVAL;
+        pos += c.second;
+    }
+    if (pos != p->total) return SS_EINVAL;
+    // tiles: every segment split into consecutive tiles, each inside its segment
+    auto check_tiles = [&](const std::vector<ss::Seg>& segs, const std::vector<ss::Tile>& tiles,
+                           const std::vector<int64_t>& seg_tile) {
+        const int64_t T = ss::kTileBytes / p->eb;
+        if (seg_tile.size() != segs.size() + 1 || seg_tile.back() != (int64_t)tiles.size())
+            return false;
+        for (size_t k = 0; k < segs.size(); ++k) {
+            const int64_t nt = (segs[k].len + T - 1) / T;
+            if (seg_tile[k + 1] - seg_tile[k] != nt) return false;
+            for (int64_t j = 0; j < nt; ++j) {
+                const ss::Tile& t = tiles[seg_tile[k] + j];
+                if (t.seg != (int32_t)k || t.idx != (int32_t)j) return false;
+            }
+        }
+        return true;
+    };
+    if (!check_tiles(p->data, p->data_tiles, p->data_seg_tile) ||
+        !check_tiles(p->zero, p->zero_tiles, p->zero_seg_tile))
+        return SS_EINVAL;
+    // packed-order tiles: a permutation of the data tiles, groups contiguous
+    if (p->packed_tiles.size() != p->data_tiles.size()) return SS_EINVAL;
+    if (p->group_ptile.size() != (size_t)p->G + 1 || p->group_ptile[0] != 0 ||
+        p->group_ptile[p->G] != (int64_t)p->packed_tiles.size())
+        return SS_EINVAL;
+    for (int g = 0; g < p->G; ++g)
+        for (int64_t t = p->group_ptile[g]; t < p->group_ptile[g + 1]; ++t) {
+            const ss::Tile& tl = p->packed_tiles[t];
+            if (tl.seg < 0 || (size_t)tl.seg >= p->data.size()) return SS_EINVAL;
+            if (p->param_group[p->data[tl.seg].param] != g) return SS_EINVAL;
+        }
+    return SS_OK;
+}
+
 const char* ss_strerror(int s) {
     switch (s) {
         case SS_OK: return "ok";

@@ -59,6 +59,28 @@ def _compare_plan(ss, kind, N, eb, dim0, inner=None, groups=None):
     plan.destroy()
 
 
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_plan_tables_validate(ss, kind):
+    cases = []
+    for N in (1, 3, 7, 8, 64):
+        if kind == 2:
+            ps = W.awkward_2d(N)
+            cases.append((N, *ps.dim0_inner(), [1, 0, 37, 62, 100]))
+        else:
+            ps = W.awkward_1d(N, kind, torch.bfloat16)
+            cases.append((N, ps.numels(), None, [1, 0, 37, 62, 100]))
+    big = W.llama_1b2()
+    if kind == 2:
+        cases.append((8, *big.dim0_inner(), big.groups))
+    for N, d0, inner, groups in cases:
+        for eb in (2, 4):
+            for g in (None, groups):
+                plan = ss.fsdp_plan_create(kind, N, eb, d0, inner, group_num_params=g,
+                                           host_only=True)
+                ss.fsdp_plan_validate(plan)
+                plan.destroy()
+
+
 def test_worked_example_through_the_library(ss):
     for kind, per_rank in ((ss.SS_FLAT_ORIG_FALSE, 2), (ss.SS_FLAT_ORIG_TRUE, 4),
                            (ss.SS_PER_PARAM_DIM0, 3)):
