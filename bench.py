@@ -848,6 +848,18 @@ def _rows_small(ss, peak, want):
         _row("step on the tiny MLP (16,640 params, N=2): replayed from a CUDA graph",
              st1.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
              extra={"us_per_step": ms * 1e3})
+        # one kernel: fsdp_sharded_step with the all-gather written in the same pass
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s_):
+            st1.fused_step()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g1, stream=s_):
+                st1.fused_step()
+        torch.cuda.current_stream().wait_stream(s_)
+        ms, mn = _time_stream(lambda: g1.replay(), 500, warmup=20)
+        _row("step on the tiny MLP (16,640 params, N=2): one-pass kernel replayed from a graph",
+             st1.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
+             extra={"us_per_step": ms * 1e3})
 
     # -- config 3: awkward sizes, N=7 ------------------------------------------
     for kind in ((W.FLAT_ORIG_FALSE, W.FLAT_ORIG_TRUE) if "awkward" in want else ()):

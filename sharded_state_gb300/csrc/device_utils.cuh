@@ -55,18 +55,4 @@ __device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
                  : "memory");
 }
 
-// Index of the last segment in [lo, hi) whose start is <= u (segments sorted by start,
-// the first one starting at or before u).
-template <typename SegT>
-__device__ __forceinline__ int find_seg(const SegT* segs, int lo, int hi, int64_t u) {
-    while (hi - lo > 1) {
-        int mid = lo + ((hi - lo) >> 1);
-        if (segs[mid].start <= u)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    return lo;
-}
-
 }  // namespace ss

@@ -21,12 +21,6 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     raise TypeError(t.dtype)
 
 
-def from_np(a: np.ndarray, device="cuda") -> torch.Tensor:
-    if a.dtype == np.uint16:
-        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
-    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32).copy()).to(device)
-
-
 def header_functions() -> list:
     """Names of the functions include/shardstate.h declares."""
     with open(os.path.join(ROOT, "include", "shardstate.h")) as f:

@@ -34,7 +34,10 @@ def _hp_kwargs(step):
 
 
 def _small_sets():
-    sets = [("tiny_mlp_flat_true_N2", W.tiny_mlp(2, W.FLAT_ORIG_TRUE))]
+    sets = [("tiny_mlp_flat_true_N2", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
+            # world size 1: the reduce-scatter is the identity, the layouts degenerate
+            ("tiny_mlp_flat_false_N1", W.tiny_mlp(1, W.FLAT_ORIG_FALSE)),
+            ("awkward2d_perparam_N1", W.awkward_2d(1, count=30, max_rows=200))]
     for N in (3, 5, 7):
         for dt in (torch.bfloat16, torch.float32):
             tag = "bf16" if dt == torch.bfloat16 else "f32"

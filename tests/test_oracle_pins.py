@@ -6,7 +6,6 @@ that realise the same definition (torch.chunk, torch.optim.AdamW, torch's
 bf16 cast, torch.autograd), closed forms, invariants and brute force.
 """
 import itertools
-import math
 import os
 import random
 
