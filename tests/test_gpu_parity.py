@@ -452,3 +452,80 @@ def test_one_group_shorthand_matches_create(ss):
     assert a.info().as_dict() == b.info().as_dict()
     for i in (0, 57, 199):
         assert ss.fsdp_plan_param_offset(a, i) == ss.fsdp_plan_param_offset(b, i)
+
+
+# ---------------------------------------------------------------------------
+# special values: subnormals, infinities, NaN, values near the bf16 / fp32 limits
+# ---------------------------------------------------------------------------
+
+def _special_bf16(n, seed):
+    """bf16 bit patterns mixing ordinary values with subnormals, +-0, +-inf, NaN and
+    values near the largest finite bf16."""
+    rng = np.random.default_rng(seed)
+    normal = torch.from_numpy(rng.normal(0, 1e-3, n).astype(np.float32)).to(torch.bfloat16)
+    bits = normal.view(torch.int16).numpy().view(np.uint16).copy()
+    specials = np.array([0x0001, 0x8001, 0x007F, 0x807F, 0x0000, 0x8000, 0x7F80, 0xFF80,
+                         0x7FC0, 0x7F7F, 0xFF7F, 0x0080, 0x8080], np.uint16)
+    pick = rng.random(n) < 0.05
+    bits[pick] = rng.choice(specials, int(pick.sum()))
+    return bits
+
+
+def test_special_values_reduce_scatter_and_adamw(ss):
+    N, c = 8, 4096 + 5
+    total = N * c
+    plan = ss.fsdp_plan_layout(ss.SS_FLAT_ORIG_FALSE, N, 2, [total])
+    g_np = [_special_bf16(total, 100 + r) for r in range(N)]
+    grads = [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda() for b in g_np]
+    # state: ordinary values plus subnormal / zero masters
+    rng = np.random.default_rng(7)
+    master_np = rng.normal(0, 0.02, total).astype(np.float32)
+    master_np[::97] = np.float32(1e-40)           # subnormal fp32
+    master_np[::101] = 0.0
+    m_np = np.zeros(total, np.float32)
+    v_np = np.zeros(total, np.float32)
+    master = torch.from_numpy(master_np.copy()).cuda()
+    m = torch.zeros(total, device="cuda")
+    v = torch.zeros(total, device="cuda")
+    shards = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+    red = torch.empty(total, device="cuda")
+    hp = ss.adamw_params(step=1)
+    ss.fsdp_reduce_scatter_adamw(plan, grads, master, m, v, shards, hp, red)
+    torch.cuda.synchronize()
+    want = oracle.reduce_scatter(N, c, g_np)
+    got = to_np(red)
+    nan_w, nan_g = np.isnan(want), np.isnan(got)
+    np.testing.assert_array_equal(nan_w, nan_g)                         # NaN exactly where expected
+    np.testing.assert_array_equal(got[~nan_w].view(np.uint32),          # everything else bit-exact,
+                                  want[~nan_w].view(np.uint32))         # subnormals and infinities included
+    om, omm, ov = master_np.copy(), m_np.copy(), v_np.copy()
+    o_params = oracle.adamw(want, om, omm, ov, step=1, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                            weight_decay=0.01)
+    finite = np.isfinite(want) & np.isfinite(om) & np.isfinite(omm) & np.isfinite(ov)
+    gm, gmm, gv = to_np(master), to_np(m), to_np(v)
+    # non-finite results appear in the same places on both sides
+    np.testing.assert_array_equal(np.isfinite(gm), np.isfinite(om))
+    np.testing.assert_array_equal(np.isnan(gmm), np.isnan(omm))
+    check_adamw_state(gm[finite], gmm[finite], gv[finite], om[finite], omm[finite], ov[finite],
+                      master_np[finite], m_np[finite], want[finite])
+    # where the update is finite the bf16 parameter is the rounding of the master
+    fin = np.isfinite(gm)
+    np.testing.assert_array_equal(to_np(shards)[fin], oracle.bf16_round(gm[fin]))
+
+
+def test_special_values_ddp_average(ss):
+    N, T = 5, 7
+    numels = [1, 9, 64, 100, 3, 1031, 8]
+    g_np = [[_special_bf16(n, 1000 * r + t) for t, n in enumerate(numels)] for r in range(N)]
+    grads = [[torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda() for b in rank]
+             for rank in g_np]
+    outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for n in numels]
+    ss.ddp_bucket_pack_average(grads, 128, outs)
+    torch.cuda.synchronize()
+    want = oracle.ddp_average(g_np)
+    for o, w in zip(outs, want):
+        got = to_np(o)
+        wn = ((w & 0x7F80) == 0x7F80) & ((w & 0x7F) != 0)
+        gn = ((got & 0x7F80) == 0x7F80) & ((got & 0x7F) != 0)
+        np.testing.assert_array_equal(wn, gn)          # NaN in the same places (payload free)
+        np.testing.assert_array_equal(got[~wn], w[~wn])
