@@ -875,6 +875,33 @@ def _rows_small(ss, peak, want):
              st3.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
              extra={"us_per_step": ms * 1e3})
 
+    # -- the same awkward shapes scaled up until they are bandwidth-bound:
+    # odd-sized parameters at odd flat offsets (runs not congruent mod 16 bytes)
+    for kind in ((W.FLAT_ORIG_FALSE, W.PER_PARAM_DIM0) if "awkward" in want else ()):
+        if kind == W.PER_PARAM_DIM0:
+            ps4 = W.awkward_2d(7, count=200, max_rows=400_000)
+        else:
+            ps4 = W.awkward_1d(7, kind, torch.bfloat16, count=200, max_len=2_000_000)
+        st4 = Step(ss, ps4, 1)
+        P4, tot4 = st4.info["unpadded_numel"], st4.info["total_numel"]
+        g4 = next(st4._rank_grad_iter("cuda"))
+        buf4 = torch.empty(tot4, dtype=torch.bfloat16, device="cuda")
+        name = W.LAYOUT_NAMES[kind]
+        ms, mn = _time_stream(lambda: ss.fsdp_pack(st4.plan, g4, buf4), 20)
+        _row(f"large awkward ({name}, {P4:,} params, N=7): pack", P4, "params/s", ms, mn,
+             2 * P4 + 2 * tot4, peak)
+        ms, mn = _time_stream(lambda: st4.rs_adamw(), 20)
+        _row(f"large awkward ({name}, N=7): RS + AdamW", P4, "params/s", ms, mn,
+             (2 * 7 + 26) * tot4, peak)
+        ms, mn = _time_stream(lambda: st4.all_gather(), 20)
+        _row(f"large awkward ({name}, N=7): all-gather + unpack", P4, "params/s", ms, mn, 4 * P4,
+             peak)
+        ms, mn = _time_stream(lambda: st4.fused_step(), 20)
+        _row(f"large awkward ({name}, N=7): one-pass step", P4, "params/s", ms, mn,
+             (2 * 7 + 26) * tot4 + 2 * P4, peak)
+        del st4, g4, buf4
+        torch.cuda.empty_cache()
+
 
 
 def _rows_ddp(args, ss, oracle, peak, used, K, bits):

@@ -55,4 +55,64 @@ __device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
                  : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// 16 bytes at an address that is only 2- (or 4-) byte aligned
+// ---------------------------------------------------------------------------
+
+// Bytes [sh, sh + 16) of the 32 bytes a:b (little-endian), sh even in 2..14.
+__device__ __forceinline__ uint4 realign16(uint4 a, uint4 b, int sh) {
+    const int bs = (sh & 3) * 8;  // 0 or 16
+    uint4 o;
+    switch (sh >> 2) {
+        case 0:
+            o.x = __funnelshift_r(a.x, a.y, bs); o.y = __funnelshift_r(a.y, a.z, bs);
+            o.z = __funnelshift_r(a.z, a.w, bs); o.w = __funnelshift_r(a.w, b.x, bs);
+            break;
+        case 1:
+            o.x = __funnelshift_r(a.y, a.z, bs); o.y = __funnelshift_r(a.z, a.w, bs);
+            o.z = __funnelshift_r(a.w, b.x, bs); o.w = __funnelshift_r(b.x, b.y, bs);
+            break;
+        case 2:
+            o.x = __funnelshift_r(a.z, a.w, bs); o.y = __funnelshift_r(a.w, b.x, bs);
+            o.z = __funnelshift_r(b.x, b.y, bs); o.w = __funnelshift_r(b.y, b.z, bs);
+            break;
+        default:
+            o.x = __funnelshift_r(a.w, b.x, bs); o.y = __funnelshift_r(b.x, b.y, bs);
+            o.z = __funnelshift_r(b.y, b.z, bs); o.w = __funnelshift_r(b.z, b.w, bs);
+            break;
+    }
+    return o;
+}
+
+// Read-only load of the 16 bytes at p (p even).  A misaligned p is served by
+// the two aligned 16-byte blocks that cover [p, p + 16): each holds at least
+// one of the requested bytes, so neither can lie on a page the caller does
+// not own.
+__device__ __forceinline__ uint4 ld_any16(const void* p) {
+    const unsigned sh = (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u);
+    if (sh == 0) return ld_stream_u4(p);
+    const unsigned char* base = static_cast<const unsigned char*>(p) - sh;
+    return realign16(ld_stream_u4(base), ld_stream_u4(base + 16), (int)sh);
+}
+
+// Store 16 bytes at p (p even): one vector store when aligned, four 32-bit
+// stores when 4-byte aligned, else 2 + 4 + 4 + 4 + 2 bytes.
+__device__ __forceinline__ void st_any16(void* p, uint4 v) {
+    const unsigned sh = (unsigned)(reinterpret_cast<uintptr_t>(p) & 15u);
+    unsigned char* c = static_cast<unsigned char*>(p);
+    if (sh == 0) {
+        st_stream_u4(p, v);
+    } else if ((sh & 3u) == 0) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(c);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else {
+        *reinterpret_cast<uint16_t*>(c) = (uint16_t)(v.x & 0xFFFFu);
+        uint32_t* w = reinterpret_cast<uint32_t*>(c + 2);
+        w[0] = __funnelshift_r(v.x, v.y, 16);
+        w[1] = __funnelshift_r(v.y, v.z, 16);
+        w[2] = __funnelshift_r(v.z, v.w, 16);
+        *reinterpret_cast<uint16_t*>(c + 14) = (uint16_t)(v.w >> 16);
+    }
+}
+
 }  // namespace ss

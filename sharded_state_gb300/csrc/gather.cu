@@ -9,8 +9,11 @@
 // copies one tile (two dependent metadata loads, then 4 x 128-bit vectors per
 // thread in flight), and the grid is one CTA per tile, so all SMs stream
 // through a narrow, advancing window of HBM.  A piece moves in 128-bit vectors
-// whenever source and destination are congruent mod 16 bytes, element by
-// element otherwise.  Pack also writes zeros over the pad segments' tiles.
+// when source and destination are congruent mod 16 bytes; otherwise the stores
+// stay 16-byte aligned and every source vector is rebuilt in registers from the
+// two aligned blocks that cover it (element copies remain only for several
+// mutually misaligned replicas).  Pack also writes zeros over the pad
+// segments' tiles.
 // Pure data movement: HBM-bound, 2 + 2*n_out bytes per bf16 element for the
 // all-gather, 4 for pack (plus pad writes).
 //
@@ -41,14 +44,63 @@ struct PtrTab {
 
 // Copy `nelem` elements of E bytes from src to the n_dst destinations; every
 // thread of the CTA takes part.  When all destinations are congruent to src
-// mod 16, the body moves in 128-bit vectors (4 per thread in flight).
-template <int E>
+// mod 16, the body moves in 128-bit vectors (4 per thread in flight); with a
+// single destination that is not, stores stay aligned and each source vector
+// is rebuilt from the two aligned blocks covering it (REALIGN).
+template <int E, bool REALIGN = true>
 __device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
                                          const unsigned char* src, int64_t nelem) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const uintptr_t s = reinterpret_cast<uintptr_t>(src);
     bool vec = true;
     for (int j = 0; j < n_dst; ++j) vec &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ s) & 15u) == 0;
+    bool dst_congruent = true;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
+    for (int j = 1; j < n_dst; ++j)
+        dst_congruent &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ d0) & 15u) == 0;
+    if (REALIGN && !vec && dst_congruent) {
+        // source and destinations differ mod 16 bytes: align the stores and
+        // rebuild each 16-byte source vector from the two aligned blocks that
+        // cover it
+        int64_t head = (int64_t)(((16u - (d0 & 15u)) & 15u) / E);
+        if (head > nelem) head = nelem;
+        if (tid < head) {
+            if (E == 2) {
+                uint16_t x = reinterpret_cast<const uint16_t*>(src)[tid];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[tid] = x;
+            } else {
+                uint32_t x = reinterpret_cast<const uint32_t*>(src)[tid];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[tid] = x;
+            }
+        }
+        const int64_t nvec = (nelem - head) * E / 16;
+        const unsigned char* sv = src + head * E;
+        int64_t q = tid;
+        for (; q + nt < nvec; q += 2 * nt) {
+            const uint4 x0 = ss::ld_any16(sv + 16 * q);
+            const uint4 x1 = ss::ld_any16(sv + 16 * (q + nt));
+            for (int j = 0; j < n_dst; ++j) {
+                ss::st_stream_u4(dst[j] + head * E + 16 * q, x0);
+                ss::st_stream_u4(dst[j] + head * E + 16 * (q + nt), x1);
+            }
+        }
+        for (; q < nvec; q += nt) {
+            const uint4 x = ss::ld_any16(sv + 16 * q);
+            for (int j = 0; j < n_dst; ++j) ss::st_stream_u4(dst[j] + head * E + 16 * q, x);
+        }
+        const int64_t done = head + nvec * 16 / E;
+        if (tid < nelem - done) {
+            const int64_t k = done + tid;
+            if (E == 2) {
+                uint16_t x = reinterpret_cast<const uint16_t*>(src)[k];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[k] = x;
+            } else {
+                uint32_t x = reinterpret_cast<const uint32_t*>(src)[k];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[k] = x;
+            }
+        }
+        return;
+    }
     if (!vec) {
         for (int64_t k = tid; k < nelem; k += nt) {
             if (E == 2) {
@@ -151,7 +203,7 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
             for (int j = 0; j < nd; ++j)
                 dsts[j] = static_cast<unsigned char*>(tab.p[(j0 + j) * ptr_stride + slot]) +
                           (sg.param_off + off) * E;
-            cta_copy<E>(dsts, nd, src, len);
+            cta_copy<E, false>(dsts, nd, src, len);
         }
     } else {
         unsigned char* dst = packed + (sg.packed_off + off) * E;

@@ -81,14 +81,19 @@ __device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const Ptr
 
 // NR > 0: exactly NR ranks, fully unrolled; NR == 0: any N, the first 8 ranks'
 // loads predicated and kept in flight together, the rest one by one.
-template <int NR, bool UNPACKED, int GATHER, bool WRITE_G>
+// f is 8-aligned (packed side); ANY: the per-parameter side (gradients read
+// at k, outputs written at k) may be misaligned and is read / written through
+// ld_any16 / st_any16.
+template <int NR, bool UNPACKED, int GATHER, bool WRITE_G, bool ANY = false>
 __device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, int slot,
                                          int64_t f, int64_t k) {
     const int n = NR > 0 ? NR : a.N;
     uint4 w[kMaxVec];
 #pragma unroll
     for (int r = 0; r < kMaxVec; ++r)
-        if (r < n) w[r] = ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
+        if (r < n)
+            w[r] = (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
+                                     : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
     const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
     const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
     const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
@@ -109,7 +114,8 @@ __device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, i
         }
     }
     for (int r = kMaxVec; NR == 0 && r < n; ++r) {  // ranks beyond the first 8
-        const uint4 x = ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
+        const uint4 x = (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
+                                          : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
         s[0] = __fadd_rn(s[0], ss::bf16_lo(x.x));
         s[1] = __fadd_rn(s[1], ss::bf16_hi(x.x));
         s[2] = __fadd_rn(s[2], ss::bf16_lo(x.y));
@@ -146,8 +152,13 @@ __device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, i
     ss::st_stream_u4(a.shards + f, p);
     if (GATHER) {
         const int goff = UNPACKED ? n * a.w : 0;
-        for (int j = 0; j < a.n_out; ++j)
-            ss::st_stream_u4(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k, p);
+        for (int j = 0; j < a.n_out; ++j) {
+            uint16_t* o = static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k;
+            if (ANY)
+                ss::st_any16(o, p);
+            else
+                ss::st_stream_u4(o, p);
+        }
     }
 }
 
@@ -191,30 +202,38 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
     const int slot = sg.param - a.param_base;
     const int64_t f0 = sg.packed_off + off;  // packed index of the tile's first element
     const int64_t k0 = sg.param_off + off;   // index inside the parameter tensor
-    // vector path: the packed index and every per-parameter pointer 16-byte aligned
-    bool vec = (f0 & 7) == 0;
-    if (UNPACKED)
-        for (int r = 0; r < a.N; ++r)
-            vec &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k0) & 15u) == 0);
-    if (GATHER) {
-        const int goff = UNPACKED ? a.N * a.w : 0;
-        for (int j = 0; j < a.n_out; ++j)
-            vec &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + j * a.w + slot]) + k0) & 15u) == 0);
-    }
     // this CTA's part [p0, p1) of the tile
     const int64_t p0 = (int64_t)blockIdx.y * kPart;
     const int64_t p1 = p0 + kPart < len ? p0 + kPart : len;
     if (p0 >= p1) return;
-    if (vec) {
-        const int64_t nvec = (p1 - p0) / 8;
-        for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + p0 + 8 * q, k0 + p0 + 8 * q);
-        for (int64_t e = p0 + 8 * nvec + threadIdx.x; e < p1; e += kThreads)
-            step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
-    } else {
-        for (int64_t e = p0 + threadIdx.x; e < p1; e += kThreads)
-            step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
+    // scalar head until the packed index is 8-aligned, then 8-element vectors
+    // (packed side aligned; the per-parameter side aligned or realigned), then
+    // a scalar tail
+    int64_t h = (8 - ((f0 + p0) & 7)) & 7;
+    if (h > p1 - p0) h = p1 - p0;
+    for (int64_t e = p0 + threadIdx.x; e < p0 + h; e += kThreads)
+        step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
+    const int64_t b0 = p0 + h;
+    const int64_t nvec = (p1 - b0) / 8;
+    bool aligned = true;  // every per-parameter pointer 16-byte aligned at k0 + b0
+    if (UNPACKED)
+        for (int r = 0; r < a.N; ++r)
+            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k0 + b0) & 15u) == 0);
+    if (GATHER) {
+        const int goff = UNPACKED ? a.N * a.w : 0;
+        for (int j = 0; j < a.n_out; ++j)
+            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + j * a.w + slot]) + k0 + b0) & 15u) == 0);
     }
+    if (aligned) {
+        for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
+            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + b0 + 8 * q, k0 + b0 + 8 * q);
+    } else {
+        for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
+            step_vec<NR, UNPACKED, GATHER, WRITE_G, true>(a, tab, slot, f0 + b0 + 8 * q,
+                                                          k0 + b0 + 8 * q);
+    }
+    for (int64_t e = b0 + 8 * nvec + threadIdx.x; e < p1; e += kThreads)
+        step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
 }
 
 using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
