@@ -189,7 +189,10 @@ __device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab
 constexpr int kSub = ss::kTileBytes / 2 / 8 / kThreads;  // 4 for 16 KiB bf16 tiles
 static_assert(kSub * kThreads * 8 * 2 == ss::kTileBytes, "tile split");
 
-template <int NR, bool UNPACKED, int GATHER, bool WRITE_G>
+// GEN false: the host has checked that every segment is whole 16-byte vectors
+// on both sides and every per-parameter pointer is 16-byte aligned, so each
+// CTA part is aligned vectors only.  GEN true: any alignment.
+template <int NR, bool UNPACKED, int GATHER, bool WRITE_G, bool GEN>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
                   StepArgs a, PtrTab tab) {
@@ -206,6 +209,12 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
     const int64_t p0 = (int64_t)blockIdx.y * kPart;
     const int64_t p1 = p0 + kPart < len ? p0 + kPart : len;
     if (p0 >= p1) return;
+    if (!GEN) {
+        const int64_t nv = (p1 - p0) / 8;
+        for (int64_t q = threadIdx.x; q < nv; q += kThreads)
+            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + p0 + 8 * q, k0 + p0 + 8 * q);
+        return;
+    }
     // scalar head until the packed index is 8-aligned, then 8-element vectors
     // (packed side aligned; the per-parameter side aligned or realigned), then
     // a scalar tail
@@ -238,15 +247,21 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
 
 using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
 
+template <int NR, bool U, bool GEN>
+Kern pick4(int gather, bool wg) {
+    if (gather == 0)
+        return wg ? fused_step_kernel<NR, U, 0, true, GEN> : fused_step_kernel<NR, U, 0, false, GEN>;
+    return wg ? fused_step_kernel<NR, U, 1, true, GEN> : fused_step_kernel<NR, U, 1, false, GEN>;
+}
+
 template <int NR, bool U>
-Kern pick3(int gather, bool wg) {
-    if (gather == 0) return wg ? fused_step_kernel<NR, U, 0, true> : fused_step_kernel<NR, U, 0, false>;
-    return wg ? fused_step_kernel<NR, U, 1, true> : fused_step_kernel<NR, U, 1, false>;
+Kern pick3(int gather, bool wg, bool gen) {
+    return gen ? pick4<NR, U, true>(gather, wg) : pick4<NR, U, false>(gather, wg);
 }
 
 template <bool U>
-Kern pick2(int N, int gather, bool wg) {
-    return N == 8 ? pick3<8, U>(gather, wg) : pick3<0, U>(gather, wg);
+Kern pick2(int N, int gather, bool wg, bool gen) {
+    return N == 8 ? pick3<8, U>(gather, wg, gen) : pick3<0, U>(gather, wg, gen);
 }
 
 AdamCoef make_coef(const ss_adamw* hp) {
@@ -299,17 +314,20 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             a.packed_grads.p[r] = s->rank_grads[r];
         }
     }
+    bool gen = !plan->vec_aligned;  // true: some run needs the general (realigning) kernel
     for (int i = pa; i < pb; ++i) {
         if (plan->numel[i] == 0) continue;
         for (int r = 0; unpacked && r < N; ++r) {
             const void* q = s->rank_param_grads[(size_t)r * n + i];
             if (!q) return SS_EINVAL;
             if (!ss::aligned(q, 2)) return SS_EALIGN;
+            gen |= !ss::aligned(q, 16);
         }
         for (int j = 0; j < s->n_out; ++j) {
             const void* q = s->params_out[(size_t)j * n + i];
             if (!q) return SS_EINVAL;
             if (!ss::aligned(q, 2)) return SS_EALIGN;
+            gen |= !ss::aligned(q, 16);
         }
     }
     a.master = s->master;
@@ -323,8 +341,8 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     const int per_param = (unpacked ? N : 0) + s->n_out;
     if (per_param > kTab) return SS_EINVAL;
     const int wmax = per_param > 0 ? kTab / per_param : (pb - pa > 0 ? pb - pa : 1);
-    Kern fn = unpacked ? pick2<true>(N, s->n_out > 0, s->reduced_grad_out != nullptr)
-                       : pick2<false>(N, s->n_out > 0, s->reduced_grad_out != nullptr);
+    Kern fn = unpacked ? pick2<true>(N, s->n_out > 0, s->reduced_grad_out != nullptr, gen)
+                       : pick2<false>(N, s->n_out > 0, s->reduced_grad_out != nullptr, gen);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     PtrTab tab;
     constexpr int64_t kMaxGrid = (int64_t)1 << 30;
