@@ -182,15 +182,26 @@ __device__ __forceinline__ void cta_zero(unsigned char* dst, int64_t nelem) {
 // DIR 0: all-gather + unpack (packed -> params); DIR 1: pack (params -> packed).
 // DIR 2: all-gather + unpack with n_out > 1 replicas.
 template <int E, int CAP, int DIR>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, DIR == 2 ? 2 : 6)
 tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
                  unsigned char* packed, PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out) {
     constexpr int64_t T = ss::kTileBytes / E;
     const ss::Tile tl = tiles[t_lo + blockIdx.x];
     const ss::Seg sg = segs[tl.seg];
-    const int64_t off = (int64_t)tl.idx * T;
-    const int64_t len = sg.len - off < T ? sg.len - off : T;
     const int slot = sg.param - param_base;
+    // The segment's tile starts are moved back by u elements, u = how far the
+    // stores' side (the packed buffer for DIR 1, the parameter otherwise; the
+    // source for DIR 2) sits past a 16-byte boundary at the segment's first
+    // element.  Every tile but the first then starts aligned and every tile
+    // but the last is whole vectors, so a misaligned segment pays for one head
+    // and one tail, not one per tile.  The last tile runs to the segment end.
+    const uintptr_t side =
+        DIR == 0 ? reinterpret_cast<uintptr_t>(tab.p[slot]) + (uintptr_t)(sg.param_off * E)
+                 : reinterpret_cast<uintptr_t>(packed) + (uintptr_t)(sg.packed_off * E);
+    const int64_t u = (int64_t)((side & 15u) / E);
+    const int64_t idx = tl.idx;
+    const int64_t off = idx == 0 ? 0 : idx * T - u;
+    const int64_t len = ((idx + 1) * T >= sg.len ? sg.len : (idx + 1) * T - u) - off;
     if (DIR == 0) {
         unsigned char* dst = static_cast<unsigned char*>(tab.p[slot]) + (sg.param_off + off) * E;
         cta_copy<E>(&dst, 1, packed + (sg.packed_off + off) * E, len);

@@ -215,34 +215,43 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
             step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + p0 + 8 * q, k0 + p0 + 8 * q);
         return;
     }
-    // scalar head until the packed index is 8-aligned, then 8-element vectors
-    // (packed side aligned; the per-parameter side aligned or realigned), then
-    // a scalar tail
-    int64_t h = (8 - ((f0 + p0) & 7)) & 7;
-    if (h > p1 - p0) h = p1 - p0;
-    for (int64_t e = p0 + threadIdx.x; e < p0 + h; e += kThreads)
-        step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
-    const int64_t b0 = p0 + h;
-    const int64_t nvec = (p1 - b0) / 8;
-    bool aligned = true;  // every per-parameter pointer 16-byte aligned at k0 + b0
+    // GEN: the part boundaries of a segment are moved back by u = packed_off
+    // mod 8 elements, so every part but the segment's first starts on an
+    // 8-aligned packed index and every part but its last is whole vectors;
+    // the scalar head and tail (< 8 elements each) occur once per segment, not
+    // once per part, and the head runs on the last threads, which have no
+    // vector in a segment's first part.  Vectors: packed side aligned,
+    // per-parameter side aligned or realigned in registers.
+    const int64_t j = (int64_t)tl.idx * kSub + blockIdx.y;  // part index within the segment
+    const int64_t u = sg.packed_off & 7;
+    const int64_t e0 = j == 0 ? 0 : j * kPart - u;
+    const int64_t e1 = (j + 1) * kPart >= sg.len ? sg.len : (j + 1) * kPart - u;
+    const int64_t fs = sg.packed_off, ks = sg.param_off;
+    int64_t h = (8 - ((fs + e0) & 7)) & 7;
+    if (h > e1 - e0) h = e1 - e0;
+    const int hi_t = kThreads - 1 - (int)threadIdx.x;
+    if (hi_t < h) step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, fs + e0 + hi_t, ks + e0 + hi_t);
+    const int64_t b0 = e0 + h;
+    const int64_t nvec = (e1 - b0) / 8;
+    bool aligned = true;  // every per-parameter pointer 16-byte aligned at ks + b0
     if (UNPACKED)
         for (int r = 0; r < a.N; ++r)
-            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k0 + b0) & 15u) == 0);
+            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + ks + b0) & 15u) == 0);
     if (GATHER) {
         const int goff = UNPACKED ? a.N * a.w : 0;
-        for (int j = 0; j < a.n_out; ++j)
-            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + j * a.w + slot]) + k0 + b0) & 15u) == 0);
+        for (int jj = 0; jj < a.n_out; ++jj)
+            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + jj * a.w + slot]) + ks + b0) & 15u) == 0);
     }
     if (aligned) {
         for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + b0 + 8 * q, k0 + b0 + 8 * q);
+            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
     } else {
         for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED, GATHER, WRITE_G, true>(a, tab, slot, f0 + b0 + 8 * q,
-                                                          k0 + b0 + 8 * q);
+            step_vec<NR, UNPACKED, GATHER, WRITE_G, true>(a, tab, slot, fs + b0 + 8 * q,
+                                                          ks + b0 + 8 * q);
     }
-    for (int64_t e = b0 + 8 * nvec + threadIdx.x; e < p1; e += kThreads)
-        step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + e, k0 + e);
+    for (int64_t e = b0 + 8 * nvec + threadIdx.x; e < e1; e += kThreads)
+        step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, fs + e, ks + e);
 }
 
 using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
