@@ -84,7 +84,9 @@ __device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const Ptr
 // f is 8-aligned (packed side); ANY: the per-parameter side (gradients read
 // at k, outputs written at k) may be misaligned and is read / written through
 // ld_any16 / st_any16.
-template <int NR, bool UNPACKED, int GATHER, bool WRITE_G, bool ANY = false>
+// The reduced-gradient output (a.gout) and the n_out per-parameter outputs
+// are runtime options: one pointer test and a loop of n_out stores.
+template <int NR, bool UNPACKED, bool ANY = false>
 __device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, int slot,
                                          int64_t f, int64_t k) {
     const int n = NR > 0 ? NR : a.N;
@@ -129,7 +131,7 @@ __device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, i
     float g[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) g[e] = __fdiv_rn(s[e], fN);
-    if (WRITE_G) {
+    if (a.gout) {
         ss::st_stream_f4(a.gout + f, make_float4(g[0], g[1], g[2], g[3]));
         ss::st_stream_f4(a.gout + f + 4, make_float4(g[4], g[5], g[6], g[7]));
     }
@@ -150,26 +152,24 @@ __device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, i
     p.z = ss::pack_bf16x2(th[4], th[5]);
     p.w = ss::pack_bf16x2(th[6], th[7]);
     ss::st_stream_u4(a.shards + f, p);
-    if (GATHER) {
-        const int goff = UNPACKED ? n * a.w : 0;
-        for (int j = 0; j < a.n_out; ++j) {
-            uint16_t* o = static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k;
-            if (ANY)
-                ss::st_any16(o, p);
-            else
-                ss::st_stream_u4(o, p);
-        }
+    const int goff = UNPACKED ? n * a.w : 0;
+    for (int j = 0; j < a.n_out; ++j) {
+        uint16_t* o = static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k;
+        if (ANY)
+            ss::st_any16(o, p);
+        else
+            ss::st_stream_u4(o, p);
     }
 }
 
-template <bool UNPACKED, int GATHER, bool WRITE_G>
+template <bool UNPACKED>
 __device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab, int slot,
                                             int64_t f, int64_t k) {
     const int n = a.N;
     float s = ss::bf16_to_f32(*grad_ptr<UNPACKED>(a, tab, 0, slot, f, k));
     for (int r = 1; r < n; ++r) s = __fadd_rn(s, ss::bf16_to_f32(*grad_ptr<UNPACKED>(a, tab, r, slot, f, k)));
     const float g = __fdiv_rn(s, (float)n);
-    if (WRITE_G) a.gout[f] = g;
+    if (a.gout) a.gout[f] = g;
     float th = a.master[f], m = a.exp_avg[f], v = a.exp_avg_sq[f];
     adamw_elem(g, th, m, v, a.c);
     a.master[f] = th;
@@ -177,10 +177,8 @@ __device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab
     a.exp_avg_sq[f] = v;
     const uint16_t p = ss::f32_to_bf16(th);
     a.shards[f] = p;
-    if (GATHER) {
-        const int goff = UNPACKED ? n * a.w : 0;
-        for (int j = 0; j < a.n_out; ++j) static_cast<uint16_t*>(tab.p[goff + j * a.w + slot])[k] = p;
-    }
+    const int goff = UNPACKED ? n * a.w : 0;
+    for (int j = 0; j < a.n_out; ++j) static_cast<uint16_t*>(tab.p[goff + j * a.w + slot])[k] = p;
 }
 
 // kSub CTAs per data tile (blockIdx.y): each takes one 8-element vector per
@@ -192,7 +190,7 @@ static_assert(kSub * kThreads * 8 * 2 == ss::kTileBytes, "tile split");
 // GEN false: the host has checked that every segment is whole 16-byte vectors
 // on both sides and every per-parameter pointer is 16-byte aligned, so each
 // CTA part is aligned vectors only.  GEN true: any alignment.
-template <int NR, bool UNPACKED, int GATHER, bool WRITE_G, bool GEN>
+template <int NR, bool UNPACKED, bool GEN>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
                   StepArgs a, PtrTab tab) {
@@ -212,7 +210,7 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
     if (!GEN) {
         const int64_t nv = (p1 - p0) / 8;
         for (int64_t q = threadIdx.x; q < nv; q += kThreads)
-            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, f0 + p0 + 8 * q, k0 + p0 + 8 * q);
+            step_vec<NR, UNPACKED>(a, tab, slot, f0 + p0 + 8 * q, k0 + p0 + 8 * q);
         return;
     }
     // GEN: the part boundaries of a segment are moved back by u = packed_off
@@ -230,47 +228,48 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
     int64_t h = (8 - ((fs + e0) & 7)) & 7;
     if (h > e1 - e0) h = e1 - e0;
     const int hi_t = kThreads - 1 - (int)threadIdx.x;
-    if (hi_t < h) step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, fs + e0 + hi_t, ks + e0 + hi_t);
+    if (hi_t < h) step_scalar<UNPACKED>(a, tab, slot, fs + e0 + hi_t, ks + e0 + hi_t);
     const int64_t b0 = e0 + h;
     const int64_t nvec = (e1 - b0) / 8;
     bool aligned = true;  // every per-parameter pointer 16-byte aligned at ks + b0
     if (UNPACKED)
         for (int r = 0; r < a.N; ++r)
             aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + ks + b0) & 15u) == 0);
-    if (GATHER) {
-        const int goff = UNPACKED ? a.N * a.w : 0;
-        for (int jj = 0; jj < a.n_out; ++jj)
-            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + jj * a.w + slot]) + ks + b0) & 15u) == 0);
-    }
+    const int goff = UNPACKED ? a.N * a.w : 0;
+    for (int jj = 0; jj < a.n_out; ++jj)
+        aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + jj * a.w + slot]) + ks + b0) & 15u) == 0);
     if (aligned) {
         for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED, GATHER, WRITE_G>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
+            step_vec<NR, UNPACKED>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
     } else {
         for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED, GATHER, WRITE_G, true>(a, tab, slot, fs + b0 + 8 * q,
+            step_vec<NR, UNPACKED, true>(a, tab, slot, fs + b0 + 8 * q,
                                                           ks + b0 + 8 * q);
     }
     for (int64_t e = b0 + 8 * nvec + threadIdx.x; e < e1; e += kThreads)
-        step_scalar<UNPACKED, GATHER, WRITE_G>(a, tab, slot, fs + e, ks + e);
+        step_scalar<UNPACKED>(a, tab, slot, fs + e, ks + e);
 }
 
 using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
 
-template <int NR, bool U, bool GEN>
-Kern pick4(int gather, bool wg) {
-    if (gather == 0)
-        return wg ? fused_step_kernel<NR, U, 0, true, GEN> : fused_step_kernel<NR, U, 0, false, GEN>;
-    return wg ? fused_step_kernel<NR, U, 1, true, GEN> : fused_step_kernel<NR, U, 1, false, GEN>;
-}
-
 template <int NR, bool U>
-Kern pick3(int gather, bool wg, bool gen) {
-    return gen ? pick4<NR, U, true>(gather, wg) : pick4<NR, U, false>(gather, wg);
+Kern pick_gen(bool gen) {
+    return gen ? fused_step_kernel<NR, U, true> : fused_step_kernel<NR, U, false>;
 }
 
+// N = 2..8 get a fully unrolled instance; other N take the general one.
 template <bool U>
-Kern pick2(int N, int gather, bool wg, bool gen) {
-    return N == 8 ? pick3<8, U>(gather, wg, gen) : pick3<0, U>(gather, wg, gen);
+Kern pick_n(int N, bool gen) {
+    switch (N) {
+        case 2: return pick_gen<2, U>(gen);
+        case 3: return pick_gen<3, U>(gen);
+        case 4: return pick_gen<4, U>(gen);
+        case 5: return pick_gen<5, U>(gen);
+        case 6: return pick_gen<6, U>(gen);
+        case 7: return pick_gen<7, U>(gen);
+        case 8: return pick_gen<8, U>(gen);
+        default: return pick_gen<0, U>(gen);
+    }
 }
 
 AdamCoef make_coef(const ss_adamw* hp) {
@@ -350,8 +349,7 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     const int per_param = (unpacked ? N : 0) + s->n_out;
     if (per_param > kTab) return SS_EINVAL;
     const int wmax = per_param > 0 ? kTab / per_param : (pb - pa > 0 ? pb - pa : 1);
-    Kern fn = unpacked ? pick2<true>(N, s->n_out > 0, s->reduced_grad_out != nullptr, gen)
-                       : pick2<false>(N, s->n_out > 0, s->reduced_grad_out != nullptr, gen);
+    Kern fn = unpacked ? pick_n<true>(N, gen) : pick_n<false>(N, gen);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     PtrTab tab;
     constexpr int64_t kMaxGrid = (int64_t)1 << 30;
