@@ -797,7 +797,27 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     ms, mn = _time_stream(lambda: ss.fsdp_all_gather_unpack(st8.plan, st8.shards, outs8, N), K)
     _row("a4 all-gather + unpack, n_out=N=8 (every rank's copy)", P, "params/s", ms, mn,
          (2 + 2 * N) * P, peak)
-    del outs8, st, st8
+    # F4: the ZeRO-1/2 step ("Scaling data parallel" 9.1-9.2): reduce-scatter
+    # the full per-rank gradients, AdamW on each rank's own 1/N, then all-gather
+    # the updated bf16 parameters to every rank (n_out = N), the all-reduce
+    # split into RS + AG with the AG moved onto the parameters
+    outs8_arr = ss.ptr_array(outs8)
+
+    def zero12_two_calls():
+        st8.rs_adamw()
+        ss.fsdp_all_gather_unpack(st8.plan, st8.shards, outs8_arr, N)
+
+    def zero12_one_pass():
+        ss.fsdp_sharded_step(st8.plan, st8.master, st8.m, st8.v, st8.shards, st8.next_hp(),
+                             rank_grads=st8._grads_arr, params_out=outs8_arr, n_out=N)
+    ms, mn = _time_stream(zero12_two_calls, K)
+    _row("ZeRO-1/2 step: RS+AdamW, then all-gather to all N=8 ranks (two calls, 1.2B)", P,
+         "params/s", ms, mn, (2 * N + 26) * total + (2 + 2 * N) * P, peak, extra={"n_out": N})
+    ms, mn = _time_stream(zero12_one_pass, K)
+    _row("ZeRO-1/2 step: RS+AdamW writing all N=8 ranks' parameters in the same pass "
+         "(fsdp_sharded_step, 1.2B)", P, "params/s", ms, mn,
+         (2 * N + 26) * total + 2 * N * P, peak, extra={"n_out": N})
+    del outs8, outs8_arr, st, st8
     torch.cuda.empty_cache()
 
 

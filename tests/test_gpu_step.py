@@ -224,3 +224,45 @@ def test_sharded_step_argument_errors(ss):
         ss.fsdp_sharded_step(f32plan, master, m, v, master, hp, rank_grads=[master, master])
     assert e.value.status == ss.SS_EINVAL
     torch.cuda.synchronize()
+
+
+def test_zero12_step_every_rank_gets_the_parameters(ss):
+    """The ZeRO-1/2 step ("Scaling data parallel" 9.1-9.2): RS+AdamW, then the
+    updated bf16 parameters all-gathered to every one of the N ranks.  The one
+    pass with n_out = N must equal RS+AdamW followed by the all-gather with
+    n_out = N bit for bit, and every replica must equal the oracle's unpack of
+    the new shards."""
+    ps = W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)
+    su = Setup(ss, ps)
+    N, total = su.N, su.total
+    grads_cpu = W.make_rank_grads(ps)
+    packed = []
+    for r in range(N):
+        b = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+        ss.fsdp_pack(su.plan, [g.cuda() for g in grads_cpu[r]], b)
+        packed.append(b)
+    sa, ma, mma, va = _state(ss, su)
+    sb, mb, mmb, vb = _state(ss, su)
+    outs_a = [torch.empty_like(p) for _ in range(N) for p in su.params]
+    outs_b, wholes = [], []
+    for _ in range(N):
+        for p in su.params:
+            o, w = guarded(p.numel(), torch.bfloat16)
+            outs_b.append(o)
+            wholes.append(w)
+    for step in (1, 2):
+        hp = ss.adamw_params(step=step, **_hp(step))
+        ss.fsdp_reduce_scatter_adamw(su.plan, packed, ma, mma, va, sa, hp)
+        ss.fsdp_all_gather_unpack(su.plan, sa, outs_a, n_out=N)
+        ss.fsdp_sharded_step(su.plan, mb, mmb, vb, sb, hp, rank_grads=packed, params_out=outs_b,
+                             n_out=N)
+        torch.cuda.synchronize()
+        for x, y in ((sa, sb), (ma, mb), (mma, mmb), (va, vb)):
+            np.testing.assert_array_equal(to_np(x).view(np.uint8), to_np(y).view(np.uint8))
+        want = su.oracle_unpack(to_np(sb), n_out=N)
+        n = len(su.params)
+        for j in range(N):
+            for i in range(n):
+                np.testing.assert_array_equal(to_np(outs_a[j * n + i]), to_np(outs_b[j * n + i]))
+                np.testing.assert_array_equal(to_np(outs_b[j * n + i]), want[j][i])
+    assert all(guards_intact(w) for w in wholes)
