@@ -42,6 +42,50 @@ struct PtrTab {
     void* p[CAP];
 };
 
+// Aligned 16-byte vectors q in [0, nvec) of dv <- the 16 source bytes at
+// sv + 16q, where sv sits sh = sv mod 16 bytes past a boundary (sh != 0).
+// Vector q is rebuilt from the aligned source blocks q and q + 1, block b
+// being the 16 bytes at sv - sh + 16b.  Warp w takes vectors [128w, 128w + 128)
+// of each chunk of 128 x (warps per CTA): lane L loads blocks 128w + 32j + L,
+// j < 4, all in one round, and takes block + 1 from lane L + 1 by a shuffle;
+// lane 31 takes it from lane 0's next group, and after the last group loads
+// it itself.  Each source block is thus loaded once, not twice.  Block q + 1
+// is loaded only for a vector q < nvec, and since sh != 0 it holds bytes of
+// that vector, so no load reaches past the 16-byte blocks the run touches.
+// The chunk loop is the same for every lane of a warp, so the shuffles see
+// the whole warp.
+__device__ __forceinline__ void cta_realign_vectors(unsigned char* dv, const unsigned char* sv,
+                                                    int64_t nvec) {
+    const int lane = threadIdx.x & 31;
+    const int64_t step = (int64_t)(blockDim.x >> 5) * 128;
+    const int sh = (int)(reinterpret_cast<uintptr_t>(sv) & 15u);
+    const unsigned char* base = sv - sh;
+    for (int64_t c0 = (int64_t)(threadIdx.x >> 5) * 128; c0 < nvec; c0 += step) {
+        uint4 x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t b = c0 + 32 * j + lane;
+            x[j] = b <= nvec ? ss::ld_stream_u4(base + 16 * b) : make_uint4(0, 0, 0, 0);
+        }
+        uint4 nx = make_uint4(0, 0, 0, 0);  // block c0 + 128, for lane 31's last vector
+        if (lane == 31 && c0 + 127 < nvec) nx = ss::ld_stream_u4(base + 16 * (c0 + 128));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // lane L reads lane L+1's value; lane 0 offers its next group's
+            // block, which is lane 31's successor block
+            const uint4 offer = (lane == 0 && j < 3) ? x[j < 3 ? j + 1 : j] : x[j];
+            uint4 nb;
+            nb.x = __shfl_sync(0xFFFFFFFFu, offer.x, (lane + 1) & 31);
+            nb.y = __shfl_sync(0xFFFFFFFFu, offer.y, (lane + 1) & 31);
+            nb.z = __shfl_sync(0xFFFFFFFFu, offer.z, (lane + 1) & 31);
+            nb.w = __shfl_sync(0xFFFFFFFFu, offer.w, (lane + 1) & 31);
+            if (j == 3 && lane == 31) nb = nx;
+            const int64_t q = c0 + 32 * j + lane;
+            if (q < nvec) ss::st_stream_u4(dv + 16 * q, ss::realign16(x[j], nb, sh));
+        }
+    }
+}
+
 // Copy `nelem` elements of E bytes from src to the n_dst destinations; every
 // thread of the CTA takes part.  When all destinations are congruent to src
 // mod 16, the body moves in 128-bit vectors (4 per thread in flight); with a
@@ -75,18 +119,13 @@ __device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
         }
         const int64_t nvec = (nelem - head) * E / 16;
         const unsigned char* sv = src + head * E;
-        int64_t q = tid;
-        for (; q + nt < nvec; q += 2 * nt) {
-            const uint4 x0 = ss::ld_any16(sv + 16 * q);
-            const uint4 x1 = ss::ld_any16(sv + 16 * (q + nt));
-            for (int j = 0; j < n_dst; ++j) {
-                ss::st_stream_u4(dst[j] + head * E + 16 * q, x0);
-                ss::st_stream_u4(dst[j] + head * E + 16 * (q + nt), x1);
+        if (n_dst == 1) {
+            cta_realign_vectors(dst[0] + head * E, sv, nvec);
+        } else {
+            for (int64_t q = tid; q < nvec; q += nt) {
+                const uint4 x = ss::ld_any16(sv + 16 * q);
+                for (int j = 0; j < n_dst; ++j) ss::st_stream_u4(dst[j] + head * E + 16 * q, x);
             }
-        }
-        for (; q < nvec; q += nt) {
-            const uint4 x = ss::ld_any16(sv + 16 * q);
-            for (int j = 0; j < n_dst; ++j) ss::st_stream_u4(dst[j] + head * E + 16 * q, x);
         }
         const int64_t done = head + nvec * 16 / E;
         if (tid < nelem - done) {
@@ -182,7 +221,7 @@ __device__ __forceinline__ void cta_zero(unsigned char* dst, int64_t nelem) {
 // DIR 0: all-gather + unpack (packed -> params); DIR 1: pack (params -> packed).
 // DIR 2: all-gather + unpack with n_out > 1 replicas.
 template <int E, int CAP, int DIR>
-__global__ void __launch_bounds__(kThreads, DIR == 2 ? 2 : 6)
+__global__ void __launch_bounds__(kThreads, DIR == 2 ? 2 : 5)
 tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
                  unsigned char* packed, PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out) {
     constexpr int64_t T = ss::kTileBytes / E;
