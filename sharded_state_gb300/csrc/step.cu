@@ -86,9 +86,11 @@ __device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const Ptr
 // ld_any16 / st_any16.
 // The reduced-gradient output (a.gout) and the n_out per-parameter outputs
 // are runtime options: one pointer test and a loop of n_out stores.
-template <int NR, bool UNPACKED, bool ANY = false>
-__device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, int slot,
-                                         int64_t f, int64_t k) {
+// OUTS false: the n_out outputs are left to the caller (the returned vector is
+// the new bf16 parameter vector).
+template <int NR, bool UNPACKED, bool ANY = false, bool OUTS = true>
+__device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, int slot,
+                                          int64_t f, int64_t k) {
     const int n = NR > 0 ? NR : a.N;
     uint4 w[kMaxVec];
 #pragma unroll
@@ -153,12 +155,66 @@ __device__ __forceinline__ void step_vec(const StepArgs& a, const PtrTab& tab, i
     p.w = ss::pack_bf16x2(th[6], th[7]);
     ss::st_stream_u4(a.shards + f, p);
     const int goff = UNPACKED ? n * a.w : 0;
-    for (int j = 0; j < a.n_out; ++j) {
+    for (int j = 0; OUTS && j < a.n_out; ++j) {
         uint16_t* o = static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k;
         if (ANY)
             ss::st_any16(o, p);
         else
             ss::st_stream_u4(o, p);
+    }
+    return p;
+}
+
+// Store bytes [lo, hi) of the 16-byte value v to blk + lo (blk 16-byte
+// aligned, lo and hi even), two bytes at a time.
+__device__ __forceinline__ void st_bytes(unsigned char* blk, uint4 v, int lo, int hi) {
+#pragma unroll
+    for (int b = 0; b < 16; b += 2) {
+        if (b >= lo && b < hi) {
+            const uint32_t w = b < 4 ? v.x : b < 8 ? v.y : b < 12 ? v.z : v.w;
+            *reinterpret_cast<uint16_t*>(blk + b) = (uint16_t)(w >> ((b & 2) * 8));
+        }
+    }
+}
+
+// The n_out per-parameter outputs of vectors q = 0..nvec-1 (one per thread,
+// thread q, nvec <= the CTA's threads), where output j's vector q goes to the
+// 16 bytes at o_j + 16q and o_j sits sh_j bytes past a 16-byte boundary.
+// Lane L takes vector q + 1 from lane L + 1 by a shuffle and writes the aligned
+// block that follows its own vector's start -- the last sh bytes of vector q
+// and the first 16 - sh of vector q + 1 -- with one 16-byte store.  Lane 31
+// and the last vector write only their own sh bytes of that block; lane 0 also
+// writes its first 16 - sh bytes into the block before, whose first sh bytes
+// belong to the previous warp's last vector (or to the scalar head).  Every
+// lane of a warp holding a vector calls this (invalid lanes pass p unused).
+template <bool UNPACKED>
+__device__ __forceinline__ void store_outputs_realigned(const StepArgs& a, const PtrTab& tab,
+                                                        int slot, int64_t k0, int q, int nvec,
+                                                        uint4 p) {
+    const int lane = threadIdx.x & 31;
+    uint4 nx;
+    nx.x = __shfl_down_sync(0xFFFFFFFFu, p.x, 1);
+    nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
+    nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
+    nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
+    if (q >= nvec) return;
+    const int goff = UNPACKED ? a.N * a.w : 0;
+    for (int j = 0; j < a.n_out; ++j) {
+        unsigned char* ob =
+            reinterpret_cast<unsigned char*>(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k0) +
+            16 * (int64_t)q;
+        const int sh = (int)(reinterpret_cast<uintptr_t>(ob) & 15u);
+        if (sh == 0) {
+            ss::st_stream_u4(ob, p);
+            continue;
+        }
+        unsigned char* blk = ob - sh + 16;  // the aligned block after this vector's start
+        const uint4 v = ss::realign16(p, nx, 16 - sh);
+        if (lane < 31 && q + 1 < nvec)
+            ss::st_stream_u4(blk, v);
+        else
+            st_bytes(blk, v, 0, sh);
+        if (lane == 0) st_bytes(blk - 16, ss::realign16(p, p, 16 - sh), sh, 16);
     }
 }
 
@@ -241,10 +297,19 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
     if (aligned) {
         for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
             step_vec<NR, UNPACKED>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
+    } else if (nvec <= kThreads) {
+        // one vector per thread; warps holding a vector take part whole, for
+        // the shuffles of the realigned output stores
+        const int q = threadIdx.x;
+        if ((q & ~31) < nvec) {
+            uint4 p = make_uint4(0, 0, 0, 0);
+            if (q < nvec)
+                p = step_vec<NR, UNPACKED, true, false>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
+            store_outputs_realigned<UNPACKED>(a, tab, slot, ks + b0, q, (int)nvec, p);
+        }
     } else {
         for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED, true>(a, tab, slot, fs + b0 + 8 * q,
-                                                          ks + b0 + 8 * q);
+            step_vec<NR, UNPACKED, true>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
     }
     for (int64_t e = b0 + 8 * nvec + threadIdx.x; e < e1; e += kThreads)
         step_scalar<UNPACKED>(a, tab, slot, fs + e, ks + e);
