@@ -59,12 +59,16 @@ def parse_args():
     ap.add_argument("--mode", choices=["step", "rows"], default="step",
                     help="step: the one-line headline; rows: one JSON line per hot-path row")
     ap.add_argument("--rows", default="all",
-                    help="rows mode: comma list of llama,block4096,tiny,awkward,ddp (default all)")
+                    help="rows mode: comma list of llama,block4096,tiny,awkward,awkward_large,ddp "
+                         "(default all; awkward_large: only the large awkward sets)")
     ap.add_argument("--step-kind", default="two_calls", choices=["two_calls", "fused"],
                     help="timed step: RS+AdamW then all-gather (two calls), or the one-pass "
                          "fsdp_sharded_step")
     ap.add_argument("--ddp-large", type=int, default=600,
                     help="rows mode: number of 4M-element DDP tensors (600 = the full list)")
+    ap.add_argument("--awkward-scale", type=float, default=1.0,
+                    help="rows mode: scale of the large awkward sets (1.0: 218M and 134M params; "
+                         "0.25 keeps a profiling capture to a few GB)")
     return ap.parse_args()
 
 
@@ -670,8 +674,8 @@ def run_rows(args):
         _rows_llama(args, ss, oracle, peak, used, K, bits)
     if "block4096" in want:
         _rows_block4096(ss, peak, K)
-    if "tiny" in want or "awkward" in want:
-        _rows_small(ss, peak, want)
+    if want & {"tiny", "awkward", "awkward_large"}:
+        _rows_small(ss, peak, want, args.awkward_scale)
     if "ddp" in want:
         _rows_ddp(args, ss, oracle, peak, used, K, bits)
 
@@ -838,15 +842,15 @@ def _rows_block4096(ss, peak, K):
     torch.cuda.empty_cache()
 
 
-def _rows_small(ss, peak, want):
+def _rows_small(ss, peak, want, awkward_scale=1.0):
     # -- config 1: tiny MLP, launch-bound -------------------------------------
-    ps1 = W.tiny_mlp()
-    st1 = Step(ss, ps1, 1)
-
-    def step1():
-        st1.rs_adamw()
-        st1.all_gather()
     if "tiny" in want:
+        ps1 = W.tiny_mlp()
+        st1 = Step(ss, ps1, 1)
+
+        def step1():
+            st1.rs_adamw()
+            st1.all_gather()
         ms, mn = _time_stream(step1, 200, warmup=20)
         by = step_bytes(2, st1.info["total_numel"], st1.info["unpadded_numel"], 1)
         _row("step on the tiny MLP (16,640 params, N=2): latency", st1.info["unpadded_numel"],
@@ -897,11 +901,13 @@ def _rows_small(ss, peak, want):
 
     # -- the same awkward shapes scaled up until they are bandwidth-bound:
     # odd-sized parameters at odd flat offsets (runs not congruent mod 16 bytes)
-    for kind in ((W.FLAT_ORIG_FALSE, W.PER_PARAM_DIM0) if "awkward" in want else ()):
+    large = "awkward" in want or "awkward_large" in want
+    for kind in ((W.FLAT_ORIG_FALSE, W.PER_PARAM_DIM0) if large else ()):
         if kind == W.PER_PARAM_DIM0:
-            ps4 = W.awkward_2d(7, count=200, max_rows=400_000)
+            ps4 = W.awkward_2d(7, count=200, max_rows=int(400_000 * awkward_scale))
         else:
-            ps4 = W.awkward_1d(7, kind, torch.bfloat16, count=200, max_len=2_000_000)
+            ps4 = W.awkward_1d(7, kind, torch.bfloat16, count=200,
+                               max_len=int(2_000_000 * awkward_scale))
         st4 = Step(ss, ps4, 1)
         P4, tot4 = st4.info["unpadded_numel"], st4.info["total_numel"]
         g4 = next(st4._rank_grad_iter("cuda"))
