@@ -433,15 +433,27 @@ def run_e2e(st: Step, args, stream, dist) -> dict:
         phys = os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
     except Exception:
         phys = 0
-    if phys and need * 2 > phys:
-        return {"value": None, "unit": "params/s", "skipped": f"needs {need / 1e9:.1f} GB pinned host"}
-    host_g = []
-    for r in range(N):
-        h = torch.empty(total, dtype=st.ps.dtype, pin_memory=True)
-        h.copy_(st.grads[r])
-        host_g.append(h)
-    host_out = [torch.empty(st.out_numel, dtype=st.ps.dtype, pin_memory=True)
-                for _ in range(st.n_out)]
+    # every rank on this node pins its own copy: keep all of them under half the RAM
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    if phys and need * local_ranks * 2 > phys:
+        return {"value": None, "unit": "params/s",
+                "skipped": f"needs {need / 1e9:.1f} GB pinned host per rank x {local_ranks} ranks"}
+    host_g, host_out, err = [], [], None
+    try:
+        for r in range(N):
+            h = torch.empty(total, dtype=st.ps.dtype, pin_memory=True)
+            h.copy_(st.grads[r])
+            host_g.append(h)
+        host_out = [torch.empty(st.out_numel, dtype=st.ps.dtype, pin_memory=True)
+                    for _ in range(st.n_out)]
+    except RuntimeError as e:  # pinned allocation refused
+        err = str(e).splitlines()[0][:120] if str(e) else "RuntimeError"
+    # every rank leaves together if any rank could not pin its buffers, so no
+    # rank is left waiting at the timed region's barrier
+    if max_over_ranks(dist, 1.0 if err else 0.0) > 0.0:
+        del host_g, host_out
+        return {"value": None, "unit": "params/s",
+                "skipped": f"pinned host allocation failed on a rank: {err or 'another rank'}"}
     G = len(st.ps.groups)
     groups = [ss.fsdp_plan_group(st.plan, g) for g in range(G)]
     numels = st.ps.numels()

@@ -77,3 +77,57 @@ def test_reference_arm_runs_on_rank_zero_only():
 def test_job_value_single_rank():
     assert bench.job_value(1_364_297_728, 200, 1, 1752.0) == pytest.approx(
         1_364_297_728 * 200 / 1.752)
+
+
+class _FakeStep:
+    """Just what run_e2e reads before its first CUDA call."""
+
+    def __init__(self):
+        self.info = {"total_numel": 64, "unpadded_numel": 60}
+        self.N = 2
+        self.n_out = 1
+        self.out_numel = 64
+        self.grads = [torch.zeros(64, dtype=torch.bfloat16) for _ in range(2)]
+
+        class _PS:
+            dtype = torch.bfloat16
+        self.ps = _PS()
+
+
+def _e2e_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), LOCAL_WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    real_empty = torch.empty
+
+    def empty(*a, pin_memory=False, **k):
+        # rank 1 cannot pin host memory; rank 0 can (served unpinned on CPU)
+        if pin_memory and rank == 1:
+            raise RuntimeError("pinned allocation refused (injected)")
+        return real_empty(*a, **k)
+    torch.empty = empty
+    try:
+        res = bench.run_e2e(_FakeStep(), None, None, dist)
+        q.put((rank, res))
+    finally:
+        torch.empty = real_empty
+        dist.destroy_process_group()
+
+
+def test_e2e_ranks_leave_together_when_one_cannot_pin():
+    """A rank whose pinned host allocation fails must not leave the others
+    waiting at the timed region's barrier: every rank reports the leg skipped."""
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_e2e_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, r in res:
+        assert r["value"] is None
+        assert "pinned host allocation failed" in r["skipped"]
+    assert "injected" in res[1][1]["skipped"]
