@@ -131,3 +131,13 @@ def test_e2e_ranks_leave_together_when_one_cannot_pin():
         assert r["value"] is None
         assert "pinned host allocation failed" in r["skipped"]
     assert "injected" in res[1][1]["skipped"]
+
+
+def test_host_stall_detection():
+    """The re-timing guard fires on one step far above the rest, not on jitter."""
+    assert not bench.host_stall([])
+    assert not bench.host_stall([8.7] * 200)
+    assert not bench.host_stall([8.7] * 199 + [9.5])           # ordinary jitter
+    assert bench.host_stall([8.7] * 199 + [4550.0])            # a multi-second stall
+    assert bench.host_stall([0.44, 4550.0, 0.44])
+    assert not bench.host_stall([0.02] * 99 + [0.5])           # 25x, but under 1 ms
