@@ -12,8 +12,10 @@
 // when source and destination are congruent mod 16 bytes; otherwise the stores
 // stay 16-byte aligned and every source vector is rebuilt in registers from the
 // two aligned blocks that cover it (element copies remain only for several
-// mutually misaligned replicas).  Pack also writes zeros over the pad
-// segments' tiles.
+// mutually misaligned replicas).  Inside a segment the tile starts are moved
+// back by the store side's misalignment, so a segment has one scalar head and
+// one scalar tail however many tiles it spans.  Pack also writes zeros over
+// the pad segments' tiles.
 // Pure data movement: HBM-bound, 2 + 2*n_out bytes per bf16 element for the
 // all-gather, 4 for pack (plus pad writes).
 //
@@ -90,7 +92,8 @@ __device__ __forceinline__ void cta_realign_vectors(unsigned char* dv, const uns
 // thread of the CTA takes part.  When all destinations are congruent to src
 // mod 16, the body moves in 128-bit vectors (4 per thread in flight); with a
 // single destination that is not, stores stay aligned and each source vector
-// is rebuilt from the two aligned blocks covering it (REALIGN).
+// is rebuilt from the two aligned blocks covering it (REALIGN; each block is
+// loaded once and passed to the neighbouring lane, cta_realign_vectors).
 template <int E, bool REALIGN = true>
 __device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
                                          const unsigned char* src, int64_t nelem) {
