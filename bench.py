@@ -965,7 +965,15 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
         ms, mn = _time_stream(lambda: st4.fused_step(), 20)
         _row(f"large awkward ({name}, N=7): one-pass step", P4, "params/s", ms, mn,
              (2 * 7 + 26) * tot4 + 2 * P4, peak)
-        del st4, g4, buf4
+        # fused copy-in: the 7 per-parameter gradient sets read in place, at
+        # their misaligned offsets inside each parameter
+        del g4
+        rank_sets = list(st4._rank_grad_iter("cuda"))
+        flat_pg = ss.ptr_array([g for rank in rank_sets for g in rank])
+        ms, mn = _time_stream(lambda: st4.fused_step(param_grads=flat_pg), 20)
+        _row(f"large awkward ({name}, N=7): one-pass step with fused copy-in", P4, "params/s",
+             ms, mn, (2 * 7 + 2) * P4 + 26 * tot4, peak)
+        del rank_sets, flat_pg, st4, buf4
         torch.cuda.empty_cache()
 
 

@@ -88,22 +88,13 @@ __device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const Ptr
 // are runtime options: one pointer test and a loop of n_out stores.
 // OUTS false: the n_out outputs are left to the caller (the returned vector is
 // the new bf16 parameter vector).
-template <int NR, bool UNPACKED, bool ANY = false, bool OUTS = true>
-__device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, int slot,
-                                          int64_t f, int64_t k) {
-    const int n = NR > 0 ? NR : a.N;
-    uint4 w[kMaxVec];
-#pragma unroll
-    for (int r = 0; r < kMaxVec; ++r)
-        if (r < n)
-            w[r] = (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
-                                     : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
-    const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
-    const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
-    const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
-    float s[8] = {ss::bf16_lo(w[0].x), ss::bf16_hi(w[0].x), ss::bf16_lo(w[0].y),
-                  ss::bf16_hi(w[0].y), ss::bf16_lo(w[0].z), ss::bf16_hi(w[0].z),
-                  ss::bf16_lo(w[0].w), ss::bf16_hi(w[0].w)};
+// Rank-order fp32 sum of the first min(n, 8) ranks' vectors, from rank 0's value.
+template <int NR>
+__device__ __forceinline__ void sum_ranks(const uint4 (&w)[kMaxVec], int n, float (&s)[8]) {
+    s[0] = ss::bf16_lo(w[0].x); s[1] = ss::bf16_hi(w[0].x);
+    s[2] = ss::bf16_lo(w[0].y); s[3] = ss::bf16_hi(w[0].y);
+    s[4] = ss::bf16_lo(w[0].z); s[5] = ss::bf16_hi(w[0].z);
+    s[6] = ss::bf16_lo(w[0].w); s[7] = ss::bf16_hi(w[0].w);
 #pragma unroll
     for (int r = 1; r < kMaxVec; ++r) {
         if (r < n) {
@@ -117,18 +108,25 @@ __device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, 
             s[7] = __fadd_rn(s[7], ss::bf16_hi(w[r].w));
         }
     }
-    for (int r = kMaxVec; NR == 0 && r < n; ++r) {  // ranks beyond the first 8
-        const uint4 x = (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
-                                          : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
-        s[0] = __fadd_rn(s[0], ss::bf16_lo(x.x));
-        s[1] = __fadd_rn(s[1], ss::bf16_hi(x.x));
-        s[2] = __fadd_rn(s[2], ss::bf16_lo(x.y));
-        s[3] = __fadd_rn(s[3], ss::bf16_hi(x.y));
-        s[4] = __fadd_rn(s[4], ss::bf16_lo(x.z));
-        s[5] = __fadd_rn(s[5], ss::bf16_hi(x.z));
-        s[6] = __fadd_rn(s[6], ss::bf16_lo(x.w));
-        s[7] = __fadd_rn(s[7], ss::bf16_hi(x.w));
-    }
+}
+
+__device__ __forceinline__ void add_rank(float (&s)[8], uint4 x) {
+    s[0] = __fadd_rn(s[0], ss::bf16_lo(x.x));
+    s[1] = __fadd_rn(s[1], ss::bf16_hi(x.x));
+    s[2] = __fadd_rn(s[2], ss::bf16_lo(x.y));
+    s[3] = __fadd_rn(s[3], ss::bf16_hi(x.y));
+    s[4] = __fadd_rn(s[4], ss::bf16_lo(x.z));
+    s[5] = __fadd_rn(s[5], ss::bf16_hi(x.z));
+    s[6] = __fadd_rn(s[6], ss::bf16_lo(x.w));
+    s[7] = __fadd_rn(s[7], ss::bf16_hi(x.w));
+}
+
+// The rank sum s of packed elements f..f+7 divided by n, AdamW on the state
+// loaded as t/m/v, state and shard stores (and the reduced gradient when
+// a.gout is set); returns the new bf16 parameter vector.
+__device__ __forceinline__ uint4 adam_vec(const StepArgs& a, int64_t f, const float (&s)[8], int n,
+                                          float4 t0, float4 t1, float4 m0, float4 m1, float4 v0,
+                                          float4 v1) {
     const float fN = (float)n;
     float g[8];
 #pragma unroll
@@ -154,6 +152,28 @@ __device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, 
     p.z = ss::pack_bf16x2(th[4], th[5]);
     p.w = ss::pack_bf16x2(th[6], th[7]);
     ss::st_stream_u4(a.shards + f, p);
+    return p;
+}
+
+template <int NR, bool UNPACKED, bool ANY = false, bool OUTS = true>
+__device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, int slot,
+                                          int64_t f, int64_t k) {
+    const int n = NR > 0 ? NR : a.N;
+    uint4 w[kMaxVec];
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r)
+        if (r < n)
+            w[r] = (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
+                                     : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
+    const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
+    const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+    const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+    float s[8];
+    sum_ranks<NR>(w, n, s);
+    for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
+        add_rank(s, (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
+                                      : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k)));
+    const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
     const int goff = UNPACKED ? n * a.w : 0;
     for (int j = 0; OUTS && j < a.n_out; ++j) {
         uint16_t* o = static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k;
@@ -161,6 +181,91 @@ __device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, 
             ss::st_any16(o, p);
         else
             ss::st_stream_u4(o, p);
+    }
+    return p;
+}
+
+// Fused copy-in at any gradient offset, N <= 8, one vector per thread q of
+// the CTA part; every lane of a warp holding a vector calls it.  Rank r's
+// gradient run starts sh_r bytes past a 16-byte boundary; block b of the run
+// is the 16 bytes at (run start - sh_r + 16b), and vector q is blocks q and
+// q + 1 joined by funnel shifts.  Thread q loads only block q of each rank
+// and takes block q + 1 from lane + 1 by a shuffle.  Lane 31 fetches its
+// successor blocks with cp.async into its own slots of shared memory -- no
+// registers, issued with the other loads -- and waits only for its own
+// copies, so warps stay independent.  A thread thus holds one 16-byte
+// register group per rank, as the aligned path does (two per rank before the
+// join would not fit all loads in flight).  Block q is loaded only for
+// q <= nvec and block q + 1 only for a vector q < nvec; each holds bytes of
+// the run, so no load leaves the run's 16-byte blocks.  Returns the new bf16
+// vector (valid threads).
+template <int NR>
+__device__ __forceinline__ uint4 step_vec_copyin_warp(const StepArgs& a, const PtrTab& tab,
+                                                      int slot, int64_t f0, int64_t k0, int q,
+                                                      int nvec) {
+    __shared__ uint4 s_next[kThreads / 32][kMaxVec];
+    const int n = NR > 0 ? NR : a.N;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool valid = q < nvec;
+    const int64_t f = f0 + 8 * (int64_t)q;
+    auto run_of = [&](int r) {
+        return reinterpret_cast<const unsigned char*>(
+            static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k0);
+    };
+    uint4 w[kMaxVec];
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r) {
+        if (r < n) {
+            const unsigned char* run = run_of(r);
+            const int sh = (int)(reinterpret_cast<uintptr_t>(run) & 15u);
+            w[r] = (sh ? q <= nvec : valid) ? ss::ld_stream_u4(run - sh + 16 * (int64_t)q)
+                                            : make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (lane == 31 && valid) {
+#pragma unroll
+        for (int r = 0; r < kMaxVec; ++r) {
+            if (r < n) {
+                const unsigned char* run = run_of(r);
+                const int sh = (int)(reinterpret_cast<uintptr_t>(run) & 15u);
+                if (sh) {
+                    const unsigned dst = (unsigned)__cvta_generic_to_shared(&s_next[warp][r]);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                                 "l"(run - sh + 16 * (int64_t)(q + 1))
+                                 : "memory");
+                }
+            }
+        }
+    }
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 t0 = z4, t1 = z4, m0 = z4, m1 = z4, v0 = z4, v1 = z4;
+    if (valid) {
+        t0 = ss::ld_rw_f4(a.master + f);
+        t1 = ss::ld_rw_f4(a.master + f + 4);
+        m0 = ss::ld_rw_f4(a.exp_avg + f);
+        m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+        v0 = ss::ld_rw_f4(a.exp_avg_sq + f);
+        v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+    }
+    if (lane == 31) asm volatile("cp.async.wait_all;" ::: "memory");
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r) {
+        if (r < n) {
+            uint4 nb;
+            nb.x = __shfl_down_sync(0xFFFFFFFFu, w[r].x, 1);
+            nb.y = __shfl_down_sync(0xFFFFFFFFu, w[r].y, 1);
+            nb.z = __shfl_down_sync(0xFFFFFFFFu, w[r].z, 1);
+            nb.w = __shfl_down_sync(0xFFFFFFFFu, w[r].w, 1);
+            const int sh = (int)(reinterpret_cast<uintptr_t>(run_of(r)) & 15u);
+            if (lane == 31 && sh && valid) nb = s_next[warp][r];
+            if (sh) w[r] = ss::realign16(w[r], nb, sh);
+        }
+    }
+    uint4 p = make_uint4(0, 0, 0, 0);
+    if (valid) {
+        float s[8];
+        sum_ranks<NR>(w, n, s);
+        p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
     }
     return p;
 }
@@ -303,7 +408,9 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
         const int q = threadIdx.x;
         if ((q & ~31) < nvec) {
             uint4 p = make_uint4(0, 0, 0, 0);
-            if (q < nvec)
+            if (UNPACKED && a.N <= kMaxVec)
+                p = step_vec_copyin_warp<NR>(a, tab, slot, fs + b0, ks + b0, q, (int)nvec);
+            else if (q < nvec)
                 p = step_vec<NR, UNPACKED, true, false>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
             store_outputs_realigned<UNPACKED>(a, tab, slot, ks + b0, q, (int)nvec, p);
         }
