@@ -213,11 +213,13 @@ __device__ __forceinline__ uint4 step_vec_copyin_warp(const StepArgs& a, const P
             static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k0);
     };
     uint4 w[kMaxVec];
+    uint32_t shs = 0;  // sh_r / 2 of every rank, 3 bits each
 #pragma unroll
     for (int r = 0; r < kMaxVec; ++r) {
         if (r < n) {
             const unsigned char* run = run_of(r);
             const int sh = (int)(reinterpret_cast<uintptr_t>(run) & 15u);
+            shs |= (uint32_t)(sh >> 1) << (3 * r);
             w[r] = (sh ? q <= nvec : valid) ? ss::ld_stream_u4(run - sh + 16 * (int64_t)q)
                                             : make_uint4(0, 0, 0, 0);
         }
@@ -226,9 +228,9 @@ __device__ __forceinline__ uint4 step_vec_copyin_warp(const StepArgs& a, const P
 #pragma unroll
         for (int r = 0; r < kMaxVec; ++r) {
             if (r < n) {
-                const unsigned char* run = run_of(r);
-                const int sh = (int)(reinterpret_cast<uintptr_t>(run) & 15u);
+                const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
                 if (sh) {
+                    const unsigned char* run = run_of(r);
                     const unsigned dst = (unsigned)__cvta_generic_to_shared(&s_next[warp][r]);
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
                                  "l"(run - sh + 16 * (int64_t)(q + 1))
@@ -256,7 +258,7 @@ __device__ __forceinline__ uint4 step_vec_copyin_warp(const StepArgs& a, const P
             nb.y = __shfl_down_sync(0xFFFFFFFFu, w[r].y, 1);
             nb.z = __shfl_down_sync(0xFFFFFFFFu, w[r].z, 1);
             nb.w = __shfl_down_sync(0xFFFFFFFFu, w[r].w, 1);
-            const int sh = (int)(reinterpret_cast<uintptr_t>(run_of(r)) & 15u);
+            const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
             if (lane == 31 && sh && valid) nb = s_next[warp][r];
             if (sh) w[r] = ss::realign16(w[r], nb, sh);
         }
