@@ -101,46 +101,24 @@ __device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
     const uintptr_t s = reinterpret_cast<uintptr_t>(src);
     bool vec = true;
     for (int j = 0; j < n_dst; ++j) vec &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ s) & 15u) == 0;
-    bool dst_congruent = true;
-    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
-    for (int j = 1; j < n_dst; ++j)
-        dst_congruent &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ d0) & 15u) == 0;
-    if (REALIGN && !vec && dst_congruent) {
-        // source and destinations differ mod 16 bytes: align the stores and
+    if (REALIGN && n_dst == 1 && !vec) {
+        // source and destination differ mod 16 bytes: align the stores and
         // rebuild each 16-byte source vector from the two aligned blocks that
         // cover it
-        int64_t head = (int64_t)(((16u - (d0 & 15u)) & 15u) / E);
+        unsigned char* d = dst[0];
+        int64_t head = (int64_t)(((16u - (reinterpret_cast<uintptr_t>(d) & 15u)) & 15u) / E);
         if (head > nelem) head = nelem;
-        if (tid < head) {
-            if (E == 2) {
-                uint16_t x = reinterpret_cast<const uint16_t*>(src)[tid];
-                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[tid] = x;
-            } else {
-                uint32_t x = reinterpret_cast<const uint32_t*>(src)[tid];
-                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[tid] = x;
-            }
-        }
         const int64_t nvec = (nelem - head) * E / 16;
-        const unsigned char* sv = src + head * E;
-        if (n_dst == 1) {
-            cta_realign_vectors(dst[0] + head * E, sv, nvec);
-        } else {
-            for (int64_t q = tid; q < nvec; q += nt) {
-                const uint4 x = ss::ld_any16(sv + 16 * q);
-                for (int j = 0; j < n_dst; ++j) ss::st_stream_u4(dst[j] + head * E + 16 * q, x);
-            }
-        }
         const int64_t done = head + nvec * 16 / E;
-        if (tid < nelem - done) {
-            const int64_t k = done + tid;
-            if (E == 2) {
-                uint16_t x = reinterpret_cast<const uint16_t*>(src)[k];
-                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[k] = x;
-            } else {
-                uint32_t x = reinterpret_cast<const uint32_t*>(src)[k];
-                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[k] = x;
-            }
+        // scalar head (before the vectors) and tail (after them)
+        const int64_t k = tid < head ? tid : done + (tid - head);
+        if (tid < head + (nelem - done)) {
+            if (E == 2)
+                reinterpret_cast<uint16_t*>(d)[k] = reinterpret_cast<const uint16_t*>(src)[k];
+            else
+                reinterpret_cast<uint32_t*>(d)[k] = reinterpret_cast<const uint32_t*>(src)[k];
         }
+        cta_realign_vectors(d + head * E, src + head * E, nvec);
         return;
     }
     if (!vec) {
