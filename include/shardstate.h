@@ -325,6 +325,11 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards,
  *     shards).
  * Pad elements are not read or written (they stay as fsdp_pack /
  * fsdp_init_master left them: zero).  bf16 plans only.
+ * Per-parameter gradients and outputs need only 2-byte alignment: a run at any
+ * offset still moves in 16-byte vectors, one side aligned and the other
+ * realigned in registers.  With n_out = N the call is the ZeRO-1/2 step
+ * ("Scaling data parallel", sections 9.1-9.2): each rank updates its own 1/N
+ * and the updated parameters reach every rank.
  */
 typedef struct {
     const void* const* rank_grads;        /* HOST [N] packed buffers (16-byte aligned), or NULL */
