@@ -962,6 +962,15 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
         ms, mn = _time_stream(lambda: st4.all_gather(), 20)
         _row(f"large awkward ({name}, N=7): all-gather + unpack", P4, "params/s", ms, mn, 4 * P4,
              peak)
+        # every rank's copy (n_out = N = 7 replicas, separately allocated)
+        outs7 = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(7)
+                 for n in ps4.numels()]
+        outs7_arr = ss.ptr_array(outs7)
+        ms, mn = _time_stream(
+            lambda: ss.fsdp_all_gather_unpack(st4.plan, st4.shards, outs7_arr, 7), 10)
+        _row(f"large awkward ({name}, N=7): all-gather + unpack, n_out=N=7", P4, "params/s", ms,
+             mn, (2 + 2 * 7) * P4, peak)
+        del outs7, outs7_arr
         ms, mn = _time_stream(lambda: st4.fused_step(), 20)
         _row(f"large awkward ({name}, N=7): one-pass step", P4, "params/s", ms, mn,
              (2 * 7 + 26) * tot4 + 2 * P4, peak)

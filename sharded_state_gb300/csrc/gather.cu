@@ -56,7 +56,10 @@ struct PtrTab {
 // that vector, so no load reaches past the 16-byte blocks the run touches.
 // The chunk loop is the same for every lane of a warp, so the shuffles see
 // the whole warp.
-__device__ __forceinline__ void cta_realign_vectors(unsigned char* dv, const unsigned char* sv,
+// The vectors go to every one of the n_dst destinations dv[j] + doff (all
+// 16-byte aligned there).
+__device__ __forceinline__ void cta_realign_vectors(unsigned char* const* dv, int n_dst,
+                                                    int64_t doff, const unsigned char* sv,
                                                     int64_t nvec) {
     const int lane = threadIdx.x & 31;
     const int64_t step = (int64_t)(blockDim.x >> 5) * 128;
@@ -83,42 +86,53 @@ __device__ __forceinline__ void cta_realign_vectors(unsigned char* dv, const uns
             nb.w = __shfl_sync(0xFFFFFFFFu, offer.w, (lane + 1) & 31);
             if (j == 3 && lane == 31) nb = nx;
             const int64_t q = c0 + 32 * j + lane;
-            if (q < nvec) ss::st_stream_u4(dv + 16 * q, ss::realign16(x[j], nb, sh));
+            if (q < nvec) {
+                const uint4 v = ss::realign16(x[j], nb, sh);
+                for (int d = 0; d < n_dst; ++d) ss::st_stream_u4(dv[d] + doff + 16 * q, v);
+            }
         }
     }
 }
 
 // Copy `nelem` elements of E bytes from src to the n_dst destinations; every
 // thread of the CTA takes part.  When all destinations are congruent to src
-// mod 16, the body moves in 128-bit vectors (4 per thread in flight); with a
-// single destination that is not, stores stay aligned and each source vector
-// is rebuilt from the two aligned blocks covering it (REALIGN; each block is
-// loaded once and passed to the neighbouring lane, cta_realign_vectors).
-template <int E, bool REALIGN = true>
+// mod 16, the body moves in 128-bit vectors (4 per thread in flight); when
+// they are congruent to one another but not to src, stores stay aligned and
+// each source vector is rebuilt from the two aligned blocks covering it (each
+// block loaded once and passed to the neighbouring lane, cta_realign_vectors).
+// Destinations at different offsets from one another are copied element by
+// element.
+template <int E>
 __device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
                                          const unsigned char* src, int64_t nelem) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const uintptr_t s = reinterpret_cast<uintptr_t>(src);
     bool vec = true;
     for (int j = 0; j < n_dst; ++j) vec &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ s) & 15u) == 0;
-    if (REALIGN && n_dst == 1 && !vec) {
-        // source and destination differ mod 16 bytes: align the stores and
-        // rebuild each 16-byte source vector from the two aligned blocks that
-        // cover it
-        unsigned char* d = dst[0];
-        int64_t head = (int64_t)(((16u - (reinterpret_cast<uintptr_t>(d) & 15u)) & 15u) / E);
+    bool dst_congruent = true;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
+    for (int j = 1; j < n_dst; ++j)
+        dst_congruent &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ d0) & 15u) == 0;
+    if (!vec && dst_congruent) {
+        // source and destinations differ mod 16 bytes (the destinations all
+        // alike): align the stores and rebuild each 16-byte source vector from
+        // the two aligned blocks that cover it
+        int64_t head = (int64_t)(((16u - (d0 & 15u)) & 15u) / E);
         if (head > nelem) head = nelem;
         const int64_t nvec = (nelem - head) * E / 16;
         const int64_t done = head + nvec * 16 / E;
         // scalar head (before the vectors) and tail (after them)
         const int64_t k = tid < head ? tid : done + (tid - head);
         if (tid < head + (nelem - done)) {
-            if (E == 2)
-                reinterpret_cast<uint16_t*>(d)[k] = reinterpret_cast<const uint16_t*>(src)[k];
-            else
-                reinterpret_cast<uint32_t*>(d)[k] = reinterpret_cast<const uint32_t*>(src)[k];
+            if (E == 2) {
+                const uint16_t x = reinterpret_cast<const uint16_t*>(src)[k];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint16_t*>(dst[j])[k] = x;
+            } else {
+                const uint32_t x = reinterpret_cast<const uint32_t*>(src)[k];
+                for (int j = 0; j < n_dst; ++j) reinterpret_cast<uint32_t*>(dst[j])[k] = x;
+            }
         }
-        cta_realign_vectors(d + head * E, src + head * E, nvec);
+        cta_realign_vectors(dst, n_dst, head * E, src + head * E, nvec);
         return;
     }
     if (!vec) {
@@ -210,13 +224,13 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
     const ss::Seg sg = segs[tl.seg];
     const int slot = sg.param - param_base;
     // The segment's tile starts are moved back by u elements, u = how far the
-    // stores' side (the packed buffer for DIR 1, the parameter otherwise; the
-    // source for DIR 2) sits past a 16-byte boundary at the segment's first
-    // element.  Every tile but the first then starts aligned and every tile
+    // stores' side (the packed buffer for DIR 1, the parameter otherwise --
+    // replica 0's for DIR 2) sits past a 16-byte boundary at the segment's
+    // first element.  Every tile but the first then starts aligned and every tile
     // but the last is whole vectors, so a misaligned segment pays for one head
     // and one tail, not one per tile.  The last tile runs to the segment end.
     const uintptr_t side =
-        DIR == 0 ? reinterpret_cast<uintptr_t>(tab.p[slot]) + (uintptr_t)(sg.param_off * E)
+        DIR != 1 ? reinterpret_cast<uintptr_t>(tab.p[slot]) + (uintptr_t)(sg.param_off * E)
                  : reinterpret_cast<uintptr_t>(packed) + (uintptr_t)(sg.packed_off * E);
     const int64_t u = (int64_t)((side & 15u) / E);
     const int64_t idx = tl.idx;
@@ -234,7 +248,7 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
             for (int j = 0; j < nd; ++j)
                 dsts[j] = static_cast<unsigned char*>(tab.p[(j0 + j) * ptr_stride + slot]) +
                           (sg.param_off + off) * E;
-            cta_copy<E, false>(dsts, nd, src, len);
+            cta_copy<E>(dsts, nd, src, len);
         }
     } else {
         unsigned char* dst = packed + (sg.packed_off + off) * E;
