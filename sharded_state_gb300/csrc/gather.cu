@@ -101,8 +101,9 @@ __device__ __forceinline__ void cta_realign_vectors(unsigned char* const* dv, in
 // each source vector is rebuilt from the two aligned blocks covering it (each
 // block loaded once and passed to the neighbouring lane, cta_realign_vectors).
 // Destinations at different offsets from one another are copied element by
-// element.
-template <int E>
+// element.  REALIGN false leaves the realigning path out (callers whose runs
+// are all congruent).
+template <int E, bool REALIGN = true>
 __device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
                                          const unsigned char* src, int64_t nelem) {
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -113,7 +114,7 @@ __device__ __forceinline__ void cta_copy(unsigned char* const* dst, int n_dst,
     const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst[0]);
     for (int j = 1; j < n_dst; ++j)
         dst_congruent &= ((reinterpret_cast<uintptr_t>(dst[j]) ^ d0) & 15u) == 0;
-    if (!vec && dst_congruent) {
+    if (REALIGN && !vec && dst_congruent) {
         // source and destinations differ mod 16 bytes (the destinations all
         // alike): align the stores and rebuild each 16-byte source vector from
         // the two aligned blocks that cover it
@@ -214,9 +215,10 @@ __device__ __forceinline__ void cta_zero(unsigned char* dst, int64_t nelem) {
 }
 
 // DIR 0: all-gather + unpack (packed -> params); DIR 1: pack (params -> packed).
-// DIR 2: all-gather + unpack with n_out > 1 replicas.
+// DIR 2: all-gather + unpack with n_out > 1 replicas; DIR 3: the same for a
+// plan and replicas all 16-byte aligned (no realigning code).
 template <int E, int CAP, int DIR>
-__global__ void __launch_bounds__(kThreads, DIR == 2 ? 2 : 5)
+__global__ void __launch_bounds__(kThreads, DIR >= 2 ? 2 : 5)
 tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
                  unsigned char* packed, PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out) {
     constexpr int64_t T = ss::kTileBytes / E;
@@ -239,7 +241,7 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
     if (DIR == 0) {
         unsigned char* dst = static_cast<unsigned char*>(tab.p[slot]) + (sg.param_off + off) * E;
         cta_copy<E>(&dst, 1, packed + (sg.packed_off + off) * E, len);
-    } else if (DIR == 2) {
+    } else if (DIR == 2 || DIR == 3) {
         unsigned char* dsts[8];
         const unsigned char* src = packed + (sg.packed_off + off) * E;
         // replicas in batches of up to 8 destinations per pass over the source
@@ -248,7 +250,7 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
             for (int j = 0; j < nd; ++j)
                 dsts[j] = static_cast<unsigned char*>(tab.p[(j0 + j) * ptr_stride + slot]) +
                           (sg.param_off + off) * E;
-            cta_copy<E>(dsts, nd, src, len);
+            cta_copy<E, DIR == 2>(dsts, nd, src, len);
         }
     } else {
         unsigned char* dst = packed + (sg.packed_off + off) * E;
@@ -336,7 +338,8 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
             tab.p[j * w + (i - a)] = ptrs[(size_t)j * p->n + i];
             ptrs_aligned &= p->numel[i] == 0 || ss::aligned(tab.p[j * w + (i - a)], 16);
         }
-    if (p->vec_aligned && ptrs_aligned && n_out == 1) {
+    const bool all_aligned = p->vec_aligned && ptrs_aligned;
+    if (all_aligned && n_out == 1) {
         return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
             if (p->eb == 2) {
                 if (dir == 0)
@@ -357,7 +360,10 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
     }
     return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
         if (p->eb == 2) {
-            if (dir == 0 && n_out > 1)
+            if (dir == 0 && n_out > 1 && all_aligned)
+                tile_copy_kernel<2, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, n_out);
+            else if (dir == 0 && n_out > 1)
                 tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
                                                                        tab, a, w, n_out);
             else if (dir == 0)
@@ -367,7 +373,10 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
                 tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
                                                                        tab, a, w, 1);
         } else {
-            if (dir == 0 && n_out > 1)
+            if (dir == 0 && n_out > 1 && all_aligned)
+                tile_copy_kernel<4, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
+                                                                       tab, a, w, n_out);
+            else if (dir == 0 && n_out > 1)
                 tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
                                                                        tab, a, w, n_out);
             else if (dir == 0)
