@@ -30,16 +30,22 @@ namespace {
 constexpr int kThreads = 256;
 
 // Sum one 8-element vector over ranks (rank order, fp32), divide by N, round.
-template <int NR>
+// ANY: the inputs at k need only 2-byte alignment (read as the two aligned
+// 16-byte blocks that cover them, joined in registers).
+template <int NR, bool ANY = false>
 __device__ __forceinline__ uint4 mean8(const void* const* in, int N, int64_t k) {
     const int n = NR > 0 ? NR : N;
-    uint4 w0 = ss::ld_stream_u4(static_cast<const uint16_t*>(in[0]) + k);
+    auto ld = [&](int r) {
+        const uint16_t* p = static_cast<const uint16_t*>(in[r]) + k;
+        return ANY ? ss::ld_any16(p) : ss::ld_stream_u4(p);
+    };
+    uint4 w0 = ld(0);
     float s[8] = {ss::bf16_lo(w0.x), ss::bf16_hi(w0.x), ss::bf16_lo(w0.y), ss::bf16_hi(w0.y),
                   ss::bf16_lo(w0.z), ss::bf16_hi(w0.z), ss::bf16_lo(w0.w), ss::bf16_hi(w0.w)};
     if (NR > 0) {
         uint4 w[NR > 1 ? NR - 1 : 1];
 #pragma unroll
-        for (int r = 1; r < NR; ++r) w[r - 1] = ss::ld_stream_u4(static_cast<const uint16_t*>(in[r]) + k);
+        for (int r = 1; r < NR; ++r) w[r - 1] = ld(r);
 #pragma unroll
         for (int r = 1; r < NR; ++r) {
             s[0] = __fadd_rn(s[0], ss::bf16_lo(w[r - 1].x));
@@ -53,7 +59,7 @@ __device__ __forceinline__ uint4 mean8(const void* const* in, int N, int64_t k) 
         }
     } else {
         for (int r = 1; r < n; ++r) {
-            uint4 w = ss::ld_stream_u4(static_cast<const uint16_t*>(in[r]) + k);
+            uint4 w = ld(r);
             s[0] = __fadd_rn(s[0], ss::bf16_lo(w.x));
             s[1] = __fadd_rn(s[1], ss::bf16_hi(w.x));
             s[2] = __fadd_rn(s[2], ss::bf16_lo(w.y));
@@ -81,16 +87,20 @@ __device__ __forceinline__ uint16_t mean1(const void* const* in, int N, int64_t 
 
 // Average one tensor piece [k0, k1) of the tensor whose N inputs and one
 // output are ptrs[0..N] (CTA-cooperative).
-template <int NR>
+// ANY false: inputs not congruent to the output go element by element (the
+// host picks ANY for the buckets that hold such a tensor).
+template <int NR, bool ANY>
 __device__ __forceinline__ void avg_piece(const void* const* ptrs, int N, int64_t k0, int64_t k1) {
     const int tid = threadIdx.x, nt = blockDim.x;
     uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(ptrs[N]));
-    // vector path needs every pointer congruent to the output mod 16 bytes
+    // The output's stores are aligned after a scalar head.  Inputs congruent
+    // to the output load as plain vectors; otherwise every input vector is
+    // rebuilt from the two aligned blocks that cover it.
     const uintptr_t ref = reinterpret_cast<uintptr_t>(out + k0) & 15u;
     bool vec = true;
     for (int r = 0; r < N; ++r)
         vec &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(ptrs[r]) + k0) & 15u) == ref);
-    if (!vec) {
+    if (!ANY && !vec) {
         for (int64_t k = k0 + tid; k < k1; k += nt) out[k] = mean1(ptrs, N, k);
         return;
     }
@@ -99,9 +109,16 @@ __device__ __forceinline__ void avg_piece(const void* const* ptrs, int N, int64_
     if (tid < head) out[k0 + tid] = mean1(ptrs, N, k0 + tid);
     const int64_t vb = k0 + head;
     const int64_t nvec = (k1 - vb) / 8;
-    for (int64_t q = tid; q < nvec; q += nt) {
-        const int64_t k = vb + 8 * q;
-        ss::st_stream_u4(out + k, mean8<NR>(ptrs, N, k));
+    if (!ANY || vec) {
+        for (int64_t q = tid; q < nvec; q += nt) {
+            const int64_t k = vb + 8 * q;
+            ss::st_stream_u4(out + k, mean8<NR>(ptrs, N, k));
+        }
+    } else {
+        for (int64_t q = tid; q < nvec; q += nt) {
+            const int64_t k = vb + 8 * q;
+            ss::st_stream_u4(out + k, mean8<NR, ANY>(ptrs, N, k));
+        }
     }
     const int64_t done = vb + 8 * nvec;
     if (tid < k1 - done) out[done + tid] = mean1(ptrs, N, done + tid);
@@ -131,7 +148,7 @@ __device__ __forceinline__ int warp_find(const int64_t* __restrict__ prefix, int
 // elements [b*T, (b+1)*T) (T = kTile), walking the tensors that cover them.
 constexpr int64_t kTile = 4096;
 
-template <int NR>
+template <int NR, bool ANY>
 __global__ void __launch_bounds__(kThreads)
 ddp_bucket_kernel(const int64_t* __restrict__ prefix, const void* const* __restrict__ ptrs, int N,
                   int o_lo, int o_hi) {
@@ -148,7 +165,7 @@ ddp_bucket_kernel(const int64_t* __restrict__ prefix, const void* const* __restr
         const int64_t t_end = prefix[o + 1];
         const int64_t piece_end = t_end < u_end ? t_end : u_end;
         if (piece_end > u)
-            avg_piece<NR>(ptrs + (size_t)o * (N + 1), N, u - prefix[o], piece_end - prefix[o]);
+            avg_piece<NR, ANY>(ptrs + (size_t)o * (N + 1), N, u - prefix[o], piece_end - prefix[o]);
         u = piece_end > u ? piece_end : u;
         ++o;
     }
@@ -173,18 +190,32 @@ cudaError_t launch_bucket(DdpKernel fn, unsigned grid, cudaStream_t st, const in
     return cudaLaunchKernelEx(&cfg, fn, prefix, ptrs, N, o_lo, o_hi);
 }
 
-DdpKernel pick(int N) {
+template <bool ANY>
+DdpKernel pick_n(int N) {
     switch (N) {
-        case 1: return ddp_bucket_kernel<1>;
-        case 2: return ddp_bucket_kernel<2>;
-        case 3: return ddp_bucket_kernel<3>;
-        case 4: return ddp_bucket_kernel<4>;
-        case 5: return ddp_bucket_kernel<5>;
-        case 6: return ddp_bucket_kernel<6>;
-        case 7: return ddp_bucket_kernel<7>;
-        case 8: return ddp_bucket_kernel<8>;
-        default: return ddp_bucket_kernel<0>;
+        case 1: return ddp_bucket_kernel<1, ANY>;
+        case 2: return ddp_bucket_kernel<2, ANY>;
+        case 3: return ddp_bucket_kernel<3, ANY>;
+        case 4: return ddp_bucket_kernel<4, ANY>;
+        case 5: return ddp_bucket_kernel<5, ANY>;
+        case 6: return ddp_bucket_kernel<6, ANY>;
+        case 7: return ddp_bucket_kernel<7, ANY>;
+        case 8: return ddp_bucket_kernel<8, ANY>;
+        default: return ddp_bucket_kernel<0, ANY>;
     }
+}
+
+// any: the bucket holds a tensor whose inputs are not all congruent to its
+// output mod 16 bytes (they are then read through realigning loads).
+DdpKernel pick(int N, bool any) { return any ? pick_n<true>(N) : pick_n<false>(N); }
+
+// Whether tensor o of a bucket-ordered pointer table needs realigning loads.
+bool needs_realign(const void* const* ptrs, int N, int o) {
+    const void* const* p = ptrs + (size_t)o * (N + 1);
+    const uintptr_t out = reinterpret_cast<uintptr_t>(p[N]);
+    for (int r = 0; r < N; ++r)
+        if ((reinterpret_cast<uintptr_t>(p[r]) ^ out) & 15u) return true;
+    return false;
 }
 
 }  // namespace
@@ -259,11 +290,13 @@ int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* nume
     const int64_t* d_prefix = static_cast<const int64_t*>(d_table);
     const void* const* d_ptrs =
         reinterpret_cast<const void* const*>(static_cast<unsigned char*>(d_table) + n_prefix * 8);
-    DdpKernel fn = pick(N);
     for (int b = 0; rc == SS_OK && b < nb; ++b) {
         const int o_lo = bucket_start[b], o_hi = bucket_start[b + 1];
         const int64_t elems = prefix[o_hi] - prefix[o_lo];
         if (elems == 0) continue;
+        bool any = false;
+        for (int o = o_lo; o < o_hi && !any; ++o) any = numels[T - 1 - o] > 0 && needs_realign(ptrs, N, o);
+        const DdpKernel fn = pick(N, any);
         const int64_t grid = (elems + kTile - 1) / kTile;
         if (grid > 0x7FFFFFFF) {
             rc = SS_EOVERFLOW;
@@ -369,11 +402,13 @@ extern "C" int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors,
     const int64_t* d_prefix = static_cast<const int64_t*>(d_table);
     const void* const* d_ptrs =
         reinterpret_cast<const void* const*>(static_cast<unsigned char*>(d_table) + n_prefix * 8);
-    DdpKernel fn = pick(N);
     for (int b = 0; b < nb; ++b) {
         const int o_lo = bucket_start[b], o_hi = bucket_start[b + 1];
         const int64_t elems = prefix[o_hi] - prefix[o_lo];
         if (elems == 0) continue;
+        bool any = false;
+        for (int o = o_lo; o < o_hi && !any; ++o) any = numels[T - 1 - o] > 0 && needs_realign(ptrs, N, o);
+        const DdpKernel fn = pick(N, any);
         const int64_t grid = (elems + kTile - 1) / kTile;
         if (grid > 0x7FFFFFFF) return SS_EOVERFLOW;
         cudaError_t le = launch_bucket(fn, (unsigned)grid, st, d_prefix, d_ptrs, N, o_lo, o_hi);
