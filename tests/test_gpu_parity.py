@@ -367,6 +367,31 @@ def test_ddp_misaligned_and_odd_sizes(ss):
         np.testing.assert_array_equal(to_np(o), w)
 
 
+def test_ddp_mixed_buckets_realigned_and_congruent(ss):
+    """N = 8, tensors spanning many 4096-element tiles; every third tensor has
+    each rank's gradient at its own offset (0..7 elements) from its output, the
+    rest are congruent, and the 256 KiB cap puts both kinds in the same and in
+    different buckets.  Bit-exact against the oracle."""
+    N = 8
+    numels = [70_001, 4096, 129, 33_333, 100_000, 8, 65_536, 12_345, 90_000, 1]
+    g = torch.Generator(device="cuda").manual_seed(7)
+    grads, outs = [], []
+    for r in range(N):
+        row = []
+        for t, n in enumerate(numels):
+            sh = (r + 3 * t) % 8 if t % 3 == 0 else 0
+            base = (torch.randn(n + 8, generator=g, device="cuda") * 1e-3).to(torch.bfloat16)
+            row.append(base[sh:sh + n])
+        grads.append(row)
+    outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for n in numels]
+    nb = ss.ddp_bucket_pack_average(grads, 256 * 1024, outs, numels=numels)
+    torch.cuda.synchronize()
+    assert nb > 1
+    want = oracle.ddp_average([[to_np(x) for x in rank] for rank in grads])
+    for o, w in zip(outs, want):
+        np.testing.assert_array_equal(to_np(o), w)
+
+
 # ---------------------------------------------------------------------------
 # errors come back as status codes, nothing launched
 # ---------------------------------------------------------------------------
