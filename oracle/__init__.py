@@ -31,26 +31,38 @@ PER_PARAM_DIM0 = 2
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    """Compile the C oracle (gcc, -O2, no FMA contraction, OpenMP if present)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
-        return _LIB
+def compile_library(src: str, out: str) -> str:
+    """gcc, -O2, no FMA contraction, OpenMP if present: src (C) -> shared library out."""
     base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-            "-shared", _SRC, "-o", _LIB + ".tmp", "-lm"]
+            "-shared", src, "-o", out + ".tmp", "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True)
-    os.replace(_LIB + ".tmp", _LIB)
-    return _LIB
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    return compile_library(_SRC, _LIB)
+
+
+# SSO_ORACLE_LIB names another build of ss_oracle.c to load instead; the
+# mutation tests use it to run the pins against oracles with planted mistakes.
+ORACLE_LIB_ENV = "SSO_ORACLE_LIB"
 
 
 def _load():
     global _lib
     if _lib is not None:
         return _lib
-    build()
-    lib = ctypes.CDLL(_LIB)
+    path = os.environ.get(ORACLE_LIB_ENV)
+    if not path:
+        path = build()
+    lib = ctypes.CDLL(path)
     i64p = ctypes.POINTER(ctypes.c_int64)
     vp = ctypes.c_void_p
     lib.sso_layout.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, i64p, i64p,
