@@ -21,12 +21,17 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(ROOT, "oracle", "ss_oracle.c")
 
-# (name, exact text in ss_oracle.c, replacement)
+# (name, exact text in ss_oracle.c, replacement).  Only mutants that change
+# some result are listed: reordering the reduce-scatter's loop over shards,
+# for one, computes every output from the same inputs and is no mistake.
 MUTANTS = [
     # bf16 rounding
     ("bf16 ties away from zero",
      "    if (dropped > half || (dropped == half && (upper & 1u))) {",
      "    if (dropped >= half) {"),
+    ("bf16 NaN keeps only its upper half (low-payload NaNs become infinities)",
+     "        return (uint16_t)((u >> 16) | 0x0040u);",
+     "        return (uint16_t)(u >> 16);"),
     # layout
     ("FLAT_ORIG_TRUE alignment of 8 elements whatever the dtype",
      "        int64_t a = 16 / elem_bytes;",
@@ -41,6 +46,9 @@ MUTANTS = [
     ("PER_PARAM pack writes a rank's chunk column-major",
      "                        int64_t dst = (int64_t)r * c + off[i] + (row - lo) * in + col;",
      "                        int64_t dst = (int64_t)r * c + off[i] + col * rows[i] + (row - lo);"),
+    ("PER_PARAM pack drops the final row of a short last chunk",
+     "                if (hi > dim0[i]) hi = dim0[i];",
+     "                if (hi > dim0[i]) hi = dim0[i] - 1;"),
     ("FLAT unpack reads rank-interleaved instead of rank-major",
      "                src_index = owner * c + local;",
      "                src_index = local * N + owner;"),
@@ -74,6 +82,9 @@ MUTANTS = [
     ("AdamW second moment of |g| instead of g^2",
      "        v = beta2 * v + (1.0 - beta2) * g * g;",
      "        v = beta2 * v + (1.0 - beta2) * fabs(g);"),
+    ("AdamW first-moment bias correction one step ahead",
+     "    const double bc1 = 1.0 - pow(beta1, (double)step);",
+     "    const double bc1 = 1.0 - pow(beta1, (double)(step + 1));"),
     ("AdamW without the first-moment bias correction",
      "        double mhat = m / bc1;",
      "        double mhat = m;"),
@@ -91,9 +102,17 @@ MUTANTS = [
     ("DDP bucket closes only above the cap",
      "        if (fill >= cap_bytes) {",
      "        if (fill > cap_bytes) {"),
+    ("DDP bucket count includes an empty trailing bucket",
+     "    return fill > 0 ? bucket + 1 : bucket;",
+     "    return bucket + 1;"),
     ("DDP buckets filled in registration order",
      "    for (int t = T - 1; t >= 0; --t) {",
      "    for (int t = 0; t < T; ++t) {"),
+    ("DDP average sums ranks in reverse order",
+     "            float acc = bf16_to_f32(grads[t][k]);\n"
+     "            for (int r = 1; r < N; ++r) acc = acc + bf16_to_f32(grads[(size_t)r * (size_t)T + (size_t)t][k]);",
+     "            float acc = bf16_to_f32(grads[(size_t)(N - 1) * (size_t)T + (size_t)t][k]);\n"
+     "            for (int r = N - 2; r >= 0; --r) acc = acc + bf16_to_f32(grads[(size_t)r * (size_t)T + (size_t)t][k]);"),
     ("DDP average returns the sum over ranks",
      "            out[t][k] = f32_to_bf16_rne(acc / divisor);",
      "            out[t][k] = f32_to_bf16_rne(acc);"),

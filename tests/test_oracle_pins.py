@@ -454,6 +454,23 @@ def test_ddp_bucket_counts_small_cases():
     assert b == [1, 1, 0] and n == 2
 
 
+def test_ddp_average_fixed_rank_order_decides_the_bf16():
+    # N = 4, ranks 4, 2^-6, 2^-22, 2^-22 (all exact in bf16).  In rank order the
+    # two 2^-22 each meet 4 + 2^-6 at half an fp32 ulp and vanish (ties to even),
+    # so the mean is 1 + 2^-8: exactly between the bf16 values 1 and 1 + 2^-7,
+    # which rounds to the even one, 1.0 (0x3F80).  Had the small values been
+    # added first (reverse order) the mean would be 1 + 2^-8 + 2^-23 and round
+    # up to 0x3F81.  The second element holds the ranks reversed, where rank
+    # order itself gives the larger sum.
+    def b16(x):
+        return np.array([np.float32(x)]).view(np.uint32)[0] >> 16
+    col0 = [4.0, 2.0 ** -6, 2.0 ** -22, 2.0 ** -22]
+    ranks = [[np.array([b16(col0[r]), b16(col0[3 - r])], dtype=np.uint16)] for r in range(4)]
+    out = oracle.ddp_average(ranks)[0]
+    assert out[0] == 0x3F80
+    assert out[1] == 0x3F81
+
+
 def test_ddp_average_is_rs_mean_rounded():
     rng = np.random.default_rng(12)
     N, T = 8, 5
