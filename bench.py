@@ -611,10 +611,24 @@ def cpu_baseline(st: Step, ps: W.ParamSet, args) -> dict:
         if time.perf_counter() - t0 >= args.cpu_seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": params / dt, "unit": "params/s", "cores": used, "kind": "oracle",
-            "sample": f"block group 0 ({params // reps:,} params, N={ps.world_size}) of the same "
-                      f"workload, {reps} oracle RS+AdamW+AG steps, inputs copied from the device "
-                      f"buffers, {dt:.1f} s"}
+    out = {"value": params / dt, "unit": "params/s", "cores": used, "kind": "oracle",
+           "sample": f"block group 0 ({params // reps:,} params, N={ps.world_size}) of the same "
+                     f"workload, {reps} oracle RS+AdamW+AG steps, inputs copied from the device "
+                     f"buffers, {dt:.1f} s"}
+    # the definitional oracle on one thread, on the same sample (half the budget)
+    oracle.set_threads(1)
+    t0 = time.perf_counter()
+    reps1, params1 = 0, 0
+    while True:
+        params1 += _oracle_step(ps, smp, 5000 + reps1)
+        reps1 += 1
+        if time.perf_counter() - t0 >= args.cpu_seconds / 2:
+            break
+    dt1 = time.perf_counter() - t0
+    oracle.set_threads(cores)
+    out["single_thread"] = {"value": params1 / dt1, "unit": "params/s", "cores": 1,
+                            "sample": f"the same sample, {reps1} steps, {dt1:.1f} s"}
+    return out
 
 
 def run_reference(args, world, rank):
