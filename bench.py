@@ -668,6 +668,10 @@ def run_reference(args, world, rank):
 # per-row measurements (--mode rows): every hot-path row on its own workload
 # ---------------------------------------------------------------------------
 
+# per-iteration times of the latest _time_stream call (its row reports their median)
+_LAST_TIMES: list = []
+
+
 def _time_stream(fn, K: int, warmup: int = 3):
     """Mean / min CUDA-event time (ms) of fn() on the current stream."""
     for _ in range(warmup):
@@ -684,6 +688,7 @@ def _time_stream(fn, K: int, warmup: int = 3):
         ts.append((a, b))
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ts]
+    _LAST_TIMES[:] = ms
     return sum(ms) / len(ms), min(ms)
 
 
@@ -701,6 +706,7 @@ def _time_cpu(fn, seconds: float):
 def _row(name, unit_count, unit, ms, ms_min, nbytes, peak, cpu=None, extra=None):
     gbs = nbytes / (ms / 1e3) / 1e9
     d = {"row": name, "value": unit_count / (ms / 1e3), "unit": unit, "ms": ms, "ms_min": ms_min,
+         "ms_median": statistics.median(_LAST_TIMES) if _LAST_TIMES else None,
          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                       "frac": gbs / peak, "algorithmic_bytes": nbytes}}
     if cpu is not None:
