@@ -95,6 +95,7 @@ static uint16_t f32_to_bf16_rne(float f) {
 }
 
 void sso_bf16_round(int64_t count, const float* in, uint16_t* out) {
+#pragma omp parallel for num_threads(g_threads) schedule(static)
     for (int64_t k = 0; k < count; ++k) out[k] = f32_to_bf16_rne(in[k]);
 }
 
