@@ -79,15 +79,6 @@ __device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const Ptr
     return static_cast<const uint16_t*>(a.packed_grads.p[r]) + f;
 }
 
-// NR > 0: exactly NR ranks, fully unrolled; NR == 0: any N, the first 8 ranks'
-// loads predicated and kept in flight together, the rest one by one.
-// f is 8-aligned (packed side); ANY: the per-parameter side (gradients read
-// at k, outputs written at k) may be misaligned and is read / written through
-// ld_any16 / st_any16.
-// The reduced-gradient output (a.gout) and the n_out per-parameter outputs
-// are runtime options: one pointer test and a loop of n_out stores.
-// OUTS false: the n_out outputs are left to the caller (the returned vector is
-// the new bf16 parameter vector).
 // Rank-order fp32 sum of the first min(n, 8) ranks' vectors, from rank 0's value.
 template <int NR>
 __device__ __forceinline__ void sum_ranks(const uint4 (&w)[kMaxVec], int n, float (&s)[8]) {
@@ -155,6 +146,15 @@ __device__ __forceinline__ uint4 adam_vec(const StepArgs& a, int64_t f, const fl
     return p;
 }
 
+// NR > 0: exactly NR ranks, fully unrolled; NR == 0: any N, the first 8 ranks'
+// loads predicated and kept in flight together, the rest one by one.
+// f is 8-aligned (packed side); ANY: the per-parameter side (gradients read
+// at k, outputs written at k) may be misaligned and is read / written through
+// ld_any16 / st_any16.
+// The reduced-gradient output (a.gout) and the n_out per-parameter outputs
+// are runtime options: one pointer test and a loop of n_out stores.
+// OUTS false: the n_out outputs are left to the caller (the returned vector is
+// the new bf16 parameter vector).
 template <int NR, bool UNPACKED, bool ANY = false, bool OUTS = true>
 __device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, int slot,
                                           int64_t f, int64_t k) {
