@@ -424,8 +424,9 @@ def run_native(args, world, rank, local, dist):
                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                         if peak_kind == "measured" else "fallback 6.8 TB/s",
                         "unit": "GB/s", "frac": rs_gbs / peak,
-                        "traffic": None if fused or N != 8 else
-                        ncu_traffic("rs_adamw_bf16_kernel<8,1,0,1,0>", total),
+                        "traffic": None if N != 8 or (fused and args.n_out != 1) else
+                        ncu_traffic("fused_step_kernel<8,0,0>" if fused
+                                    else "rs_adamw_bf16_kernel<8,1,0,1,0>", total),
                         "traffic_source": "ncu capture per element x elements per launch "
                                           "(profiles/ncu_traffic.json)",
                         "per_unit_bytes": 2 * N + 26 + (2 * args.n_out if fused else 0),
