@@ -61,9 +61,9 @@ def parse_args():
     ap.add_argument("--rows", default="all",
                     help="rows mode: comma list of llama,block4096,tiny,awkward,awkward_large,ddp "
                          "(default all; awkward_large: only the large awkward sets)")
-    ap.add_argument("--step-kind", default="two_calls", choices=["two_calls", "fused"],
-                    help="timed step: RS+AdamW then all-gather (two calls), or the one-pass "
-                         "fsdp_sharded_step")
+    ap.add_argument("--step-kind", default="fused", choices=["two_calls", "fused"],
+                    help="timed step: the one-pass fsdp_sharded_step (default), or RS+AdamW "
+                         "then all-gather as two calls")
     ap.add_argument("--ddp-large", type=int, default=600,
                     help="rows mode: number of 4M-element DDP tensors (600 = the full list)")
     ap.add_argument("--awkward-scale", type=float, default=1.0,
@@ -312,19 +312,19 @@ class Step:
         self.ss.fsdp_reduce_scatter_adamw(self.plan, self._grads_arr, self.master, self.m, self.v,
                                           self.shards, hp, None, group, stream)
 
-    def fused_step(self, stream=None, param_grads=None):
-        """fsdp_sharded_step: RS+AdamW with the all-gather written in the same pass."""
-        self.t += 1
-        hp = self.ss.adamw_params(step=self.t, **{k: v for k, v in W.adamw_hparams().items()
-                                                   if k != "step"})
+    def fused_step(self, stream=None, param_grads=None, group=-1, hp=None):
+        """fsdp_sharded_step: RS+AdamW with the all-gather written in the same pass
+        (every group, or one group with the step's shared hyper-parameters)."""
+        if hp is None:
+            hp = self.next_hp()
         if param_grads is None:
             self.ss.fsdp_sharded_step(self.plan, self.master, self.m, self.v, self.shards, hp,
                                       rank_grads=self._grads_arr, params_out=self._outs_arr,
-                                      n_out=self.n_out, stream=stream)
+                                      n_out=self.n_out, group=group, stream=stream)
         else:
             self.ss.fsdp_sharded_step(self.plan, self.master, self.m, self.v, self.shards, hp,
                                       rank_param_grads=param_grads, params_out=self._outs_arr,
-                                      n_out=self.n_out, stream=stream)
+                                      n_out=self.n_out, group=group, stream=stream)
 
     def all_gather(self, stream=None, group=-1):
         self.ss.fsdp_all_gather_unpack(self.plan, self.shards, self._outs_arr, self.n_out, group,
@@ -415,17 +415,21 @@ def run_native(args, world, rank, local, dist):
                                             step_kind=args.step_kind),
            "hbm_gbs": hbm, "bytes_per_step": by["step"],
            "frac_of_measured_peak": hbm / peak, "frac_of_nominal_8tbs": hbm / NOMINAL_HBM_GBS,
-           "kernels": {"rs_adamw": {"ms": rs_avg, "ms_min": min(rs_ms), "gbs": rs_gbs,
-                                    "bytes": by["rs_adamw"]},
-                       "all_gather_unpack": {"ms": ag_avg, "ms_min": min(ag_ms), "gbs": ag_gbs,
-                                             "bytes": by["all_gather"]}},
-           "roofline": {"bound": "hbm", "kernel": "fused_step" if fused else "rs_adamw",
+           "kernels": ({"one_pass_step": {"ms": rs_avg, "ms_min": min(rs_ms), "gbs": rs_gbs,
+                                          "bytes": by["rs_adamw"]}} if fused else
+                       {"rs_adamw": {"ms": rs_avg, "ms_min": min(rs_ms), "gbs": rs_gbs,
+                                     "bytes": by["rs_adamw"]},
+                        "all_gather_unpack": {"ms": ag_avg, "ms_min": min(ag_ms), "gbs": ag_gbs,
+                                              "bytes": by["all_gather"]}}),
+           "roofline": {"bound": "hbm",
+                        "kernel": ("fused_step_flat_kernel (one-pass RS+AdamW+AG)" if fused
+                                   else "rs_adamw_bf16_kernel"),
                         "achieved": rs_gbs, "peak": peak,
                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                         if peak_kind == "measured" else "fallback 6.8 TB/s",
                         "unit": "GB/s", "frac": rs_gbs / peak,
                         "traffic": None if N != 8 or (fused and args.n_out != 1) else
-                        ncu_traffic("fused_step_kernel<8,0,0>" if fused
+                        ncu_traffic("fused_step_flat_kernel<8>" if fused
                                     else "rs_adamw_bf16_kernel<8,1,0,1,0>", total),
                         "traffic_source": "ncu capture per element x elements per launch "
                                           "(profiles/ncu_traffic.json)",
@@ -515,8 +519,11 @@ def run_e2e(st: Step, args, stream, dist) -> dict:
                 ev_in[g].record(h2d)
         for g in order:
             stream.wait_event(ev_in[g])
-            st.rs_adamw(sp, group=g, hp=hp)
-            st.all_gather(sp, group=g)
+            if args.step_kind == "fused":
+                st.fused_step(sp, group=g, hp=hp)
+            else:
+                st.rs_adamw(sp, group=g, hp=hp)
+                st.all_gather(sp, group=g)
             ev_done[g].record(stream)
             d2h.wait_event(ev_done[g])
             lo, hi = out_rng[g]

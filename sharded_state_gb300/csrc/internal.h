@@ -39,6 +39,21 @@ struct Tile {
 };
 static_assert(sizeof(Tile) == 8, "Tile layout");
 
+// Block of packed elements indexed by the plan's packed segment map
+// (ss_plan::pm_block); one flat CTA of 256 threads x 8 elements.
+constexpr int64_t kMapBlock = 2048;
+
+// One data segment of the packed segment map: everything a kernel needs to
+// place packed elements [packed_off, packed_off + len) in their parameter.
+struct PmEntry {
+    int64_t packed_off;
+    int64_t param_off;
+    int64_t len;
+    int32_t param;
+    int32_t reserved;
+};
+static_assert(sizeof(PmEntry) == 32, "PmEntry layout");
+
 }  // namespace ss
 
 struct ss_plan {
@@ -72,6 +87,15 @@ struct ss_plan {
     ss::Tile* d_data_tiles = nullptr;
     ss::Tile* d_zero_tiles = nullptr;
     ss::Tile* d_packed_tiles = nullptr;
+    // The data segments in packed-offset order (pm[m], m = 0..M-1).
+    // pm_block[B] is the last m whose packed offset is <= B * kMapBlock (0 if
+    // none), for every block B in [0, total / kMapBlock + 1]: the segment
+    // holding packed element f is among pm_block[f / kMapBlock] ..
+    // pm_block[f / kMapBlock + 1].
+    std::vector<ss::PmEntry> pm;
+    std::vector<int> pm_block;
+    ss::PmEntry* d_pm = nullptr;
+    int* d_pm_block = nullptr;
     // every data segment's packed offset, parameter offset and length are
     // multiples of 16 bytes (enables the copy kernels' fast path)
     bool vec_aligned = false;

@@ -24,6 +24,7 @@
 #include <atomic>
 #include <cstring>
 #include <new>
+#include <tuple>
 
 #include "internal.h"
 
@@ -179,6 +180,31 @@ void build_packed_tiles(ss_plan* p) {
     while (g < p->G) p->group_ptile[++g] = (int64_t)p->packed_tiles.size();
 }
 
+// The packed segment map: data segments by packed offset, and for every
+// kMapBlock-element block the last segment starting at or before it.
+void build_packed_map(ss_plan* p) {
+    std::vector<int> order;
+    order.reserve(p->data.size());
+    for (size_t k = 0; k < p->data.size(); ++k)
+        if (p->data[k].len > 0) order.push_back((int)k);
+    std::sort(order.begin(), order.end(),
+              [&](int a, int b) { return p->data[a].packed_off < p->data[b].packed_off; });
+    p->pm.resize(order.size());
+    for (size_t m = 0; m < order.size(); ++m) {
+        const ss::Seg& sg = p->data[order[m]];
+        p->pm[m] = ss::PmEntry{sg.packed_off, sg.param_off, sg.len, sg.param, 0};
+    }
+    const int64_t nb = p->total / ss::kMapBlock + 2;
+    p->pm_block.assign((size_t)nb, 0);
+    const int M = (int)order.size();
+    int m = 0;
+    for (int64_t B = 0; B < nb; ++B) {
+        const int64_t pos = B * ss::kMapBlock;
+        while (m + 1 < M && p->pm[m + 1].packed_off <= pos) ++m;
+        p->pm_block[(size_t)B] = m;
+    }
+}
+
 int upload(ss_plan* p) {
     cudaError_t e = cudaGetDevice(&p->device);
     if (e != cudaSuccess) return ss::cuda_fail(e);
@@ -217,6 +243,20 @@ int upload(ss_plan* p) {
     if (!p->packed_tiles.empty()) {
         e = cudaMemcpy(p->d_packed_tiles, p->packed_tiles.data(),
                        p->packed_tiles.size() * sizeof(ss::Tile), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return ss::cuda_fail(e);
+    }
+    e = cudaMalloc(&p->d_pm, std::max<size_t>(p->pm.size(), 1) * sizeof(ss::PmEntry));
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    e = cudaMalloc(&p->d_pm_block, std::max<size_t>(p->pm_block.size(), 1) * sizeof(int));
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    if (!p->pm.empty()) {
+        e = cudaMemcpy(p->d_pm, p->pm.data(), p->pm.size() * sizeof(ss::PmEntry),
+                       cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return ss::cuda_fail(e);
+    }
+    if (!p->pm_block.empty()) {
+        e = cudaMemcpy(p->d_pm_block, p->pm_block.data(), p->pm_block.size() * sizeof(int),
+                       cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return ss::cuda_fail(e);
     }
     p->has_dev = true;
@@ -332,8 +372,10 @@ int fsdp_plan_create(const ss_plan_desc* d, ss_plan** out) {
             else if (!build_tiles(p->data, p->eb, &p->data_tiles, &p->data_seg_tile) ||
                      !build_tiles(p->zero, p->eb, &p->zero_tiles, &p->zero_seg_tile))
                 rc = SS_EOVERFLOW;
-            else
+            else {
                 build_packed_tiles(p);
+                build_packed_map(p);
+            }
             const int64_t per16 = 16 / p->eb;
             p->vec_aligned = true;
             for (const ss::Seg& sg : p->data)
@@ -405,6 +447,8 @@ void fsdp_plan_destroy(ss_plan* p) {
     if (p->d_data_tiles) cudaFree(p->d_data_tiles);
     if (p->d_zero_tiles) cudaFree(p->d_zero_tiles);
     if (p->d_packed_tiles) cudaFree(p->d_packed_tiles);
+    if (p->d_pm) cudaFree(p->d_pm);
+    if (p->d_pm_block) cudaFree(p->d_pm_block);
     delete p;
 }
 
@@ -470,6 +514,36 @@ int fsdp_plan_validate(const ss_plan* p) {
             if (tl.seg < 0 || (size_t)tl.seg >= p->data.size()) return SS_EINVAL;
             if (p->param_group[p->data[tl.seg].param] != g) return SS_EINVAL;
         }
+    // packed segment map: every data segment once, by strictly increasing
+    // offset; pm_block[B] is the last segment starting at or before block B
+    const size_t M = p->pm.size();
+    if (M != p->data.size()) return SS_EINVAL;
+    {
+        std::vector<std::tuple<int64_t, int64_t, int64_t, int>> segs_by_off, pm_by_off;
+        for (const ss::Seg& sg : p->data)
+            segs_by_off.emplace_back(sg.packed_off, sg.param_off, sg.len, sg.param);
+        for (const ss::PmEntry& e : p->pm) pm_by_off.emplace_back(e.packed_off, e.param_off, e.len, e.param);
+        std::sort(segs_by_off.begin(), segs_by_off.end());
+        if (segs_by_off != pm_by_off) return SS_EINVAL;
+    }
+    for (size_t m = 0; m < M; ++m) {
+        const ss::PmEntry& e = p->pm[m];
+        if (e.param < 0 || e.param >= p->n || e.len <= 0) return SS_EINVAL;
+        if (e.param_off < 0 || e.param_off + e.len > p->numel[e.param]) return SS_EINVAL;
+        if (m > 0 && e.packed_off < p->pm[m - 1].packed_off + p->pm[m - 1].len) return SS_EINVAL;
+    }
+    if (p->pm_block.size() != (size_t)(p->total / ss::kMapBlock + 2)) return SS_EINVAL;
+    for (size_t B = 0; B < p->pm_block.size(); ++B) {
+        const int m = p->pm_block[B];
+        if (M == 0) {
+            if (m != 0) return SS_EINVAL;
+            continue;
+        }
+        if (m < 0 || (size_t)m >= M) return SS_EINVAL;
+        const int64_t pos = (int64_t)B * ss::kMapBlock;
+        if (m > 0 && p->pm[m].packed_off > pos) return SS_EINVAL;
+        if ((size_t)m + 1 < M && p->pm[m + 1].packed_off <= pos) return SS_EINVAL;
+    }
     return SS_OK;
 }
 

@@ -424,6 +424,73 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
         step_scalar<UNPACKED>(a, tab, slot, fs + e, ks + e);
 }
 
+// Flat form of the one-pass step, for packed gradients on plans whose runs
+// are all whole 16-byte vectors with 16-byte aligned per-parameter pointers:
+// thread q of the grid takes packed elements f = vbeg + 8q .. f + 7, as the
+// reduce-scatter kernel does.  Every load the update needs (gradients and
+// state) depends on f alone.  The segment holding f is needed only for the
+// per-parameter output store, so its lookup is started first and finishes
+// while the data loads are in flight: the block index gives the segment that
+// covers the start of f's kMapBlock block, which is f's own segment unless a
+// segment starts inside the block; only then a binary search over the few
+// segments that start in the block follows.  A pad vector is read but nothing
+// is stored.
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 3)
+fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
+                       int64_t vbeg, int64_t nvec, StepArgs a, PtrTab tab) {
+    const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (q >= nvec) return;
+    const int64_t f = vbeg + 8 * q;
+    const int64_t B = f / ss::kMapBlock;
+    int m = __ldg(pm_block + B);
+    const int n = NR > 0 ? NR : a.N;
+    uint4 w[kMaxVec];
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r)
+        if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f);
+    const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
+    const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+    const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+    ss::PmEntry e = pm[m];
+    if (f < e.packed_off || f >= e.packed_off + e.len) {  // a segment starts inside the block
+        int hi = __ldg(pm_block + B + 1);
+        while (m < hi) {
+            const int mid = (m + hi + 1) >> 1;
+            if (pm[mid].packed_off <= f)
+                m = mid;
+            else
+                hi = mid - 1;
+        }
+        e = pm[m];
+    }
+    const int64_t rel = f - e.packed_off;
+    if (rel < 0 || rel >= e.len) return;  // a pad vector
+    float s[8];
+    sum_ranks<NR>(w, n, s);
+    for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
+        add_rank(s, ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f));
+    const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
+    const int slot = e.param - a.param_base;
+    for (int j = 0; j < a.n_out; ++j)
+        ss::st_stream_u4(static_cast<uint16_t*>(tab.p[j * a.w + slot]) + e.param_off + rel, p);
+}
+
+using FlatKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, StepArgs, PtrTab);
+
+FlatKern pick_flat(int N) {
+    switch (N) {
+        case 2: return fused_step_flat_kernel<2>;
+        case 3: return fused_step_flat_kernel<3>;
+        case 4: return fused_step_flat_kernel<4>;
+        case 5: return fused_step_flat_kernel<5>;
+        case 6: return fused_step_flat_kernel<6>;
+        case 7: return fused_step_flat_kernel<7>;
+        case 8: return fused_step_flat_kernel<8>;
+        default: return fused_step_flat_kernel<0>;
+    }
+}
+
 using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
 
 template <int NR, bool U>
@@ -548,6 +615,23 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                 tab.p[goff + j * a.w + (i - wa)] = s->params_out[(size_t)j * n + i];
         }
     };
+    if (!unpacked && !gen && pb - pa <= wmax && lo % 8 == 0 && hi % 8 == 0) {
+        // packed gradients, everything aligned, one pointer table: the flat
+        // form, one thread per packed vector
+        if (hi <= lo || plan->pm.empty()) return SS_OK;
+        fill(pa, pb);
+        const int64_t nvec = (hi - lo) / 8;
+        FlatKern ff = pick_flat(N);
+        constexpr int64_t kMaxBlocks = 0x7FFFFFFF;
+        for (int64_t v0 = 0; v0 < nvec; v0 += kMaxBlocks * kThreads) {
+            const int64_t cnt = nvec - v0 < kMaxBlocks * kThreads ? nvec - v0 : kMaxBlocks * kThreads;
+            ff<<<(unsigned)((cnt + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+                plan->d_pm, plan->d_pm_block, lo + 8 * v0, cnt, a, tab);
+            int rc = ss::check_launch();
+            if (rc) return rc;
+        }
+        return SS_OK;
+    }
     if (pb - pa <= wmax) {
         // every parameter's pointers fit one table: walk the tiles in packed
         // order, so consecutive CTAs stream the gradient / state / shard
