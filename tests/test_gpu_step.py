@@ -39,6 +39,9 @@ CASES = [("tiny_mlp", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
          ("awkward2d_N3", W.awkward_2d(3)),
          ("small_llama_N3", W.llama_1b2(world_size=3, layers=3, hidden=40, ffn=72, vocab=100)),
          ("small_llama_N8", W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)),
+         # aligned plans for the flat kernel's general instance (N = 12 with pads, N = 1)
+         ("small_llama_N12", W.llama_1b2(world_size=12, layers=1, hidden=96, ffn=104, vocab=100)),
+         ("small_llama_N1", W.llama_1b2(world_size=1, layers=1, hidden=32, ffn=64, vocab=64)),
          ("per_param_N12", W.ParamSet([f"p{i}" for i in range(4)], [(130, 3), (64,), (0, 4), (257, 8)],
                                       [4], 12, W.PER_PARAM_DIM0, torch.bfloat16, seed=11))]
 
