@@ -424,18 +424,18 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
         step_scalar<UNPACKED>(a, tab, slot, fs + e, ks + e);
 }
 
-// Flat form of the one-pass step, for packed gradients on plans whose runs
-// are all whole 16-byte vectors with 16-byte aligned per-parameter pointers:
-// thread q of the grid takes packed elements f = vbeg + 8q .. f + 7, as the
-// reduce-scatter kernel does.  Every load the update needs (gradients and
-// state) depends on f alone.  The segment holding f is needed only for the
-// per-parameter output store, so its lookup is started first and finishes
-// while the data loads are in flight: the block index gives the segment that
-// covers the start of f's kMapBlock block, which is f's own segment unless a
-// segment starts inside the block; only then a binary search over the few
-// segments that start in the block follows.  A pad vector is read but nothing
-// is stored.
-template <int NR>
+// Flat form of the one-pass step, for plans whose runs are all whole 16-byte
+// vectors with 16-byte aligned per-parameter pointers: thread q of the grid
+// takes packed elements f = vbeg + 8q .. f + 7, as the reduce-scatter kernel
+// does.  The state loads depend on f alone and go out first, and so do the
+// gradient loads when the gradients are packed.  The segment holding f --
+// needed for the per-parameter gradients (UNPACKED) and outputs -- is looked
+// up meanwhile: the block index gives the segment that covers the start of
+// f's kMapBlock block, which is f's own segment unless a segment starts
+// inside the block; only then a binary search over the few segments that
+// start in the block follows.  A pad vector is read (state, packed
+// gradients) but nothing is stored.
+template <int NR, bool UNPACKED>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
                        int64_t vbeg, int64_t nvec, StepArgs a, PtrTab tab) {
@@ -446,9 +446,11 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     int m = __ldg(pm_block + B);
     const int n = NR > 0 ? NR : a.N;
     uint4 w[kMaxVec];
+    if (!UNPACKED) {
 #pragma unroll
-    for (int r = 0; r < kMaxVec; ++r)
-        if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f);
+        for (int r = 0; r < kMaxVec; ++r)
+            if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f);
+    }
     const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
     const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
     const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
@@ -466,28 +468,36 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     }
     const int64_t rel = f - e.packed_off;
     if (rel < 0 || rel >= e.len) return;  // a pad vector
+    const int slot = e.param - a.param_base;
+    const int64_t k = e.param_off + rel;  // index inside the parameter tensor
+    if (UNPACKED) {
+#pragma unroll
+        for (int r = 0; r < kMaxVec; ++r)
+            if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k);
+    }
     float s[8];
     sum_ranks<NR>(w, n, s);
     for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
-        add_rank(s, ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f));
+        add_rank(s, ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k)));
     const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
-    const int slot = e.param - a.param_base;
+    const int goff = UNPACKED ? n * a.w : 0;
     for (int j = 0; j < a.n_out; ++j)
-        ss::st_stream_u4(static_cast<uint16_t*>(tab.p[j * a.w + slot]) + e.param_off + rel, p);
+        ss::st_stream_u4(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k, p);
 }
 
 using FlatKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, StepArgs, PtrTab);
 
+template <bool U>
 FlatKern pick_flat(int N) {
     switch (N) {
-        case 2: return fused_step_flat_kernel<2>;
-        case 3: return fused_step_flat_kernel<3>;
-        case 4: return fused_step_flat_kernel<4>;
-        case 5: return fused_step_flat_kernel<5>;
-        case 6: return fused_step_flat_kernel<6>;
-        case 7: return fused_step_flat_kernel<7>;
-        case 8: return fused_step_flat_kernel<8>;
-        default: return fused_step_flat_kernel<0>;
+        case 2: return fused_step_flat_kernel<2, U>;
+        case 3: return fused_step_flat_kernel<3, U>;
+        case 4: return fused_step_flat_kernel<4, U>;
+        case 5: return fused_step_flat_kernel<5, U>;
+        case 6: return fused_step_flat_kernel<6, U>;
+        case 7: return fused_step_flat_kernel<7, U>;
+        case 8: return fused_step_flat_kernel<8, U>;
+        default: return fused_step_flat_kernel<0, U>;
     }
 }
 
@@ -615,13 +625,13 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                 tab.p[goff + j * a.w + (i - wa)] = s->params_out[(size_t)j * n + i];
         }
     };
-    if (!unpacked && !gen && pb - pa <= wmax && lo % 8 == 0 && hi % 8 == 0) {
-        // packed gradients, everything aligned, one pointer table: the flat
-        // form, one thread per packed vector
+    if (!gen && pb - pa <= wmax && lo % 8 == 0 && hi % 8 == 0) {
+        // everything aligned, one pointer table: the flat form, one thread
+        // per packed vector
         if (hi <= lo || plan->pm.empty()) return SS_OK;
         fill(pa, pb);
         const int64_t nvec = (hi - lo) / 8;
-        FlatKern ff = pick_flat(N);
+        FlatKern ff = unpacked ? pick_flat<true>(N) : pick_flat<false>(N);
         constexpr int64_t kMaxBlocks = 0x7FFFFFFF;
         for (int64_t v0 = 0; v0 < nvec; v0 += kMaxBlocks * kThreads) {
             const int64_t cnt = nvec - v0 < kMaxBlocks * kThreads ? nvec - v0 : kMaxBlocks * kThreads;
