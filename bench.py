@@ -1012,6 +1012,20 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
              ms, mn, (2 * 7 + 2) * P4 + 26 * tot4, peak)
         del rank_sets, flat_pg, st4, buf4
         torch.cuda.empty_cache()
+    # the same 1-D awkward set in fp32 (a FlatParameter of fp32 parameters)
+    if large:
+        ps5 = W.awkward_1d(7, W.FLAT_ORIG_FALSE, torch.float32, count=200,
+                           max_len=int(2_000_000 * awkward_scale))
+        st5 = Step(ss, ps5, 1)
+        P5, tot5 = st5.info["unpadded_numel"], st5.info["total_numel"]
+        ms, mn = _time_stream(lambda: st5.rs_adamw(), 20)
+        _row(f"large awkward fp32 (flat_orig_false, {P5:,} params, N=7): RS + AdamW", P5,
+             "params/s", ms, mn, (4 * 7 + 28) * tot5, peak)
+        ms, mn = _time_stream(lambda: st5.all_gather(), 20)
+        _row(f"large awkward fp32 (flat_orig_false, N=7): all-gather + unpack", P5, "params/s",
+             ms, mn, 8 * P5, peak)
+        del st5
+        torch.cuda.empty_cache()
 
 
 

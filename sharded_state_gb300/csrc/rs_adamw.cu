@@ -189,37 +189,42 @@ rs_adamw_f32_kernel(RankPtrs grads, int N, int64_t vbeg, int64_t nvec, float* __
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nvec; q += stride) {
         const int64_t f = vbeg + q * 4;
-        uint4 w0 = ss::ld_stream_u4(static_cast<const float*>(grads.p[0]) + f);
-        float s[4] = {__uint_as_float(w0.x), __uint_as_float(w0.y), __uint_as_float(w0.z),
-                      __uint_as_float(w0.w)};
-        if (NR > 0) {
-            uint4 w[NR > 1 ? NR - 1 : 1];
+        // every load of this vector before any arithmetic, as in the bf16 kernel
+        constexpr int kW = NR > 0 ? NR : 8;
+        uint4 w[kW];
+        const int nfirst = NR > 0 ? NR : (n < 8 ? n : 8);
 #pragma unroll
-            for (int r = 1; r < NR; ++r)
-                w[r - 1] = ss::ld_stream_u4(static_cast<const float*>(grads.p[r]) + f);
+        for (int r = 0; r < kW; ++r)
+            if (NR > 0 || r < nfirst) w[r] = ss::ld_stream_u4(static_cast<const float*>(grads.p[r]) + f);
+        float4 t, m, v;
+        if (ADAM) {
+            t = ss::ld_rw_f4(MASTER ? master + f : shards + f);
+            m = ss::ld_rw_f4(exp_avg + f);
+            v = ss::ld_rw_f4(exp_avg_sq + f);
+        }
+        float s[4] = {__uint_as_float(w[0].x), __uint_as_float(w[0].y), __uint_as_float(w[0].z),
+                      __uint_as_float(w[0].w)};
 #pragma unroll
-            for (int r = 1; r < NR; ++r) {
-                s[0] = __fadd_rn(s[0], __uint_as_float(w[r - 1].x));
-                s[1] = __fadd_rn(s[1], __uint_as_float(w[r - 1].y));
-                s[2] = __fadd_rn(s[2], __uint_as_float(w[r - 1].z));
-                s[3] = __fadd_rn(s[3], __uint_as_float(w[r - 1].w));
+        for (int r = 1; r < kW; ++r) {
+            if (NR > 0 || r < nfirst) {
+                s[0] = __fadd_rn(s[0], __uint_as_float(w[r].x));
+                s[1] = __fadd_rn(s[1], __uint_as_float(w[r].y));
+                s[2] = __fadd_rn(s[2], __uint_as_float(w[r].z));
+                s[3] = __fadd_rn(s[3], __uint_as_float(w[r].w));
             }
-        } else {
-            for (int r = 1; r < n; ++r) {
-                uint4 w = ss::ld_stream_u4(static_cast<const float*>(grads.p[r]) + f);
-                s[0] = __fadd_rn(s[0], __uint_as_float(w.x));
-                s[1] = __fadd_rn(s[1], __uint_as_float(w.y));
-                s[2] = __fadd_rn(s[2], __uint_as_float(w.z));
-                s[3] = __fadd_rn(s[3], __uint_as_float(w.w));
-            }
+        }
+        for (int r = 8; NR == 0 && r < n; ++r) {  // ranks beyond the first 8 (N > 8)
+            const uint4 x = ss::ld_stream_u4(static_cast<const float*>(grads.p[r]) + f);
+            s[0] = __fadd_rn(s[0], __uint_as_float(x.x));
+            s[1] = __fadd_rn(s[1], __uint_as_float(x.y));
+            s[2] = __fadd_rn(s[2], __uint_as_float(x.z));
+            s[3] = __fadd_rn(s[3], __uint_as_float(x.w));
         }
         float g[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) g[k] = __fdiv_rn(s[k], fN);
         if (WRITE_G) ss::st_stream_f4(gout + f, make_float4(g[0], g[1], g[2], g[3]));
         if (ADAM) {
-            float4 t = ss::ld_rw_f4(MASTER ? master + f : shards + f), m = ss::ld_rw_f4(exp_avg + f),
-                   v = ss::ld_rw_f4(exp_avg_sq + f);
             float th[4] = {t.x, t.y, t.z, t.w}, mm[4] = {m.x, m.y, m.z, m.w},
                   vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -321,7 +326,11 @@ F32Kernel pick_f32(int N) {
     switch (N) {
         case 1: return rs_adamw_f32_kernel<1, ADAM, WG, M>;
         case 2: return rs_adamw_f32_kernel<2, ADAM, WG, M>;
+        case 3: return rs_adamw_f32_kernel<3, ADAM, WG, M>;
         case 4: return rs_adamw_f32_kernel<4, ADAM, WG, M>;
+        case 5: return rs_adamw_f32_kernel<5, ADAM, WG, M>;
+        case 6: return rs_adamw_f32_kernel<6, ADAM, WG, M>;
+        case 7: return rs_adamw_f32_kernel<7, ADAM, WG, M>;
         case 8: return rs_adamw_f32_kernel<8, ADAM, WG, M>;
         default: return rs_adamw_f32_kernel<0, ADAM, WG, M>;
     }
