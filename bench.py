@@ -503,7 +503,7 @@ def run_e2e(st: Step, args, stream, dist) -> dict:
     K = max(args.e2e_steps, 1)
     P = st.info["unpadded_numel"]
 
-    order = list(range(G))  # registration order (largest-group-in-the-middle measured slower)
+    order = list(range(G))  # registration order (root-first and largest-in-the-middle measured slower)
 
     def one_step():
         hp = st.next_hp()
