@@ -297,6 +297,28 @@ __global__ void init_master_kernel(const void* shards, int eb, int64_t lo, int64
     }
 }
 
+// The same for 16-byte vectors of bf16 shards: elements [8*vlo, 8*vhi), one
+// vector per thread (every buffer 16-byte aligned there).
+__global__ void __launch_bounds__(kThreads)
+init_master_bf16_vec_kernel(const uint16_t* __restrict__ shards, int64_t vlo, int64_t nvec,
+                            float* __restrict__ master, float* __restrict__ m,
+                            float* __restrict__ v) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nvec; q += stride) {
+        const int64_t f = 8 * (vlo + q);
+        const uint4 w = ss::ld_stream_u4(shards + f);
+        ss::st_stream_f4(master + f, make_float4(ss::bf16_lo(w.x), ss::bf16_hi(w.x), ss::bf16_lo(w.y),
+                                                 ss::bf16_hi(w.y)));
+        ss::st_stream_f4(master + f + 4, make_float4(ss::bf16_lo(w.z), ss::bf16_hi(w.z),
+                                                     ss::bf16_lo(w.w), ss::bf16_hi(w.w)));
+        ss::st_stream_f4(m + f, z);
+        ss::st_stream_f4(m + f + 4, z);
+        ss::st_stream_f4(v + f, z);
+        ss::st_stream_f4(v + f + 4, z);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
@@ -456,12 +478,26 @@ int fsdp_init_master(const ss_plan* plan, const void* param_shards, float* maste
     for (const void* b : bufs)
         if (!ss::aligned(b, 16)) return SS_EALIGN;
     if (hi <= lo) return SS_OK;
-    int64_t blocks = (hi - lo + kThreads - 1) / kThreads;
-    int64_t cap = (int64_t)ss::num_sms() * 8;
-    init_master_kernel<<<(int)(blocks < cap ? blocks : cap), kThreads, 0,
-                         reinterpret_cast<cudaStream_t>(stream)>>>(param_shards, plan->eb, lo, hi,
-                                                                   master, exp_avg, exp_avg_sq);
-    return ss::check_launch();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t cap = (int64_t)ss::num_sms() * 8;
+    auto scalar = [&](int64_t a0, int64_t a1) -> int {
+        if (a1 <= a0) return SS_OK;
+        const int64_t blocks = (a1 - a0 + kThreads - 1) / kThreads;
+        init_master_kernel<<<(int)(blocks < cap ? blocks : cap), kThreads, 0, st>>>(
+            param_shards, plan->eb, a0, a1, master, exp_avg, exp_avg_sq);
+        return ss::check_launch();
+    };
+    if (plan->eb != 2) return scalar(lo, hi);
+    // bf16: 16-byte vectors over the 8-aligned middle, scalar head and tail
+    const int64_t vlo = (lo + 7) / 8, vhi = hi / 8;
+    if (vhi <= vlo) return scalar(lo, hi);
+    int rc = scalar(lo, 8 * vlo);
+    if (rc) return rc;
+    init_master_bf16_vec_kernel<<<grid_for(vhi - vlo), kThreads, 0, st>>>(
+        static_cast<const uint16_t*>(param_shards), vlo, vhi - vlo, master, exp_avg, exp_avg_sq);
+    rc = ss::check_launch();
+    if (rc) return rc;
+    return scalar(8 * vhi, hi);
 }
 
 }  // extern "C"
