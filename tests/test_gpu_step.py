@@ -207,6 +207,52 @@ def test_sharded_step_full_size_equals_two_calls(ss):
     torch.cuda.empty_cache()
 
 
+def test_sharded_step_full_size_copy_in_equals_pack_and_two_calls(ss):
+    """The 1.2B model with the gradients as 8 per-parameter sets (fused
+    copy-in, the flat kernel's UNPACKED form): bit-identical to packing each
+    set and running RS+AdamW + all-gather."""
+    ps = W.llama_1b2()
+    su = Setup(ss, ps, make_values=False)
+    total, N = su.total, su.N
+    gen = torch.Generator(device="cuda").manual_seed(44)
+    init = (torch.randn(total, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+    sets = [[(torch.randn(s, device="cuda", generator=gen) * 1e-3).to(torch.bfloat16)
+             for s in ps.shapes] for _ in range(N)]
+    flat_sets = [g for rank in sets for g in rank]
+    res = []
+    for mode in ("pack_two_calls", "copy_in"):
+        shards = init.clone()
+        master = torch.empty(total, device="cuda")
+        m = torch.empty_like(master)
+        v = torch.empty_like(master)
+        ss.fsdp_init_master(su.plan, shards, master, m, v)
+        outs = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in ps.shapes]
+        hp = ss.adamw_params(step=1)
+        if mode == "pack_two_calls":
+            packed = []
+            for r in range(N):
+                b = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+                ss.fsdp_pack(su.plan, sets[r], b)
+                packed.append(b)
+            ss.fsdp_reduce_scatter_adamw(su.plan, packed, master, m, v, shards, hp)
+            ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+            torch.cuda.synchronize()
+            del packed
+        else:
+            ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_param_grads=flat_sets,
+                                 params_out=outs, n_out=1)
+            torch.cuda.synchronize()
+        res.append((shards, master, m, v, outs))
+    a, b = res
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    for x, y in zip(a[1:4], b[1:4]):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    for x, y in zip(a[4], b[4]):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    del res, a, b, sets, flat_sets
+    torch.cuda.empty_cache()
+
+
 def test_sharded_step_argument_errors(ss):
     su = Setup(ss, W.tiny_mlp())
     shards, master, m, v = _state(ss, su)
