@@ -1,17 +1,20 @@
 #!/usr/bin/env python
 """Benchmark of the sharded RS+AdamW+AG step (FSDP / ZeRO-3 per-step pass) on GB300.
 
-One step = the whole hot path over one synthetic batch of gradients:
-  1. fsdp_reduce_scatter_adamw over every fully_shard group (one launch):
-     N virtual ranks' bf16 gradients summed in fp32 in rank order, divided by
-     N, AdamW on every rank's shard of the fp32 master/moments, bf16 shards
-     written;
-  2. fsdp_all_gather_unpack over every group (one launch): the N shards back
-     into full per-parameter bf16 tensors (n_out replicas, default 1).
+One step = the whole hot path over one synthetic batch of gradients, by
+default as one fsdp_sharded_step launch over every fully_shard group:
+  - the reduce-scatter: N virtual ranks' bf16 gradients summed in fp32 in
+    rank order and divided by N;
+  - AdamW on every rank's shard of the fp32 master/moments, bf16 shards
+    written;
+  - the all-gather + unpack: the new values written into full per-parameter
+    bf16 tensors (n_out replicas, default 1).
+--step-kind two_calls runs the same step as fsdp_reduce_scatter_adamw then
+fsdp_all_gather_unpack (two launches, bit-identical results).
 Default workload: the 1.2B Llama-shaped model (24 layers, hidden 2048, FFN
 5632, vocab 32000, untied embeddings) with N = 8 virtual ranks, FSDP2
 per-parameter dim-0 layout, 24 block groups + 1 root group, 1,364,297,728
-parameters.  Every buffer is resident in HBM; the 62.8 GB a step moves are far
+parameters.  Every buffer is resident in HBM; the 60 GB a step moves are far
 larger than L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
@@ -98,7 +101,7 @@ def workload_config(ps: W.ParamSet, info, n_out: int) -> dict:
             "layout": W.LAYOUT_NAMES[ps.layout], "n_out": n_out,
             "storage": "bf16 grads/params, fp32 master/exp_avg/exp_avg_sq",
             "adamw": {k: v for k, v in W.adamw_hparams().items() if k != "step"},
-            "l2": "no flush: inputs of every step (>= 62 GB at the default workload) exceed L2"}
+            "l2": "no flush: the bytes every step moves (>= 60 GB at the default workload) exceed L2"}
 
 
 def ncu_traffic(kernel: str, units: int):
