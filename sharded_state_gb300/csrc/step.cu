@@ -356,11 +356,20 @@ static_assert(kSub * kThreads * 8 * 2 == ss::kTileBytes, "tile split");
 template <int NR, bool UNPACKED, bool GEN>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
-                  StepArgs a, PtrTab tab) {
+                  const ss::PmEntry* __restrict__ ext, StepArgs a, PtrTab tab) {
     constexpr int64_t T = ss::kTileBytes / 2;
-    const ss::Tile tl = tiles[t_lo + blockIdx.x];
-    const ss::Seg sg = segs[tl.seg];
-    const int64_t off = (int64_t)tl.idx * T;
+    // The tile and its segment: one 32-byte load when the packed-order table
+    // with the segment inline is given (ext), else the tile, then its segment.
+    ss::PmEntry sg;
+    if (ext) {
+        sg = ext[t_lo + blockIdx.x];
+    } else {
+        const ss::Tile tl = tiles[t_lo + blockIdx.x];
+        const ss::Seg x = segs[tl.seg];
+        sg = ss::PmEntry{x.packed_off, x.param_off, x.len, x.param, tl.idx};
+    }
+    const int64_t tile_idx = sg.reserved;
+    const int64_t off = tile_idx * T;
     const int64_t len = sg.len - off < T ? sg.len - off : T;
     constexpr int64_t kPart = T / kSub;  // elements of this CTA's part of the tile
     const int slot = sg.param - a.param_base;
@@ -383,7 +392,7 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
     // once per part, and the head runs on the last threads, which have no
     // vector in a segment's first part.  Vectors: packed side aligned,
     // per-parameter side aligned or realigned in registers.
-    const int64_t j = (int64_t)tl.idx * kSub + blockIdx.y;  // part index within the segment
+    const int64_t j = tile_idx * kSub + blockIdx.y;  // part index within the segment
     const int64_t u = sg.packed_off & 7;
     const int64_t e0 = j == 0 ? 0 : j * kPart - u;
     const int64_t e1 = (j + 1) * kPart >= sg.len ? sg.len : (j + 1) * kPart - u;
@@ -501,7 +510,8 @@ FlatKern pick_flat(int N) {
     }
 }
 
-using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
+using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, const ss::PmEntry*, StepArgs,
+                     PtrTab);
 
 template <int NR, bool U>
 Kern pick_gen(bool gen) {
@@ -604,10 +614,11 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     PtrTab tab;
     constexpr int64_t kMaxGrid = (int64_t)1 << 30;
-    auto launch = [&](const ss::Tile* tiles, int64_t t_lo, int64_t t_hi) -> int {
+    auto launch = [&](const ss::Tile* tiles, const ss::PmEntry* ext, int64_t t_lo,
+                      int64_t t_hi) -> int {
         for (int64_t t = t_lo; t < t_hi; t += kMaxGrid) {
             const int64_t cnt = t_hi - t < kMaxGrid ? t_hi - t : kMaxGrid;
-            fn<<<dim3((unsigned)cnt, kSub), kThreads, 0, st>>>(tiles, t, plan->d_data, a, tab);
+            fn<<<dim3((unsigned)cnt, kSub), kThreads, 0, st>>>(tiles, t, plan->d_data, ext, a, tab);
             int rc = ss::check_launch();
             if (rc) return rc;
         }
@@ -648,14 +659,16 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         // buffers front to back
         fill(pa, pb);
         const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
-        return launch(plan->d_packed_tiles, plan->group_ptile[ga], plan->group_ptile[gb]);
+        return launch(plan->d_packed_tiles, plan->d_packed_tiles_ext, plan->group_ptile[ga],
+                      plan->group_ptile[gb]);
     }
     for (int wa = pa; wa < pb; wa += wmax) {
         const int wb = wa + wmax < pb ? wa + wmax : pb;
         const int s_lo = plan->param_seg[wa], s_hi = plan->param_seg[wb];
         if (s_hi <= s_lo) continue;
         fill(wa, wb);
-        int rc = launch(plan->d_data_tiles, plan->data_seg_tile[s_lo], plan->data_seg_tile[s_hi]);
+        int rc = launch(plan->d_data_tiles, nullptr, plan->data_seg_tile[s_lo],
+                        plan->data_seg_tile[s_hi]);
         if (rc) return rc;
     }
     return SS_OK;
