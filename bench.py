@@ -907,8 +907,11 @@ def _rows_block4096(ss, peak, K):
         st2.all_gather()
     ms, mn = _time_stream(step2, K)
     by = step_bytes(8, total2, P2, 1)
-    _row("step on one Llama block, hidden 4096 (202M params, N=8)", P2, "params/s", ms, mn,
-         by["step"], peak)
+    _row("step on one Llama block, hidden 4096 (202M params, N=8): two calls", P2, "params/s", ms,
+         mn, by["step"], peak)
+    ms, mn = _time_stream(lambda: st2.fused_step(), K)
+    _row("step on one Llama block, hidden 4096 (202M params, N=8): one pass", P2, "params/s", ms,
+         mn, (2 * 8 + 26) * total2 + 2 * P2, peak)
     del st2
     torch.cuda.empty_cache()
 
