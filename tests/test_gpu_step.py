@@ -43,7 +43,12 @@ CASES = [("tiny_mlp", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
          ("small_llama_N12", W.llama_1b2(world_size=12, layers=1, hidden=96, ffn=104, vocab=100)),
          ("small_llama_N1", W.llama_1b2(world_size=1, layers=1, hidden=32, ffn=64, vocab=64)),
          ("per_param_N12", W.ParamSet([f"p{i}" for i in range(4)], [(130, 3), (64,), (0, 4), (257, 8)],
-                                      [4], 12, W.PER_PARAM_DIM0, torch.bfloat16, seed=11))]
+                                      [4], 12, W.PER_PARAM_DIM0, torch.bfloat16, seed=11)),
+         # 500 tiny aligned params: dozens of segment starts (and pad runs) in
+         # every 2048-element block, so the flat kernel's binary search runs
+         ("tiny_params_N4", W.ParamSet([f"t{i}" for i in range(500)],
+                                       [(1 + (7 * i) % 9, 8) for i in range(500)],
+                                       [500], 4, W.PER_PARAM_DIM0, torch.bfloat16, seed=13))]
 
 
 def _state(ss, su):
