@@ -2,12 +2,14 @@
 // (copy-in) + reduce-scatter + AdamW + (all-gather + unpack).
 //
 // fsdp_reduce_scatter_adamw streams the packed index space and
-// fsdp_all_gather_unpack then reads the new shards back to unpack them.  This
-// kernel walks the plan's data tiles instead (one CTA per 16 KiB tile of one
-// parameter's run inside one rank's shard, "FSDP1 vs FSDP2" section 03 / 04),
-// so for every element it knows both its packed index f (gradient buffers,
-// optimizer state, shards) and its place k inside the parameter tensor.  That
-// lets one pass
+// fsdp_all_gather_unpack then reads the new shards back to unpack them.  The
+// kernels here know for every element both its packed index f (gradient
+// buffers, optimizer state, shards) and its place k inside the parameter
+// tensor ("FSDP1 vs FSDP2" section 03 / 04: a run of one parameter inside one
+// rank's shard).  Two forms: fused_step_flat_kernel streams f like the
+// reduce-scatter and places each vector through the plan's packed segment
+// map (plans whose runs are all whole 16-byte vectors); fused_step_kernel
+// walks the plan's data tiles (any alignment).  That lets one pass
 //   - read the N gradients either from the packed rank buffers (the
 //     reduce-scatter input FSDP builds by copy-in) or directly from the N
 //     per-parameter gradient sets, which fuses the copy-in away;
