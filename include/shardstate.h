@@ -311,9 +311,10 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards,
 /*
  * The whole sharded step in one pass over the parameters: (copy-in) +
  * reduce-scatter + AdamW + (all-gather + unpack).  Same arithmetic as
- * fsdp_reduce_scatter_adamw followed by fsdp_all_gather_unpack, but the
- * kernel walks the plan's data tiles (runs of one parameter inside one rank's
- * shard), so in one pass it can
+ * fsdp_reduce_scatter_adamw followed by fsdp_all_gather_unpack, with
+ * bit-identical results, but the kernel knows each element's place inside its
+ * parameter (the plan's runs of one parameter inside one rank's shard), so in
+ * one pass it can
  *   - read rank r's gradient either from its packed buffer (rank_grads[r],
  *     as fsdp_pack writes it) or straight from rank r's per-parameter
  *     gradient tensors (rank_param_grads[r*num_params + i]), fusing away the
