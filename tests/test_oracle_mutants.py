@@ -119,6 +119,48 @@ MUTANTS = [
 ]
 
 
+# The oracle's Python parts: (name, file under oracle/, exact text, replacement).
+PY_MUTANTS = [
+    ("ZeRO-1 resident bytes with one gradient copy fewer", "ledger.py",
+     "        return 2 * P * b + P * bopt / N",
+     "        return P * b + P * bopt / N"),
+    ("ZeRO-2 resident bytes without the sharded gradient", "ledger.py",
+     "        return P * b + P * (b + bopt) / N",
+     "        return P * b + P * bopt / N"),
+    ("ZeRO-3 resident bytes without the sharded gradient", "ledger.py",
+     "        return P * (2 * b + bopt) / N",
+     "        return P * (b + bopt) / N"),
+    ("worst peak without the gathered parameter copy", "ledger.py",
+     "        return resident + P * b",
+     "        return resident"),
+    ("FULL_SHARD traffic without the (N-1)/N factor", "ledger.py",
+     "        return 3 * P * (N - 1) / N",
+     "        return 3 * P"),
+    ("SHARD_GRAD_OP / NO_SHARD traffic halved", "ledger.py",
+     "        return 2 * P * (N - 1) / N",
+     "        return P * (N - 1) / N"),
+    ("LayerNorm backward without its second mean term", "dp_equivalence.py",
+     "    do = rstd * (dxhat - dxhat.mean(axis=1, keepdims=True)\n"
+     "                 - xhat * (dxhat * xhat).mean(axis=1, keepdims=True))",
+     "    do = rstd * (dxhat - dxhat.mean(axis=1, keepdims=True))"),
+    ("ReLU backward without the mask", "dp_equivalence.py",
+     "    da = dh * (a > 0)",
+     "    da = dh"),
+    ("loss gradient of the sum, not the mean, over samples", "dp_equivalence.py",
+     "    dy = diff / B",
+     "    dy = diff"),
+    ("unequal rank batches averaged without token weights", "dp_equivalence.py",
+     "        w = (n_r / B) if token_weighted else (1.0 / N)",
+     "        w = 1.0 / N"),
+    ("micro-batch gradients summed, not averaged", "dp_equivalence.py",
+     "            acc[k] += g[k] / micro_batches",
+     "            acc[k] += g[k]"),
+]
+
+PY_CONTROL = ("control: Python oracle copied with nothing planted", "ledger.py",
+              '"""Closed-form memory and communication ledgers of DP / ZeRO / FSDP.',
+              '"""Closed-form memory and communication ledgers of DP / ZeRO / FSDP (control).')
+
 # A "mutation" that changes nothing but a comment: built and run like the others.
 CONTROL = ("control: no mistake planted",
            "/* Round a binary32 to the nearest bf16, ties to the even bf16.  Written from",
@@ -151,6 +193,34 @@ def _run_mutant(workdir, name, find, replace):
     return r.returncode, r.stdout[-2000:] + r.stderr[-2000:]
 
 
+def _run_py_mutant(workdir, lib, name, relfile, find, replace):
+    """Copy the oracle package, the workloads and the pin suite, plant one
+    mistake in a Python file of the copied oracle, and run the pins there
+    (against the unmodified C library): (pytest exit code, output)."""
+    import shutil
+    skip = shutil.ignore_patterns("__pycache__", "*.so", "*.pyc")
+    shutil.copytree(os.path.join(ROOT, "oracle"), os.path.join(workdir, "oracle"), ignore=skip)
+    shutil.copytree(os.path.join(ROOT, "workloads"), os.path.join(workdir, "workloads"), ignore=skip)
+    tdir = os.path.join(workdir, "tests")
+    os.makedirs(tdir)
+    for f in ("__init__.py", "conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(HERE, f), tdir)
+    shutil.copytree(os.path.join(HERE, "golden"), os.path.join(tdir, "golden"))
+    path = os.path.join(workdir, "oracle", relfile)
+    with open(path) as f:
+        src = f.read()
+    if src.count(find) != 1:
+        return None, f"mutation target not unique or missing: {name}"
+    with open(path, "w") as f:
+        f.write(src.replace(find, replace))
+    env = dict(os.environ, **{oracle.ORACLE_LIB_ENV: lib, "OMP_NUM_THREADS": "2"})
+    env.pop("PYTHONPATH", None)
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(tdir, "test_oracle_pins.py"),
+                        "-x", "-q", "-p", "no:cacheprovider"],
+                       cwd=workdir, env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode, r.stdout[-2000:] + r.stderr[-2000:]
+
+
 @pytest.fixture(scope="module")
 def mutant_results(tmp_path_factory):
     """Every mutant built and run against the pins, several at a time."""
@@ -158,8 +228,11 @@ def mutant_results(tmp_path_factory):
     base = tmp_path_factory.mktemp("mutants")
     workers = max(1, min(8, os.cpu_count() or 1))
     jobs = MUTANTS + [CONTROL]
+    lib = oracle.build()
     with cf.ThreadPoolExecutor(max_workers=workers) as ex:
         futs = {m[0]: ex.submit(_run_mutant, str(base / f"m{i}"), *m) for i, m in enumerate(jobs)}
+        for i, m in enumerate(PY_MUTANTS + [PY_CONTROL]):
+            futs[m[0]] = ex.submit(_run_py_mutant, str(base / f"p{i}"), lib, *m)
         return {name: f.result() for name, f in futs.items()}
 
 
@@ -172,7 +245,15 @@ def test_unmutated_build_passes_the_pins(mutant_results):
 
 
 @pytest.mark.skipif(not _gcc_available(), reason="gcc is needed to build the mutants")
-@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_unmutated_python_copy_passes_the_pins(mutant_results):
+    """The control for the Python mutants: the copied tree with nothing planted
+    passes the pins, so a failing run is the pins at work, not the copy."""
+    code, out = mutant_results[PY_CONTROL[0]]
+    assert code == 0, out
+
+
+@pytest.mark.skipif(not _gcc_available(), reason="gcc is needed to build the mutants")
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS] + [m[0] for m in PY_MUTANTS])
 def test_pins_catch_mutant(mutant_results, name):
     code, out = mutant_results[name]
     # exit code 1: the pins ran and at least one failed (a crash or a
