@@ -42,6 +42,9 @@ CASES = [("tiny_mlp", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
          # aligned plans for the flat kernel's general instance (N = 12 with pads, N = 1)
          ("small_llama_N12", W.llama_1b2(world_size=12, layers=1, hidden=96, ffn=104, vocab=100)),
          ("small_llama_N1", W.llama_1b2(world_size=1, layers=1, hidden=32, ffn=64, vocab=64)),
+         # the largest world size the ABI takes (SS_MAX_WORLD), aligned: the
+         # flat kernel with 8 ranks' loads in flight and the other 56 in a loop
+         ("llama_N64", W.llama_1b2(world_size=64, layers=1, hidden=512, ffn=1024, vocab=128)),
          ("per_param_N12", W.ParamSet([f"p{i}" for i in range(4)], [(130, 3), (64,), (0, 4), (257, 8)],
                                       [4], 12, W.PER_PARAM_DIM0, torch.bfloat16, seed=11)),
          # 500 tiny aligned params: dozens of segment starts (and pad runs) in
