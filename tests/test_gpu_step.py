@@ -323,3 +323,28 @@ def test_zero12_step_every_rank_gets_the_parameters(ss):
                 np.testing.assert_array_equal(to_np(outs_a[j * n + i]), to_np(outs_b[j * n + i]))
                 np.testing.assert_array_equal(to_np(outs_b[j * n + i]), want[j][i])
     assert all(guards_intact(w) for w in wholes)
+
+
+def test_sharded_step_max_replicas(ss):
+    """n_out = SS_MAX_REPLICAS outputs from the one pass equal the all-gather
+    with the same replica count after RS+AdamW, bit for bit."""
+    ps = W.tiny_mlp(2, W.FLAT_ORIG_TRUE)
+    su = Setup(ss, ps)
+    N, total, R = su.N, su.total, ss.SS_MAX_REPLICAS
+    packed = []
+    for r, rank in enumerate(W.make_rank_grads(ps)):
+        b = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+        ss.fsdp_pack(su.plan, [g.cuda() for g in rank], b)
+        packed.append(b)
+    sa, ma, mma, va = _state(ss, su)
+    sb, mb, mmb, vb = _state(ss, su)
+    outs_a = [torch.empty_like(p) for _ in range(R) for p in su.params]
+    outs_b = [torch.empty_like(p) for _ in range(R) for p in su.params]
+    hp = ss.adamw_params(step=1, **_hp(1))
+    ss.fsdp_reduce_scatter_adamw(su.plan, packed, ma, mma, va, sa, hp)
+    ss.fsdp_all_gather_unpack(su.plan, sa, outs_a, n_out=R)
+    ss.fsdp_sharded_step(su.plan, mb, mmb, vb, sb, hp, rank_grads=packed, params_out=outs_b, n_out=R)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(sa), to_np(sb))
+    for x, y in zip(outs_a, outs_b):
+        np.testing.assert_array_equal(to_np(x), to_np(y))
