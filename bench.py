@@ -814,7 +814,18 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     ms, mn = _time_stream(lambda: st.fused_step(param_grads=flat_pg), K)
     _row("one-pass step with fused copy-in: N per-parameter grad sets -> RS+AdamW -> shards + "
          "unpacked params (1.2B, N=8)", P, "params/s", ms, mn, (2 * N + 28) * P, peak)
-    del rank_sets, flat_pg
+    # its unfused counterpart: pack each rank's set (the copy-in), then the two calls
+    set_arrs = [ss.ptr_array(rank) for rank in rank_sets]
+
+    def pack_then_step():
+        for r in range(N):
+            ss.fsdp_pack(st.plan, set_arrs[r], st.grads[r])
+        st.rs_adamw()
+        st.all_gather()
+    ms, mn = _time_stream(pack_then_step, max(K // 4, 5))
+    _row("F1 counterpart: N packs of the per-parameter grad sets, then RS+AdamW and all-gather "
+         "(1.2B, N=8)", P, "params/s", ms, mn, 4 * N * P + (2 * N + 26) * total + 4 * P, peak)
+    del rank_sets, flat_pg, set_arrs
     # F2: FULL_SHARD gathers the parameters twice per iteration (forward and
     # backward), SHARD_GRAD_OP once ("FSDP1 vs FSDP2", strategy table)
     def full_shard():
