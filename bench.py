@@ -938,8 +938,14 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
             st1.all_gather()
         ms, mn = _time_stream(step1, 200, warmup=20)
         by = step_bytes(2, st1.info["total_numel"], st1.info["unpadded_numel"], 1)
-        _row("step on the tiny MLP (16,640 params, N=2): latency", st1.info["unpadded_numel"],
-             "params/s", ms, mn, by["step"], peak, extra={"us_per_step": ms * 1e3})
+        _row("step on the tiny MLP (16,640 params, N=2): latency, two calls",
+             st1.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
+             extra={"us_per_step": ms * 1e3})
+        ms, mn = _time_stream(lambda: st1.fused_step(), 200, warmup=20)
+        _row("step on the tiny MLP (16,640 params, N=2): latency, one fsdp_sharded_step call",
+             st1.info["unpadded_numel"], "params/s", ms, mn,
+             (2 * 2 + 26) * st1.info["total_numel"] + 2 * st1.info["unpadded_numel"], peak,
+             extra={"us_per_step": ms * 1e3})
         # the same two C-ABI calls captured once in a CUDA graph and replayed:
         # the launch-bound step without host-side call overhead (the AdamW step
         # count is frozen in the captured arguments, which does not change the
