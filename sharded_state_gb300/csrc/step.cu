@@ -6,10 +6,12 @@
 // kernels here know for every element both its packed index f (gradient
 // buffers, optimizer state, shards) and its place k inside the parameter
 // tensor ("FSDP1 vs FSDP2" section 03 / 04: a run of one parameter inside one
-// rank's shard).  Two forms: fused_step_flat_kernel streams f like the
-// reduce-scatter and places each vector through the plan's packed segment
-// map (plans whose runs are all whole 16-byte vectors); fused_step_kernel
-// walks the plan's data tiles (any alignment).  That lets one pass
+// rank's shard).  Two forms: the flat kernels stream f like the
+// reduce-scatter and place each vector through the plan's packed segment
+// map (fused_step_flat_kernel: runs all whole 16-byte vectors;
+// fused_step_flat_any_kernel: packed gradients, any alignment);
+// fused_step_kernel walks the plan's data tiles (any alignment, used for the
+// copy-in on misaligned plans and for parameter windows).  That lets one pass
 //   - read the N gradients either from the packed rank buffers (the
 //     reduce-scatter input FSDP builds by copy-in) or directly from the N
 //     per-parameter gradient sets, which fuses the copy-in away;
@@ -114,36 +116,53 @@ __device__ __forceinline__ void add_rank(float (&s)[8], uint4 x) {
     s[7] = __fadd_rn(s[7], ss::bf16_hi(x.w));
 }
 
+// The rank sum s of 8 elements divided by n (g) and AdamW on the state loaded
+// as t/m/v, giving the new master, moments th/mm/vv.
+__device__ __forceinline__ void adam_compute(const StepArgs& a, const float (&s)[8], int n, float4 t0,
+                                             float4 t1, float4 m0, float4 m1, float4 v0, float4 v1,
+                                             float (&g)[8], float (&th)[8], float (&mm)[8],
+                                             float (&vv)[8]) {
+    const float fN = (float)n;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = __fdiv_rn(s[e], fN);
+    th[0] = t0.x; th[1] = t0.y; th[2] = t0.z; th[3] = t0.w;
+    th[4] = t1.x; th[5] = t1.y; th[6] = t1.z; th[7] = t1.w;
+    mm[0] = m0.x; mm[1] = m0.y; mm[2] = m0.z; mm[3] = m0.w;
+    mm[4] = m1.x; mm[5] = m1.y; mm[6] = m1.z; mm[7] = m1.w;
+    vv[0] = v0.x; vv[1] = v0.y; vv[2] = v0.z; vv[3] = v0.w;
+    vv[4] = v1.x; vv[5] = v1.y; vv[6] = v1.z; vv[7] = v1.w;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) adamw_elem(g[e], th[e], mm[e], vv[e], a.c);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&th)[8]) {
+    uint4 p;
+    p.x = ss::pack_bf16x2(th[0], th[1]);
+    p.y = ss::pack_bf16x2(th[2], th[3]);
+    p.z = ss::pack_bf16x2(th[4], th[5]);
+    p.w = ss::pack_bf16x2(th[6], th[7]);
+    return p;
+}
+
 // The rank sum s of packed elements f..f+7 divided by n, AdamW on the state
 // loaded as t/m/v, state and shard stores (and the reduced gradient when
 // a.gout is set); returns the new bf16 parameter vector.
 __device__ __forceinline__ uint4 adam_vec(const StepArgs& a, int64_t f, const float (&s)[8], int n,
                                           float4 t0, float4 t1, float4 m0, float4 m1, float4 v0,
                                           float4 v1) {
-    const float fN = (float)n;
-    float g[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) g[e] = __fdiv_rn(s[e], fN);
+    float g[8], th[8], mm[8], vv[8];
+    adam_compute(a, s, n, t0, t1, m0, m1, v0, v1, g, th, mm, vv);
     if (a.gout) {
         ss::st_stream_f4(a.gout + f, make_float4(g[0], g[1], g[2], g[3]));
         ss::st_stream_f4(a.gout + f + 4, make_float4(g[4], g[5], g[6], g[7]));
     }
-    float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-    float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) adamw_elem(g[e], th[e], mm[e], vv[e], a.c);
     ss::st_stream_f4(a.master + f, make_float4(th[0], th[1], th[2], th[3]));
     ss::st_stream_f4(a.master + f + 4, make_float4(th[4], th[5], th[6], th[7]));
     ss::st_stream_f4(a.exp_avg + f, make_float4(mm[0], mm[1], mm[2], mm[3]));
     ss::st_stream_f4(a.exp_avg + f + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
     ss::st_stream_f4(a.exp_avg_sq + f, make_float4(vv[0], vv[1], vv[2], vv[3]));
     ss::st_stream_f4(a.exp_avg_sq + f + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
-    uint4 p;
-    p.x = ss::pack_bf16x2(th[0], th[1]);
-    p.y = ss::pack_bf16x2(th[2], th[3]);
-    p.z = ss::pack_bf16x2(th[4], th[5]);
-    p.w = ss::pack_bf16x2(th[6], th[7]);
+    const uint4 p = pack_bf16x8(th);
     ss::st_stream_u4(a.shards + f, p);
     return p;
 }
@@ -435,6 +454,26 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
         step_scalar<UNPACKED>(a, tab, slot, fs + e, ks + e);
 }
 
+// The map entry of packed element f in block B = f / kMapBlock, given the
+// block's first candidate m = pm_block[B] and e = pm[m]: unless e's segment
+// holds f, a binary search over the entries that start inside the block for
+// the last one that starts at or before f (m stays pm_block[B] when none
+// does: f lies before the first segment).  m and e are updated.
+__device__ __forceinline__ void locate(const ss::PmEntry* __restrict__ pm,
+                                       const int* __restrict__ pm_block, int64_t B, int64_t f,
+                                       int& m, ss::PmEntry& e) {
+    if (f >= e.packed_off && f < e.packed_off + e.len) return;
+    int hi = __ldg(pm_block + B + 1);
+    while (m < hi) {
+        const int mid = (m + hi + 1) >> 1;
+        if (pm[mid].packed_off <= f)
+            m = mid;
+        else
+            hi = mid - 1;
+    }
+    e = pm[m];
+}
+
 // Flat form of the one-pass step, for plans whose runs are all whole 16-byte
 // vectors with 16-byte aligned per-parameter pointers: thread q of the grid
 // takes packed elements f = vbeg + 8q .. f + 7, as the reduce-scatter kernel
@@ -466,17 +505,7 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
     const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
     ss::PmEntry e = pm[m];
-    if (f < e.packed_off || f >= e.packed_off + e.len) {  // a segment starts inside the block
-        int hi = __ldg(pm_block + B + 1);
-        while (m < hi) {
-            const int mid = (m + hi + 1) >> 1;
-            if (pm[mid].packed_off <= f)
-                m = mid;
-            else
-                hi = mid - 1;
-        }
-        e = pm[m];
-    }
+    locate(pm, pm_block, B, f, m, e);
     const int64_t rel = f - e.packed_off;
     if (rel < 0 || rel >= e.len) return;  // a pad vector
     const int slot = e.param - a.param_base;
@@ -509,6 +538,144 @@ FlatKern pick_flat(int N) {
         case 7: return fused_step_flat_kernel<7, U>;
         case 8: return fused_step_flat_kernel<8, U>;
         default: return fused_step_flat_kernel<0, U>;
+    }
+}
+
+// The call range's elements outside whole packed vectors: [h0, h0 + nh) at
+// its start and [t0, t0 + nt) at its end, fewer than 8 each.
+struct EdgeElems {
+    int64_t h0, t0;
+    int nh, nt;
+};
+
+// Flat form of the one-pass step for packed gradients at any alignment of the
+// runs and of the per-parameter outputs.  Thread q takes the 8-aligned packed
+// vector f = vbeg + 8q; its gradient and state loads are aligned and go out
+// before the segment lookup, as in the aligned flat kernel.
+//  - A vector inside one segment (the common case) stores its state and shard
+//    as vectors.  Its per-parameter output starts sh bytes past a 16-byte
+//    boundary; when the next lane holds the next vector of the same segment,
+//    the lane writes the aligned block after its start whole (its last sh
+//    bytes, the next vector's first 16 - sh), otherwise only its own bytes of
+//    that block; a lane whose previous lane is not its predecessor in the
+//    segment also writes its first 16 - sh bytes into the block before.
+//  - A vector that meets a segment end (the rest pad or the next segment's
+//    start) is stored element by element, each element placed by its own
+//    segment; pad elements are not stored.
+//  - Threads nvec .. nvec + 15 take the range's edge elements one by one.
+// Lanes never leave before the shuffles, so whole warps take part in them.
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 3)
+fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
+                           int M, int64_t vbeg, int64_t nvec, EdgeElems ed, StepArgs a, PtrTab tab) {
+    const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int n = NR > 0 ? NR : a.N;
+    int key = -1;  // map entry of a vector inside one segment, else -1
+    int slot = 0;
+    int64_t k = 0;
+    uint4 p = make_uint4(0, 0, 0, 0);
+    if (q < nvec) {
+        const int64_t f = vbeg + 8 * q;
+        const int64_t B = f / ss::kMapBlock;
+        int m = __ldg(pm_block + B);
+        uint4 w[kMaxVec];
+#pragma unroll
+        for (int r = 0; r < kMaxVec; ++r)
+            if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f);
+        const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
+        const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+        const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+        ss::PmEntry e = pm[m];
+        locate(pm, pm_block, B, f, m, e);
+        float s[8];
+        sum_ranks<NR>(w, n, s);
+        for (int r = kMaxVec; NR == 0 && r < n; ++r)
+            add_rank(s, ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f));
+        if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
+            p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
+            key = m;
+            slot = e.param - a.param_base;
+            k = e.param_off + (f - e.packed_off);
+        } else {
+            float g[8], th[8], mm[8], vv[8];
+            adam_compute(a, s, n, t0, t1, m0, m1, v0, v1, g, th, mm, vv);
+            const int goff = 0;
+            int c = m;  // the entry of element f + i: the last one starting at or before it
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t x = f + i;
+                while (c + 1 < M && pm[c + 1].packed_off <= x) {
+                    ++c;
+                    e = pm[c];
+                }
+                if (x < e.packed_off || x >= e.packed_off + e.len) continue;  // pad
+                if (a.gout) a.gout[x] = g[i];
+                a.master[x] = th[i];
+                a.exp_avg[x] = mm[i];
+                a.exp_avg_sq[x] = vv[i];
+                const uint16_t b = ss::f32_to_bf16(th[i]);
+                a.shards[x] = b;
+                const int sl = e.param - a.param_base;
+                const int64_t kx = e.param_off + (x - e.packed_off);
+                for (int j = 0; j < a.n_out; ++j)
+                    static_cast<uint16_t*>(tab.p[goff + j * a.w + sl])[kx] = b;
+            }
+        }
+    }
+    const int nkey = __shfl_down_sync(0xFFFFFFFFu, key, 1);
+    const int pkey = __shfl_up_sync(0xFFFFFFFFu, key, 1);
+    uint4 nx;
+    nx.x = __shfl_down_sync(0xFFFFFFFFu, p.x, 1);
+    nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
+    nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
+    nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
+    if (key >= 0) {
+        const bool same_next = lane < 31 && nkey == key;
+        const bool same_prev = lane > 0 && pkey == key;
+        for (int j = 0; j < a.n_out; ++j) {
+            unsigned char* ob = reinterpret_cast<unsigned char*>(static_cast<uint16_t*>(tab.p[j * a.w + slot]) + k);
+            const int sh = (int)(reinterpret_cast<uintptr_t>(ob) & 15u);
+            if (sh == 0) {
+                ss::st_stream_u4(ob, p);
+                continue;
+            }
+            unsigned char* blk = ob - sh + 16;  // the aligned block after this vector's start
+            const uint4 v = ss::realign16(p, nx, 16 - sh);
+            if (same_next)
+                ss::st_stream_u4(blk, v);
+            else
+                st_bytes(blk, v, 0, sh);
+            if (!same_prev) st_bytes(blk - 16, ss::realign16(p, p, 16 - sh), sh, 16);
+        }
+    }
+    if (q >= nvec && q < nvec + 16) {
+        const int i = (int)(q - nvec);
+        if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
+            const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
+            const int64_t B = x / ss::kMapBlock;
+            int m = __ldg(pm_block + B);
+            ss::PmEntry e = pm[m];
+            locate(pm, pm_block, B, x, m, e);
+            if (x >= e.packed_off && x < e.packed_off + e.len)
+                step_scalar<false>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
+        }
+    }
+}
+
+using FlatAnyKern = void (*)(const ss::PmEntry*, const int*, int, int64_t, int64_t, EdgeElems,
+                             StepArgs, PtrTab);
+
+FlatAnyKern pick_flat_any(int N) {
+    switch (N) {
+        case 2: return fused_step_flat_any_kernel<2>;
+        case 3: return fused_step_flat_any_kernel<3>;
+        case 4: return fused_step_flat_any_kernel<4>;
+        case 5: return fused_step_flat_any_kernel<5>;
+        case 6: return fused_step_flat_any_kernel<6>;
+        case 7: return fused_step_flat_any_kernel<7>;
+        case 8: return fused_step_flat_any_kernel<8>;
+        default: return fused_step_flat_any_kernel<0>;
     }
 }
 
@@ -653,6 +820,38 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             int rc = ss::check_launch();
             if (rc) return rc;
         }
+        return SS_OK;
+    }
+    if (!unpacked && pb - pa <= wmax) {
+        // packed gradients, any alignment: the flat form with per-lane
+        // realigned output stores; whole vectors [lo8, hi8), the edges one by
+        // one
+        if (hi <= lo || plan->pm.empty()) return SS_OK;
+        fill(pa, pb);
+        const int64_t lo8 = (lo + 7) / 8 * 8, hi8 = hi / 8 * 8;
+        EdgeElems ed;
+        int64_t nvec = 0;
+        if (lo8 <= hi8) {
+            nvec = (hi8 - lo8) / 8;
+            ed = EdgeElems{lo, hi8, (int)(lo8 - lo), (int)(hi - hi8)};
+        } else {  // the range lies inside one 8-element vector
+            ed = EdgeElems{lo, hi, (int)(hi - lo), 0};
+        }
+        const EdgeElems none{0, 0, 0, 0};
+        FlatAnyKern ff = pick_flat_any(N);
+        const int M = (int)plan->pm.size();
+        constexpr int64_t kChunk = (int64_t)0x7FFFFFF0 * kThreads;  // vectors per launch
+        int64_t v0 = 0;
+        do {
+            const int64_t cnt = nvec - v0 < kChunk ? nvec - v0 : kChunk;
+            const bool last = v0 + cnt >= nvec;
+            const int64_t threads = cnt + (last ? 16 : 0);
+            ff<<<(unsigned)((threads + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+                plan->d_pm, plan->d_pm_block, M, lo8 + 8 * v0, cnt, last ? ed : none, a, tab);
+            int rc = ss::check_launch();
+            if (rc) return rc;
+            v0 += cnt;
+        } while (v0 < nvec);
         return SS_OK;
     }
     if (pb - pa <= wmax) {

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.gpu_common import Setup, guarded, guards_intact
+from tests.gpu_common import SENTINEL_BF16, Setup, guarded, guards_intact
 from tests.helpers import check_adamw_state, check_bf16_params, to_np
 
 pytestmark = pytest.mark.gpu
@@ -154,6 +154,54 @@ def test_sharded_step_windows_and_groups(ss):
     for other in results[1:]:
         for x, y in zip(results[0], other):
             np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+@pytest.mark.parametrize("kind", [W.FLAT_ORIG_FALSE, W.FLAT_ORIG_TRUE, W.PER_PARAM_DIM0])
+def test_sharded_step_groups_inside_one_vector(ss, kind):
+    # one group per tiny parameter at N = 2: group ranges such as [10, 12) lie
+    # inside one 8-element packed vector, others start or end mid-vector, so
+    # the flat kernel's edge elements and its whole misaligned vectors both run
+    shapes = [(3,), (5,), (1,), (2,), (700,), (9,), (13,), (8,), (31,)]
+    ps = W.ParamSet([f"q{i}" for i in range(len(shapes))], shapes, [1, 1, 1, 1, 1, 2, 1, 1], 2,
+                    kind, torch.bfloat16, seed=17)
+    su = Setup(ss, ps)
+    N, n = su.N, len(su.params)
+    grads = [[g.cuda() for g in rank] for rank in W.make_rank_grads(ps)]
+    packed = []
+    for r in range(N):
+        b = torch.empty(su.total, dtype=torch.bfloat16, device="cuda")
+        ss.fsdp_pack(su.plan, grads[r], b)
+        packed.append(b)
+    results, wholes, firsts = [], [], []
+    for mode in ("two_calls", "one_pass"):
+        shards, master, m, v = _state(ss, su)
+        red = torch.zeros(su.total, device="cuda")
+        outs = []
+        for _ in range(2):
+            for p in su.params:
+                o, w = guarded(p.numel() + 1, torch.bfloat16)
+                outs.append(o[1:])          # 2 bytes past a 16-byte boundary
+                wholes.append(w)
+                firsts.append(o[:1])        # the element before: never written
+        for step in (1, 2):
+            hp = ss.adamw_params(step=step, **_hp(step))
+            for g in range(len(ps.groups)):
+                if mode == "two_calls":
+                    ss.fsdp_reduce_scatter_adamw(su.plan, packed, master, m, v, shards, hp, red,
+                                                 group=g)
+                    ss.fsdp_all_gather_unpack(su.plan, shards, outs, n_out=2, group=g)
+                else:
+                    ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_grads=packed,
+                                         params_out=outs, n_out=2, reduced_grad_out=red, group=g)
+        torch.cuda.synchronize()
+        results.append([to_np(t) for t in [shards, master, m, v, red] + outs])
+    assert all(guards_intact(w) for w in wholes)
+    assert all(int(to_np(f).view(np.uint16)[0]) == SENTINEL_BF16 for f in firsts)
+    for x, y in zip(*results):
+        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+    for j in range(2):
+        for i in range(n):
+            assert results[1][5 + j * n + i].size == su.params[i].numel()
 
 
 def test_sharded_step_state_against_oracle(ss):
