@@ -178,12 +178,6 @@ void build_packed_tiles(ss_plan* p) {
             p->packed_tiles.push_back(p->data_tiles[t]);
     }
     while (g < p->G) p->group_ptile[++g] = (int64_t)p->packed_tiles.size();
-    p->packed_tiles_ext.resize(p->packed_tiles.size());
-    for (size_t t = 0; t < p->packed_tiles.size(); ++t) {
-        const ss::Seg& sg = p->data[p->packed_tiles[t].seg];
-        p->packed_tiles_ext[t] = ss::PmEntry{sg.packed_off, sg.param_off, sg.len, sg.param,
-                                             p->packed_tiles[t].idx};
-    }
 }
 
 // The packed segment map: data segments by packed offset, and for every
@@ -249,14 +243,6 @@ int upload(ss_plan* p) {
     if (!p->packed_tiles.empty()) {
         e = cudaMemcpy(p->d_packed_tiles, p->packed_tiles.data(),
                        p->packed_tiles.size() * sizeof(ss::Tile), cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) return ss::cuda_fail(e);
-    }
-    e = cudaMalloc(&p->d_packed_tiles_ext, std::max<size_t>(p->packed_tiles_ext.size(), 1) *
-                                               sizeof(ss::PmEntry));
-    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
-    if (!p->packed_tiles_ext.empty()) {
-        e = cudaMemcpy(p->d_packed_tiles_ext, p->packed_tiles_ext.data(),
-                       p->packed_tiles_ext.size() * sizeof(ss::PmEntry), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return ss::cuda_fail(e);
     }
     e = cudaMalloc(&p->d_pm, std::max<size_t>(p->pm.size(), 1) * sizeof(ss::PmEntry));
@@ -461,7 +447,6 @@ void fsdp_plan_destroy(ss_plan* p) {
     if (p->d_data_tiles) cudaFree(p->d_data_tiles);
     if (p->d_zero_tiles) cudaFree(p->d_zero_tiles);
     if (p->d_packed_tiles) cudaFree(p->d_packed_tiles);
-    if (p->d_packed_tiles_ext) cudaFree(p->d_packed_tiles_ext);
     if (p->d_pm) cudaFree(p->d_pm);
     if (p->d_pm_block) cudaFree(p->d_pm_block);
     delete p;
@@ -529,16 +514,6 @@ int fsdp_plan_validate(const ss_plan* p) {
             if (tl.seg < 0 || (size_t)tl.seg >= p->data.size()) return SS_EINVAL;
             if (p->param_group[p->data[tl.seg].param] != g) return SS_EINVAL;
         }
-    // packed-order tiles with their segment inline: the same tiles, same fields
-    if (p->packed_tiles_ext.size() != p->packed_tiles.size()) return SS_EINVAL;
-    for (size_t t = 0; t < p->packed_tiles.size(); ++t) {
-        const ss::Tile& tl = p->packed_tiles[t];
-        const ss::Seg& sg = p->data[tl.seg];
-        const ss::PmEntry& x = p->packed_tiles_ext[t];
-        if (x.packed_off != sg.packed_off || x.param_off != sg.param_off || x.len != sg.len ||
-            x.param != sg.param || x.reserved != tl.idx)
-            return SS_EINVAL;
-    }
     // packed segment map: every data segment once, by strictly increasing
     // offset; pm_block[B] is the last segment starting at or before block B
     const size_t M = p->pm.size();

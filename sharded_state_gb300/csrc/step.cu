@@ -135,34 +135,36 @@ __device__ __forceinline__ void adam_compute(const StepArgs& a, const float (&s)
     for (int e = 0; e < 8; ++e) adamw_elem(g[e], th[e], mm[e], vv[e], a.c);
 }
 
-__device__ __forceinline__ uint4 pack_bf16x8(const float (&th)[8]) {
-    uint4 p;
-    p.x = ss::pack_bf16x2(th[0], th[1]);
-    p.y = ss::pack_bf16x2(th[2], th[3]);
-    p.z = ss::pack_bf16x2(th[4], th[5]);
-    p.w = ss::pack_bf16x2(th[6], th[7]);
-    return p;
-}
-
 // The rank sum s of packed elements f..f+7 divided by n, AdamW on the state
 // loaded as t/m/v, state and shard stores (and the reduced gradient when
 // a.gout is set); returns the new bf16 parameter vector.
 __device__ __forceinline__ uint4 adam_vec(const StepArgs& a, int64_t f, const float (&s)[8], int n,
                                           float4 t0, float4 t1, float4 m0, float4 m1, float4 v0,
                                           float4 v1) {
-    float g[8], th[8], mm[8], vv[8];
-    adam_compute(a, s, n, t0, t1, m0, m1, v0, v1, g, th, mm, vv);
+    const float fN = (float)n;
+    float g[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[e] = __fdiv_rn(s[e], fN);
     if (a.gout) {
         ss::st_stream_f4(a.gout + f, make_float4(g[0], g[1], g[2], g[3]));
         ss::st_stream_f4(a.gout + f + 4, make_float4(g[4], g[5], g[6], g[7]));
     }
+    float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+    float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) adamw_elem(g[e], th[e], mm[e], vv[e], a.c);
     ss::st_stream_f4(a.master + f, make_float4(th[0], th[1], th[2], th[3]));
     ss::st_stream_f4(a.master + f + 4, make_float4(th[4], th[5], th[6], th[7]));
     ss::st_stream_f4(a.exp_avg + f, make_float4(mm[0], mm[1], mm[2], mm[3]));
     ss::st_stream_f4(a.exp_avg + f + 4, make_float4(mm[4], mm[5], mm[6], mm[7]));
     ss::st_stream_f4(a.exp_avg_sq + f, make_float4(vv[0], vv[1], vv[2], vv[3]));
     ss::st_stream_f4(a.exp_avg_sq + f + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
-    const uint4 p = pack_bf16x8(th);
+    uint4 p;
+    p.x = ss::pack_bf16x2(th[0], th[1]);
+    p.y = ss::pack_bf16x2(th[2], th[3]);
+    p.z = ss::pack_bf16x2(th[4], th[5]);
+    p.w = ss::pack_bf16x2(th[6], th[7]);
     ss::st_stream_u4(a.shards + f, p);
     return p;
 }
@@ -377,19 +379,11 @@ static_assert(kSub * kThreads * 8 * 2 == ss::kTileBytes, "tile split");
 template <int NR, bool UNPACKED, bool GEN>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
-                  const ss::PmEntry* __restrict__ ext, StepArgs a, PtrTab tab) {
+                  StepArgs a, PtrTab tab) {
     constexpr int64_t T = ss::kTileBytes / 2;
-    // The tile and its segment: one 32-byte load when the packed-order table
-    // with the segment inline is given (ext), else the tile, then its segment.
-    ss::PmEntry sg;
-    if (ext) {
-        sg = ext[t_lo + blockIdx.x];
-    } else {
-        const ss::Tile tl = tiles[t_lo + blockIdx.x];
-        const ss::Seg x = segs[tl.seg];
-        sg = ss::PmEntry{x.packed_off, x.param_off, x.len, x.param, tl.idx};
-    }
-    const int64_t tile_idx = sg.reserved;
+    const ss::Tile tl = tiles[t_lo + blockIdx.x];
+    const ss::Seg sg = segs[tl.seg];
+    const int64_t tile_idx = tl.idx;
     const int64_t off = tile_idx * T;
     const int64_t len = sg.len - off < T ? sg.len - off : T;
     constexpr int64_t kPart = T / kSub;  // elements of this CTA's part of the tile
@@ -454,24 +448,39 @@ fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Se
         step_scalar<UNPACKED>(a, tab, slot, fs + e, ks + e);
 }
 
+// The plan's packed segment map on the device.
+struct SegMap {
+    const ss::PmEntry* __restrict__ pm;  // data segments by packed offset
+    const int* __restrict__ pm_block;    // per kMapBlock block: last entry at or before it
+    int M;                               // entries (where a kernel needs them)
+};
+
 // The map entry of packed element f in block B = f / kMapBlock, given the
 // block's first candidate m = pm_block[B] and e = pm[m]: unless e's segment
 // holds f, a binary search over the entries that start inside the block for
 // the last one that starts at or before f (m stays pm_block[B] when none
 // does: f lies before the first segment).  m and e are updated.
-__device__ __forceinline__ void locate(const ss::PmEntry* __restrict__ pm,
-                                       const int* __restrict__ pm_block, int64_t B, int64_t f,
-                                       int& m, ss::PmEntry& e) {
+__device__ __forceinline__ void locate(const SegMap& mp, int64_t B, int64_t f, int& m,
+                                       ss::PmEntry& e) {
     if (f >= e.packed_off && f < e.packed_off + e.len) return;
-    int hi = __ldg(pm_block + B + 1);
+    int hi = __ldg(mp.pm_block + B + 1);
     while (m < hi) {
         const int mid = (m + hi + 1) >> 1;
-        if (pm[mid].packed_off <= f)
+        if (mp.pm[mid].packed_off <= f)
             m = mid;
         else
             hi = mid - 1;
     }
-    e = pm[m];
+    e = mp.pm[m];
+}
+
+// The map entry of packed element f (its index in m).
+__device__ __forceinline__ ss::PmEntry lookup(const SegMap& mp, int64_t f, int& m) {
+    const int64_t B = f / ss::kMapBlock;
+    m = __ldg(mp.pm_block + B);
+    ss::PmEntry e = mp.pm[m];
+    locate(mp, B, f, m, e);
+    return e;
 }
 
 // Flat form of the one-pass step, for plans whose runs are all whole 16-byte
@@ -505,7 +514,17 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
     const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
     ss::PmEntry e = pm[m];
-    locate(pm, pm_block, B, f, m, e);
+    if (f < e.packed_off || f >= e.packed_off + e.len) {  // a segment starts inside the block
+        int hi = __ldg(pm_block + B + 1);
+        while (m < hi) {
+            const int mid = (m + hi + 1) >> 1;
+            if (pm[mid].packed_off <= f)
+                m = mid;
+            else
+                hi = mid - 1;
+        }
+        e = pm[m];
+    }
     const int64_t rel = f - e.packed_off;
     if (rel < 0 || rel >= e.len) return;  // a pad vector
     const int slot = e.param - a.param_base;
@@ -541,6 +560,34 @@ FlatKern pick_flat(int N) {
     }
 }
 
+// The n_out per-parameter outputs of one vector p at index k of parameter
+// `slot` (output j at tab[goff + j*w + slot]), sh bytes past a 16-byte
+// boundary: the aligned block after the vector's start is written whole
+// (this vector's last sh bytes, then the first 16 - sh of nx, the next
+// vector of the same run) when same_next, else only this vector's bytes of
+// it; unless same_prev (the previous vector of the run writes the block
+// before whole), the vector's first 16 - sh bytes go into the block before.
+__device__ __forceinline__ void store_outputs_lane(const StepArgs& a, const PtrTab& tab, int goff,
+                                                   int slot, int64_t k, uint4 p, uint4 nx,
+                                                   bool same_next, bool same_prev) {
+    for (int j = 0; j < a.n_out; ++j) {
+        unsigned char* ob =
+            reinterpret_cast<unsigned char*>(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k);
+        const int sh = (int)(reinterpret_cast<uintptr_t>(ob) & 15u);
+        if (sh == 0) {
+            ss::st_stream_u4(ob, p);
+            continue;
+        }
+        unsigned char* blk = ob - sh + 16;  // the aligned block after this vector's start
+        const uint4 v = ss::realign16(p, nx, 16 - sh);
+        if (same_next)
+            ss::st_stream_u4(blk, v);
+        else
+            st_bytes(blk, v, 0, sh);
+        if (!same_prev) st_bytes(blk - 16, ss::realign16(p, p, 16 - sh), sh, 16);
+    }
+}
+
 // The call range's elements outside whole packed vectors: [h0, h0 + nh) at
 // its start and [t0, t0 + nt) at its end, fewer than 8 each.
 struct EdgeElems {
@@ -568,6 +615,7 @@ template <int NR>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
                            int M, int64_t vbeg, int64_t nvec, EdgeElems ed, StepArgs a, PtrTab tab) {
+    const SegMap mp{pm, pm_block, M};
     const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const int n = NR > 0 ? NR : a.N;
@@ -578,7 +626,7 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
     if (q < nvec) {
         const int64_t f = vbeg + 8 * q;
         const int64_t B = f / ss::kMapBlock;
-        int m = __ldg(pm_block + B);
+        int m = __ldg(mp.pm_block + B);
         uint4 w[kMaxVec];
 #pragma unroll
         for (int r = 0; r < kMaxVec; ++r)
@@ -586,8 +634,8 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
         const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
         const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
-        ss::PmEntry e = pm[m];
-        locate(pm, pm_block, B, f, m, e);
+        ss::PmEntry e = mp.pm[m];
+        locate(mp, B, f, m, e);
         float s[8];
         sum_ranks<NR>(w, n, s);
         for (int r = kMaxVec; NR == 0 && r < n; ++r)
@@ -605,9 +653,9 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int64_t x = f + i;
-                while (c + 1 < M && pm[c + 1].packed_off <= x) {
+                while (c + 1 < mp.M && mp.pm[c + 1].packed_off <= x) {
                     ++c;
-                    e = pm[c];
+                    e = mp.pm[c];
                 }
                 if (x < e.packed_off || x >= e.packed_off + e.len) continue;  // pad
                 if (a.gout) a.gout[x] = g[i];
@@ -630,36 +678,156 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
     nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
     nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
     nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
-    if (key >= 0) {
-        const bool same_next = lane < 31 && nkey == key;
-        const bool same_prev = lane > 0 && pkey == key;
-        for (int j = 0; j < a.n_out; ++j) {
-            unsigned char* ob = reinterpret_cast<unsigned char*>(static_cast<uint16_t*>(tab.p[j * a.w + slot]) + k);
-            const int sh = (int)(reinterpret_cast<uintptr_t>(ob) & 15u);
-            if (sh == 0) {
-                ss::st_stream_u4(ob, p);
-                continue;
-            }
-            unsigned char* blk = ob - sh + 16;  // the aligned block after this vector's start
-            const uint4 v = ss::realign16(p, nx, 16 - sh);
-            if (same_next)
-                ss::st_stream_u4(blk, v);
-            else
-                st_bytes(blk, v, 0, sh);
-            if (!same_prev) st_bytes(blk - 16, ss::realign16(p, p, 16 - sh), sh, 16);
-        }
-    }
+    if (key >= 0) store_outputs_lane(a, tab, 0, slot, k, p, nx, lane < 31 && nkey == key,
+                                     lane > 0 && pkey == key);
     if (q >= nvec && q < nvec + 16) {
         const int i = (int)(q - nvec);
         if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
             const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
-            const int64_t B = x / ss::kMapBlock;
-            int m = __ldg(pm_block + B);
-            ss::PmEntry e = pm[m];
-            locate(pm, pm_block, B, x, m, e);
+            int m;
+            const ss::PmEntry e = lookup(mp, x, m);
             if (x >= e.packed_off && x < e.packed_off + e.len)
                 step_scalar<false>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
         }
+    }
+}
+
+// Flat form of the one-pass step with per-parameter gradients (fused
+// copy-in) at any alignment.  Each warp takes 31 consecutive 8-aligned packed
+// vectors, q = 31 * warp + lane; lane 31 looks up and loads the next warp's
+// first vector without computing it.  A lane whose vector lies inside one
+// segment loads, per rank, the one aligned 16-byte block that holds the
+// vector's first bytes; when the next lane's vector is the next one of the
+// same segment, that lane's block is this vector's second block and arrives
+// by a shuffle, so a warp inside one segment reads each gradient block once.
+// Only a lane at a segment end loads its second block itself, after the
+// shuffle.  Both blocks hold bytes of the vector, so no load leaves the
+// gradient tensor's 16-byte blocks.  The state loads depend on f alone and go
+// out before the lookup.  A vector that meets a segment end runs element by
+// element; the range's edge elements run on lanes 0..15 of one extra warp.
+// Outputs as in fused_step_flat_any_kernel, lane 31 storing nothing.
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 3)
+fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
+                              int64_t vbeg, int64_t nvec, int64_t nwarps, EdgeElems ed, StepArgs a,
+                              PtrTab tab) {
+    const SegMap mp{pm, pm_block, 0};
+    constexpr int kVpw = 31;  // vectors per warp
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t q = gw * kVpw + lane;
+    const bool has = gw < nwarps && q < nvec;
+    const bool computes = has && lane < kVpw;
+    const int n = NR > 0 ? NR : a.N;
+    const int nr = n < kMaxVec ? n : kMaxVec;
+    const int64_t f = vbeg + 8 * q;
+    const int goff = n * a.w;
+    int key = -1, slot = 0, m = 0;
+    int64_t k = 0;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 t0 = z4, t1 = z4, m0 = z4, m1 = z4, v0 = z4, v1 = z4;
+    if (has) {
+        const int64_t B = f / ss::kMapBlock;
+        m = __ldg(mp.pm_block + B);
+        if (computes) {
+            t0 = ss::ld_rw_f4(a.master + f);
+            t1 = ss::ld_rw_f4(a.master + f + 4);
+            m0 = ss::ld_rw_f4(a.exp_avg + f);
+            m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+            v0 = ss::ld_rw_f4(a.exp_avg_sq + f);
+            v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+        }
+        ss::PmEntry e = mp.pm[m];
+        locate(mp, B, f, m, e);
+        if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
+            key = m;
+            slot = e.param - a.param_base;
+            k = e.param_off + (f - e.packed_off);
+        }
+    }
+    const int nkey = __shfl_down_sync(0xFFFFFFFFu, key, 1);
+    const int pkey = __shfl_up_sync(0xFFFFFFFFu, key, 1);
+    const bool gnext = lane < 31 && key >= 0 && nkey == key;
+    uint4 w[kMaxVec];
+    uint32_t shs = 0;  // sh_r / 2 of every rank, 3 bits each
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r) {
+        if (r < nr) {
+            w[r] = make_uint4(0, 0, 0, 0);
+            if (key >= 0) {
+                const unsigned char* g = reinterpret_cast<const unsigned char*>(
+                    static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k);
+                const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
+                shs |= (uint32_t)(sh >> 1) << (3 * r);
+                w[r] = ss::ld_stream_u4(g - sh);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r) {
+        if (r < nr) {
+            uint4 nb;
+            nb.x = __shfl_down_sync(0xFFFFFFFFu, w[r].x, 1);
+            nb.y = __shfl_down_sync(0xFFFFFFFFu, w[r].y, 1);
+            nb.z = __shfl_down_sync(0xFFFFFFFFu, w[r].z, 1);
+            nb.w = __shfl_down_sync(0xFFFFFFFFu, w[r].w, 1);
+            const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
+            if (sh && computes && key >= 0 && !gnext)
+                nb = ss::ld_stream_u4(reinterpret_cast<const unsigned char*>(
+                                          static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k) -
+                                      sh + 16);
+            if (sh) w[r] = ss::realign16(w[r], nb, sh);
+        }
+    }
+    uint4 p = make_uint4(0, 0, 0, 0);
+    if (computes && key >= 0) {
+        float s[8];
+        sum_ranks<NR>(w, n, s);
+        for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
+            add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
+        p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
+    } else if (computes) {  // the vector meets a segment end: element by element
+        for (int i = 0; i < 8; ++i) {
+            const int64_t x = f + i;
+            int c;
+            const ss::PmEntry e = lookup(mp, x, c);
+            if (x >= e.packed_off && x < e.packed_off + e.len)
+                step_scalar<true>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
+        }
+    }
+    uint4 nx;
+    nx.x = __shfl_down_sync(0xFFFFFFFFu, p.x, 1);
+    nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
+    nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
+    nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
+    if (computes && key >= 0)
+        store_outputs_lane(a, tab, goff, slot, k, p, nx, lane < kVpw - 1 && nkey == key,
+                           lane > 0 && pkey == key);
+    if (gw == nwarps && lane < 16) {
+        const int i = lane;
+        if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
+            const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
+            int c;
+            const ss::PmEntry e = lookup(mp, x, c);
+            if (x >= e.packed_off && x < e.packed_off + e.len)
+                step_scalar<true>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
+        }
+    }
+}
+
+using FlatCopyinKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t,
+                                EdgeElems, StepArgs, PtrTab);
+
+FlatCopyinKern pick_flat_copyin(int N) {
+    switch (N) {
+        case 2: return fused_step_flat_copyin_kernel<2>;
+        case 3: return fused_step_flat_copyin_kernel<3>;
+        case 4: return fused_step_flat_copyin_kernel<4>;
+        case 5: return fused_step_flat_copyin_kernel<5>;
+        case 6: return fused_step_flat_copyin_kernel<6>;
+        case 7: return fused_step_flat_copyin_kernel<7>;
+        case 8: return fused_step_flat_copyin_kernel<8>;
+        default: return fused_step_flat_copyin_kernel<0>;
     }
 }
 
@@ -679,8 +847,7 @@ FlatAnyKern pick_flat_any(int N) {
     }
 }
 
-using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, const ss::PmEntry*, StepArgs,
-                     PtrTab);
+using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
 
 template <int NR, bool U>
 Kern pick_gen(bool gen) {
@@ -783,11 +950,10 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     PtrTab tab;
     constexpr int64_t kMaxGrid = (int64_t)1 << 30;
-    auto launch = [&](const ss::Tile* tiles, const ss::PmEntry* ext, int64_t t_lo,
-                      int64_t t_hi) -> int {
+    auto launch = [&](const ss::Tile* tiles, int64_t t_lo, int64_t t_hi) -> int {
         for (int64_t t = t_lo; t < t_hi; t += kMaxGrid) {
             const int64_t cnt = t_hi - t < kMaxGrid ? t_hi - t : kMaxGrid;
-            fn<<<dim3((unsigned)cnt, kSub), kThreads, 0, st>>>(tiles, t, plan->d_data, ext, a, tab);
+            fn<<<dim3((unsigned)cnt, kSub), kThreads, 0, st>>>(tiles, t, plan->d_data, a, tab);
             int rc = ss::check_launch();
             if (rc) return rc;
         }
@@ -822,8 +988,8 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         }
         return SS_OK;
     }
-    if (!unpacked && pb - pa <= wmax) {
-        // packed gradients, any alignment: the flat form with per-lane
+    if (pb - pa <= wmax) {
+        // any alignment, one pointer table: the flat forms with per-lane
         // realigned output stores; whole vectors [lo8, hi8), the edges one by
         // one
         if (hi <= lo || plan->pm.empty()) return SS_OK;
@@ -838,8 +1004,27 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             ed = EdgeElems{lo, hi, (int)(hi - lo), 0};
         }
         const EdgeElems none{0, 0, 0, 0};
+        if (unpacked) {
+            // 31 vectors per warp and one extra warp for the edges
+            FlatCopyinKern fc = pick_flat_copyin(N);
+            const int64_t nw = (nvec + 30) / 31;
+            constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
+            int64_t w0 = 0;
+            do {
+                const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
+                const bool last = w0 + cw >= nw;
+                const int64_t cv = last ? nvec - 31 * w0 : 31 * cw;
+                const int64_t warps = cw + (last ? 1 : 0);
+                fc<<<(unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
+                    plan->d_pm, plan->d_pm_block, lo8 + 8 * 31 * w0, cv, cw, last ? ed : none, a,
+                    tab);
+                int rc = ss::check_launch();
+                if (rc) return rc;
+                w0 += cw;
+            } while (w0 < nw);
+            return SS_OK;
+        }
         FlatAnyKern ff = pick_flat_any(N);
-        const int M = (int)plan->pm.size();
         constexpr int64_t kChunk = (int64_t)0x7FFFFFF0 * kThreads;  // vectors per launch
         int64_t v0 = 0;
         do {
@@ -847,29 +1032,20 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             const bool last = v0 + cnt >= nvec;
             const int64_t threads = cnt + (last ? 16 : 0);
             ff<<<(unsigned)((threads + kThreads - 1) / kThreads), kThreads, 0, st>>>(
-                plan->d_pm, plan->d_pm_block, M, lo8 + 8 * v0, cnt, last ? ed : none, a, tab);
+                plan->d_pm, plan->d_pm_block, (int)plan->pm.size(), lo8 + 8 * v0, cnt,
+                last ? ed : none, a, tab);
             int rc = ss::check_launch();
             if (rc) return rc;
             v0 += cnt;
         } while (v0 < nvec);
         return SS_OK;
     }
-    if (pb - pa <= wmax) {
-        // every parameter's pointers fit one table: walk the tiles in packed
-        // order, so consecutive CTAs stream the gradient / state / shard
-        // buffers front to back
-        fill(pa, pb);
-        const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
-        return launch(plan->d_packed_tiles, plan->d_packed_tiles_ext, plan->group_ptile[ga],
-                      plan->group_ptile[gb]);
-    }
     for (int wa = pa; wa < pb; wa += wmax) {
         const int wb = wa + wmax < pb ? wa + wmax : pb;
         const int s_lo = plan->param_seg[wa], s_hi = plan->param_seg[wb];
         if (s_hi <= s_lo) continue;
         fill(wa, wb);
-        int rc = launch(plan->d_data_tiles, nullptr, plan->data_seg_tile[s_lo],
-                        plan->data_seg_tile[s_hi]);
+        int rc = launch(plan->d_data_tiles, plan->data_seg_tile[s_lo], plan->data_seg_tile[s_hi]);
         if (rc) return rc;
     }
     return SS_OK;

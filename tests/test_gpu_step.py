@@ -160,7 +160,8 @@ def test_sharded_step_windows_and_groups(ss):
 def test_sharded_step_groups_inside_one_vector(ss, kind):
     # one group per tiny parameter at N = 2: group ranges such as [10, 12) lie
     # inside one 8-element packed vector, others start or end mid-vector, so
-    # the flat kernel's edge elements and its whole misaligned vectors both run
+    # the flat kernels' edge elements and their whole misaligned vectors both
+    # run, with packed gradients and with the fused copy-in
     shapes = [(3,), (5,), (1,), (2,), (700,), (9,), (13,), (8,), (31,)]
     ps = W.ParamSet([f"q{i}" for i in range(len(shapes))], shapes, [1, 1, 1, 1, 1, 2, 1, 1], 2,
                     kind, torch.bfloat16, seed=17)
@@ -172,8 +173,17 @@ def test_sharded_step_groups_inside_one_vector(ss, kind):
         b = torch.empty(su.total, dtype=torch.bfloat16, device="cuda")
         ss.fsdp_pack(su.plan, grads[r], b)
         packed.append(b)
+    # the same gradients as per-parameter views, each 2 * (r + i) mod 16 bytes
+    # past a 16-byte boundary, for the fused copy-in
+    views = []
+    for r in range(N):
+        for i, g in enumerate(grads[r]):
+            o, _ = guarded(g.numel() + 8, torch.bfloat16)
+            v = o[(r + i) % 8:(r + i) % 8 + g.numel()]
+            v.copy_(g.view(-1))
+            views.append(v)
     results, wholes, firsts = [], [], []
-    for mode in ("two_calls", "one_pass"):
+    for mode in ("two_calls", "one_pass", "copy_in"):
         shards, master, m, v = _state(ss, su)
         red = torch.zeros(su.total, device="cuda")
         outs = []
@@ -190,15 +200,19 @@ def test_sharded_step_groups_inside_one_vector(ss, kind):
                     ss.fsdp_reduce_scatter_adamw(su.plan, packed, master, m, v, shards, hp, red,
                                                  group=g)
                     ss.fsdp_all_gather_unpack(su.plan, shards, outs, n_out=2, group=g)
-                else:
+                elif mode == "one_pass":
                     ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_grads=packed,
+                                         params_out=outs, n_out=2, reduced_grad_out=red, group=g)
+                else:
+                    ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp, rank_param_grads=views,
                                          params_out=outs, n_out=2, reduced_grad_out=red, group=g)
         torch.cuda.synchronize()
         results.append([to_np(t) for t in [shards, master, m, v, red] + outs])
     assert all(guards_intact(w) for w in wholes)
     assert all(int(to_np(f).view(np.uint16)[0]) == SENTINEL_BF16 for f in firsts)
-    for x, y in zip(*results):
-        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+    for other in results[1:]:
+        for x, y in zip(results[0], other):
+            np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
     for j in range(2):
         for i in range(n):
             assert results[1][5 + j * n + i].size == su.params[i].numel()
