@@ -43,6 +43,11 @@ __device__ __forceinline__ float4 ld_rw_f4(const float* p) {
     return r;
 }
 
+// Ask L2 for the line holding p ahead of its load (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Streaming 128-bit stores (evict-first).
 __device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
     asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),

@@ -39,6 +39,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTab = 2048;
 constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
+constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the flat copy-in
+constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) it keeps
 
 struct RankPtrs {
     const void* p[SS_MAX_WORLD];
@@ -693,42 +695,46 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
 }
 
 // Flat form of the one-pass step with per-parameter gradients (fused
-// copy-in) at any alignment.  Each warp takes 31 consecutive 8-aligned packed
-// vectors, q = 31 * warp + lane; lane 31 looks up and loads the next warp's
-// first vector without computing it.  A lane whose vector lies inside one
-// segment loads, per rank, the one aligned 16-byte block that holds the
-// vector's first bytes; when the next lane's vector is the next one of the
-// same segment, that lane's block is this vector's second block and arrives
-// by a shuffle, so a warp inside one segment reads each gradient block once.
-// Only a lane at a segment end loads its second block itself, after the
-// shuffle.  Both blocks hold bytes of the vector, so no load leaves the
-// gradient tensor's 16-byte blocks.  The state loads depend on f alone and go
-// out before the lookup.  A vector that meets a segment end runs element by
-// element; the range's edge elements run on lanes 0..15 of one extra warp.
+// copy-in) at any alignment.  Warp gw takes `iters` rounds of 31 consecutive
+// 8-aligned packed vectors, round it holding q = 31 * (gw * iters + it) +
+// lane; lane 31 looks up and loads the next round's first vector without
+// computing it.  A lane keeps the segment of its last vector: while the next
+// vector lies inside it, the vector is placed with no lookup, so its
+// gradient loads go out with its state loads; otherwise it looks the segment
+// up in the packed segment map.  A lane whose vector lies inside one segment
+// loads, per rank, the one aligned 16-byte block that holds the vector's
+// first bytes; when the next lane's vector is the next one of the same
+// segment, that lane's block is this vector's second block and arrives by a
+// shuffle, so a warp inside one segment reads each gradient block once.  Only
+// a lane at a segment end loads its second block itself, after the shuffle.
+// Both blocks hold bytes of the vector, so no load leaves the gradient
+// tensor's 16-byte blocks.  A vector that meets a segment end runs element by
+// element; the range's edge elements run on lanes 0..15 of warp nwarps.
 // Outputs as in fused_step_flat_any_kernel, lane 31 storing nothing.
 template <int NR>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
-                              int64_t vbeg, int64_t nvec, int64_t nwarps, EdgeElems ed, StepArgs a,
-                              PtrTab tab) {
+                              int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, EdgeElems ed,
+                              StepArgs a, PtrTab tab) {
     const SegMap mp{pm, pm_block, 0};
-    constexpr int kVpw = 31;  // vectors per warp
+    constexpr int kVpw = 31;  // vectors per warp and round
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    const int64_t q = gw * kVpw + lane;
-    const bool has = gw < nwarps && q < nvec;
-    const bool computes = has && lane < kVpw;
     const int n = NR > 0 ? NR : a.N;
     const int nr = n < kMaxVec ? n : kMaxVec;
-    const int64_t f = vbeg + 8 * q;
     const int goff = n * a.w;
-    int key = -1, slot = 0, m = 0;
-    int64_t k = 0;
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 t0 = z4, t1 = z4, m0 = z4, m1 = z4, v0 = z4, v1 = z4;
-    if (has) {
-        const int64_t B = f / ss::kMapBlock;
-        m = __ldg(mp.pm_block + B);
+    const int64_t fend = vbeg + 8 * nvec;
+    // the segment of this lane's last whole vector: its end, k - f and
+    // parameter slot, and its map index (hkey < 0: none)
+    int64_t hend = 0, hdelta = 0;
+    int hslot = 0, hkey = -1;
+    int64_t f = vbeg + 8 * (gw * iters * kVpw + lane);
+    for (int it = gw < nwarps ? iters : 0; it > 0; --it, f += 8 * kVpw) {
+        if (__shfl_sync(0xFFFFFFFFu, f, 0) >= fend) break;  // the same for the whole warp
+        const bool has = f < fend;
+        const bool computes = has && lane < kVpw;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 t0 = z4, t1 = z4, m0 = z4, m1 = z4, v0 = z4, v1 = z4;
         if (computes) {
             t0 = ss::ld_rw_f4(a.master + f);
             t1 = ss::ld_rw_f4(a.master + f + 4);
@@ -737,85 +743,108 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
             v0 = ss::ld_rw_f4(a.exp_avg_sq + f);
             v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
         }
-        ss::PmEntry e = mp.pm[m];
-        locate(mp, B, f, m, e);
-        if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
-            key = m;
-            slot = e.param - a.param_base;
-            k = e.param_off + (f - e.packed_off);
-        }
-    }
-    const int nkey = __shfl_down_sync(0xFFFFFFFFu, key, 1);
-    const int pkey = __shfl_up_sync(0xFFFFFFFFu, key, 1);
-    const bool gnext = lane < 31 && key >= 0 && nkey == key;
-    uint4 w[kMaxVec];
-    uint32_t shs = 0;  // sh_r / 2 of every rank, 3 bits each
-#pragma unroll
-    for (int r = 0; r < kMaxVec; ++r) {
-        if (r < nr) {
-            w[r] = make_uint4(0, 0, 0, 0);
-            if (key >= 0) {
-                const unsigned char* g = reinterpret_cast<const unsigned char*>(
-                    static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k);
-                const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
-                shs |= (uint32_t)(sh >> 1) << (3 * r);
-                w[r] = ss::ld_stream_u4(g - sh);
+        if (has && (hkey < 0 || f + 8 > hend)) {  // leaves the last segment: look it up
+            int m;
+            const ss::PmEntry e = lookup(mp, f, m);
+            hkey = -1;
+            if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
+                hkey = m;
+                hend = e.packed_off + e.len;
+                hdelta = e.param_off - e.packed_off;
+                hslot = e.param - a.param_base;
             }
         }
-    }
+        const int key = has ? hkey : -1, slot = hslot;
+        const int64_t k = f + hdelta;
+        const int nkey = __shfl_down_sync(0xFFFFFFFFu, key, 1);
+        const int pkey = __shfl_up_sync(0xFFFFFFFFu, key, 1);
+        const bool gnext = lane < 31 && key >= 0 && nkey == key;
+        uint4 w[kMaxVec];
+        uint32_t shs = 0;  // sh_r / 2 of every rank, 3 bits each
 #pragma unroll
-    for (int r = 0; r < kMaxVec; ++r) {
-        if (r < nr) {
-            uint4 nb;
-            nb.x = __shfl_down_sync(0xFFFFFFFFu, w[r].x, 1);
-            nb.y = __shfl_down_sync(0xFFFFFFFFu, w[r].y, 1);
-            nb.z = __shfl_down_sync(0xFFFFFFFFu, w[r].z, 1);
-            nb.w = __shfl_down_sync(0xFFFFFFFFu, w[r].w, 1);
-            const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
-            if (sh && computes && key >= 0 && !gnext)
-                nb = ss::ld_stream_u4(reinterpret_cast<const unsigned char*>(
-                                          static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k) -
-                                      sh + 16);
-            if (sh) w[r] = ss::realign16(w[r], nb, sh);
+        for (int r = 0; r < kMaxVec; ++r) {
+            if (r < nr) {
+                w[r] = make_uint4(0, 0, 0, 0);
+                if (key >= 0) {
+                    const unsigned char* g = reinterpret_cast<const unsigned char*>(
+                        static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k);
+                    const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
+                    shs |= (uint32_t)(sh >> 1) << (3 * r);
+                    w[r] = ss::ld_stream_u4(g - sh);
+                }
+            }
         }
-    }
-    uint4 p = make_uint4(0, 0, 0, 0);
-    if (computes && key >= 0) {
-        float s[8];
-        sum_ranks<NR>(w, n, s);
-        for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
-            add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
-        p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
-    } else if (computes) {  // the vector meets a segment end: element by element
-        for (int i = 0; i < 8; ++i) {
-            const int64_t x = f + i;
-            int c;
-            const ss::PmEntry e = lookup(mp, x, c);
-            if (x >= e.packed_off && x < e.packed_off + e.len)
-                step_scalar<true>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
+        // the lane's next vector, 31 vectors on: its state and (when it stays
+        // in this segment) its first gradient blocks into L2 while this round
+        // computes, so the next round's loads wait for L2 rather than DRAM
+        const int64_t fn = f + 8 * kVpw;
+        if (it > 1 && fn < fend) {
+            if (lane < kVpw) {
+                ss::prefetch_l2(a.master + fn);
+                ss::prefetch_l2(a.exp_avg + fn);
+                ss::prefetch_l2(a.exp_avg_sq + fn);
+            }
+            if (key >= 0 && fn + 8 <= hend) {
+#pragma unroll
+                for (int r = 0; r < kMaxVec; ++r)
+                    if (r < nr) ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + fn + hdelta);
+            }
         }
+#pragma unroll
+        for (int r = 0; r < kMaxVec; ++r) {
+            if (r < nr) {
+                uint4 nb;
+                nb.x = __shfl_down_sync(0xFFFFFFFFu, w[r].x, 1);
+                nb.y = __shfl_down_sync(0xFFFFFFFFu, w[r].y, 1);
+                nb.z = __shfl_down_sync(0xFFFFFFFFu, w[r].z, 1);
+                nb.w = __shfl_down_sync(0xFFFFFFFFu, w[r].w, 1);
+                const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
+                if (sh && computes && key >= 0 && !gnext)
+                    nb = ss::ld_stream_u4(reinterpret_cast<const unsigned char*>(
+                                              static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k) -
+                                          sh + 16);
+                if (sh) w[r] = ss::realign16(w[r], nb, sh);
+            }
+        }
+        uint4 p = make_uint4(0, 0, 0, 0);
+        if (computes && key >= 0) {
+            float s[8];
+            sum_ranks<NR>(w, n, s);
+            for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
+                add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
+            p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
+        } else if (computes) {  // the vector meets a segment end: element by element
+            for (int i = 0; i < 8; ++i) {
+                const int64_t x = f + i;
+                int c;
+                const ss::PmEntry ex = lookup(mp, x, c);
+                if (x >= ex.packed_off && x < ex.packed_off + ex.len)
+                    step_scalar<true>(a, tab, ex.param - a.param_base, x,
+                                      ex.param_off + (x - ex.packed_off));
+            }
+        }
+        uint4 nx;
+        nx.x = __shfl_down_sync(0xFFFFFFFFu, p.x, 1);
+        nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
+        nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
+        nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
+        if (computes && key >= 0)
+            store_outputs_lane(a, tab, goff, slot, k, p, nx, lane < kVpw - 1 && nkey == key,
+                               lane > 0 && pkey == key);
     }
-    uint4 nx;
-    nx.x = __shfl_down_sync(0xFFFFFFFFu, p.x, 1);
-    nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
-    nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
-    nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
-    if (computes && key >= 0)
-        store_outputs_lane(a, tab, goff, slot, k, p, nx, lane < kVpw - 1 && nkey == key,
-                           lane > 0 && pkey == key);
     if (gw == nwarps && lane < 16) {
         const int i = lane;
         if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
             const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
             int c;
-            const ss::PmEntry e = lookup(mp, x, c);
-            if (x >= e.packed_off && x < e.packed_off + e.len)
-                step_scalar<true>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
+            const ss::PmEntry ex = lookup(mp, x, c);
+            if (x >= ex.packed_off && x < ex.packed_off + ex.len)
+                step_scalar<true>(a, tab, ex.param - a.param_base, x, ex.param_off + (x - ex.packed_off));
         }
     }
 }
 
-using FlatCopyinKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t,
+using FlatCopyinKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int,
                                 EdgeElems, StepArgs, PtrTab);
 
 FlatCopyinKern pick_flat_copyin(int N) {
@@ -1005,19 +1034,25 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         }
         const EdgeElems none{0, 0, 0, 0};
         if (unpacked) {
-            // 31 vectors per warp and one extra warp for the edges
+            // rounds of 31 vectors per warp, as many rounds per warp as keep
+            // kCopyinWaves waves of CTAs (at most kCopyinIters), and one
+            // extra warp for the edges
             FlatCopyinKern fc = pick_flat_copyin(N);
-            const int64_t nw = (nvec + 30) / 31;
+            const int64_t per_round = 31 * (int64_t)(kThreads / 32);  // vectors per CTA round
+            int64_t it = nvec / (per_round * kCopyinWaves * 3 * 152);
+            const int iters = (int)(it < 1 ? 1 : it > kCopyinIters ? kCopyinIters : it);
+            const int64_t span = 31 * (int64_t)iters;  // vectors per warp
+            const int64_t nw = (nvec + span - 1) / span;
             constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
             int64_t w0 = 0;
             do {
                 const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
                 const bool last = w0 + cw >= nw;
-                const int64_t cv = last ? nvec - 31 * w0 : 31 * cw;
+                const int64_t cv = last ? nvec - span * w0 : span * cw;
                 const int64_t warps = cw + (last ? 1 : 0);
                 fc<<<(unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
-                    plan->d_pm, plan->d_pm_block, lo8 + 8 * 31 * w0, cv, cw, last ? ed : none, a,
-                    tab);
+                    plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv, cw, iters,
+                    last ? ed : none, a, tab);
                 int rc = ss::check_launch();
                 if (rc) return rc;
                 w0 += cw;
