@@ -41,6 +41,7 @@ constexpr int kTab = 2048;
 constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
 constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the flat copy-in
 constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) it keeps
+constexpr int kFlatRounds = 4;    // most rounds per warp of the aligned flat copy-in
 
 struct RankPtrs {
     const void* p[SS_MAX_WORLD];
@@ -546,6 +547,83 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
         ss::st_stream_u4(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k, p);
 }
 
+// fused_step_flat_kernel with per-parameter gradients (the fused copy-in),
+// in rounds: warp gw takes `iters` rounds of 32 consecutive packed vectors
+// (lane = vector, as in the one-shot form).  The gradient loads wait for the
+// vector's segment, so a lane keeps its segment from one round to the next
+// (no lookup while it stays inside) and, once this round's loads are out,
+// asks L2 for the next round's state and gradient lines: the next round's
+// loads then wait for L2 rather than DRAM while this one computes.
+template <int NR>  // 2..8
+__global__ void __launch_bounds__(kThreads, 3)
+fused_step_flat_rounds_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
+                              int64_t vbeg, int64_t nvec, int iters, StepArgs a, PtrTab tab) {
+    const SegMap mp{pm, pm_block, 0};
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    constexpr int n = NR;
+    const int64_t fend = vbeg + 8 * nvec;
+    int64_t hend = 0, hdelta = 0;  // the lane's last segment: its end and k - f
+    int hslot = -1;                // and parameter slot (-1: none)
+    int64_t f = vbeg + 8 * (gw * iters * 32 + lane);
+    for (int it = iters; it > 0 && f < fend; --it, f += 8 * 32) {
+        const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
+        const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+        const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+        if (hslot < 0 || f + 8 > hend) {  // leaves the last segment: look it up
+            int m;
+            const ss::PmEntry e = lookup(mp, f, m);
+            hslot = -1;
+            if (f >= e.packed_off && f < e.packed_off + e.len) {
+                hend = e.packed_off + e.len;
+                hdelta = e.param_off - e.packed_off;
+                hslot = e.param - a.param_base;
+            }
+        }
+        const int64_t fn = f + 8 * 32;
+        const bool next = it > 1 && fn < fend;
+        if (next) {
+            ss::prefetch_l2(a.master + fn);
+            ss::prefetch_l2(a.exp_avg + fn);
+            ss::prefetch_l2(a.exp_avg_sq + fn);
+        }
+        if (hslot < 0) continue;  // a pad vector
+        const int slot = hslot;
+        const int64_t k = f + hdelta;  // index inside the parameter tensor
+        uint4 w[kMaxVec];
+#pragma unroll
+        for (int r = 0; r < kMaxVec; ++r)
+            if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k);
+        if (next && fn + 8 <= hend) {
+#pragma unroll
+            for (int r = 0; r < kMaxVec; ++r)
+                if (r < n) ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + fn + hdelta);
+        }
+        float s[8];
+        sum_ranks<NR>(w, n, s);
+        const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
+        const int goff = n * a.w;
+        for (int j = 0; j < a.n_out; ++j)
+            ss::st_stream_u4(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k, p);
+    }
+}
+
+using FlatRoundsKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int, StepArgs,
+                                PtrTab);
+
+FlatRoundsKern pick_flat_rounds(int N) {
+    switch (N) {
+        case 2: return fused_step_flat_rounds_kernel<2>;
+        case 3: return fused_step_flat_rounds_kernel<3>;
+        case 4: return fused_step_flat_rounds_kernel<4>;
+        case 5: return fused_step_flat_rounds_kernel<5>;
+        case 6: return fused_step_flat_rounds_kernel<6>;
+        case 7: return fused_step_flat_rounds_kernel<7>;
+        case 8: return fused_step_flat_rounds_kernel<8>;
+        default: return nullptr;  // the one-shot form
+    }
+}
+
 using FlatKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, StepArgs, PtrTab);
 
 template <bool U>
@@ -1006,6 +1084,25 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         if (hi <= lo || plan->pm.empty()) return SS_OK;
         fill(pa, pb);
         const int64_t nvec = (hi - lo) / 8;
+        FlatRoundsKern fr = unpacked && kFlatRounds > 0 ? pick_flat_rounds(N) : nullptr;
+        if (fr) {
+            // rounds of 32 vectors per warp, as many as keep kCopyinWaves
+            // waves of CTAs (at most kFlatRounds)
+            int64_t it = nvec / ((int64_t)kThreads * kCopyinWaves * 3 * 152);
+            const int iters = (int)(it < 1 ? 1 : it > kFlatRounds ? kFlatRounds : it);
+            const int64_t span = 32 * (int64_t)iters;  // vectors per warp
+            const int64_t nw = (nvec + span - 1) / span;
+            constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
+            for (int64_t w0 = 0; w0 < nw; w0 += kChunkW) {
+                const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
+                const int64_t cv = w0 + cw >= nw ? nvec - span * w0 : span * cw;
+                fr<<<(unsigned)((cw + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
+                    plan->d_pm, plan->d_pm_block, lo + 8 * span * w0, cv, iters, a, tab);
+                int rc = ss::check_launch();
+                if (rc) return rc;
+            }
+            return SS_OK;
+        }
         FlatKern ff = unpacked ? pick_flat<true>(N) : pick_flat<false>(N);
         constexpr int64_t kMaxBlocks = 0x7FFFFFFF;
         for (int64_t v0 = 0; v0 < nvec; v0 += kMaxBlocks * kThreads) {
