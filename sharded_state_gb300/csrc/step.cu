@@ -8,10 +8,12 @@
 // tensor ("FSDP1 vs FSDP2" section 03 / 04: a run of one parameter inside one
 // rank's shard).  Two forms: the flat kernels stream f like the
 // reduce-scatter and place each vector through the plan's packed segment
-// map (fused_step_flat_kernel: runs all whole 16-byte vectors;
-// fused_step_flat_any_kernel: packed gradients, any alignment);
-// fused_step_kernel walks the plan's data tiles (any alignment, used for the
-// copy-in on misaligned plans and for parameter windows).  That lets one pass
+// map (fused_step_flat_kernel and, for the copy-in, its rounds form
+// fused_step_flat_rounds_kernel: runs all whole 16-byte vectors;
+// fused_step_flat_any_kernel: packed gradients, any alignment;
+// fused_step_flat_copyin_kernel: per-parameter gradients, any alignment);
+// fused_step_kernel walks the plan's data tiles (any alignment, used when
+// the parameters need more than one pointer table).  That lets one pass
 //   - read the N gradients either from the packed rank buffers (the
 //     reduce-scatter input FSDP builds by copy-in) or directly from the N
 //     per-parameter gradient sets, which fuses the copy-in away;
