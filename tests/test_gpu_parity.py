@@ -538,6 +538,56 @@ def test_special_values_reduce_scatter_and_adamw(ss):
     np.testing.assert_array_equal(to_np(shards)[fin], oracle.bf16_round(gm[fin]))
 
 
+def _same_or_both_nan(x, y):
+    """Bit-identical where either side is a number; NaN in the same places."""
+    x, y = np.asarray(x), np.asarray(y)
+    if x.dtype == np.uint16:  # bf16 bits
+        nx = ((x & 0x7F80) == 0x7F80) & ((x & 0x7F) != 0)
+        ny = ((y & 0x7F80) == 0x7F80) & ((y & 0x7F) != 0)
+    else:
+        nx, ny = np.isnan(x), np.isnan(y)
+    np.testing.assert_array_equal(nx, ny)
+    np.testing.assert_array_equal(x[~nx].view(np.uint8), y[~ny].view(np.uint8))
+
+
+@pytest.mark.parametrize("N", [2, 4, 6, 8])
+def test_special_values_one_pass_step(ss, N):
+    # subnormal rank sums, infinities and NaN through the one pass: its
+    # reduced gradient must be the oracle's reduce-scatter, and its state,
+    # shards and outputs those of the two calls
+    c = 2048 + 3
+    total = N * c
+    plan = ss.fsdp_plan_layout(ss.SS_FLAT_ORIG_FALSE, N, 2, [total])
+    g_np = [_special_bf16(total, 200 + 7 * N + r) for r in range(N)]
+    grads = [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda() for b in g_np]
+    rng = np.random.default_rng(8)
+    master_np = rng.normal(0, 0.02, total).astype(np.float32)
+    master_np[::97] = np.float32(1e-40)
+    runs = []
+    for one_pass in (False, True):
+        master = torch.from_numpy(master_np.copy()).cuda()
+        m = torch.zeros(total, device="cuda")
+        v = torch.zeros(total, device="cuda")
+        shards = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+        red = torch.empty(total, device="cuda")
+        out = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+        hp = ss.adamw_params(step=1)
+        if one_pass:
+            ss.fsdp_sharded_step(plan, master, m, v, shards, hp, rank_grads=grads, params_out=[out],
+                                 n_out=1, reduced_grad_out=red)
+        else:
+            ss.fsdp_reduce_scatter_adamw(plan, grads, master, m, v, shards, hp, red)
+            ss.fsdp_all_gather_unpack(plan, shards, [out], n_out=1)
+        torch.cuda.synchronize()
+        runs.append([to_np(t) for t in (red, master, m, v, shards, out)])
+    want = oracle.reduce_scatter(N, c, g_np)
+    for got in (runs[0][0], runs[1][0]):
+        _same_or_both_nan(got, want)
+    for x, y in zip(runs[0], runs[1]):
+        _same_or_both_nan(x, y)
+    assert np.isnan(want).any() and (np.abs(want[np.isfinite(want)]) < 1.2e-38).any()
+
+
 def test_special_values_ddp_average(ss):
     N, T = 5, 7
     numels = [1, 9, 64, 100, 3, 1031, 8]
