@@ -64,9 +64,10 @@ def parse_args():
     ap.add_argument("--rows", default="all",
                     help="rows mode: comma list of llama,block4096,tiny,awkward,awkward_large,ddp "
                          "(default all; awkward_large: only the large awkward sets)")
-    ap.add_argument("--step-kind", default="fused", choices=["two_calls", "fused"],
-                    help="timed step: the one-pass fsdp_sharded_step (default), or RS+AdamW "
-                         "then all-gather as two calls")
+    ap.add_argument("--step-kind", default="fused", choices=["two_calls", "fused", "copy_in"],
+                    help="timed step: the one-pass fsdp_sharded_step from packed gradients "
+                         "(default), RS+AdamW then all-gather as two calls, or the one pass "
+                         "reading N per-parameter gradient sets (fused copy-in)")
     ap.add_argument("--ddp-large", type=int, default=600,
                     help="rows mode: number of 4M-element DDP tensors (600 = the full list)")
     ap.add_argument("--awkward-scale", type=float, default=1.0,
@@ -347,10 +348,15 @@ def run_native(args, world, rank, local, dist):
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
-    fused = args.step_kind == "fused"
+    fused = args.step_kind in ("fused", "copy_in")
+    # the fused copy-in reads N per-parameter gradient sets instead of the
+    # packed rank buffers
+    param_grads = None
+    if args.step_kind == "copy_in":
+        param_grads = ss.ptr_array([g for rank in st._rank_grad_iter("cuda") for g in rank])
     for _ in range(max(args.warmup, 0)):
         if fused:
-            st.fused_step(sp)
+            st.fused_step(sp, param_grads=param_grads)
         else:
             st.rs_adamw(sp)
             st.all_gather(sp)
@@ -372,7 +378,7 @@ def run_native(args, world, rank, local, dist):
         for k in range(K):
             ev[k][0].record(stream)
             if fused:
-                st.fused_step(sp)
+                st.fused_step(sp, param_grads=param_grads)
             else:
                 st.rs_adamw(sp)
             ev[k][1].record(stream)
@@ -425,14 +431,17 @@ def run_native(args, world, rank, local, dist):
                         "all_gather_unpack": {"ms": ag_avg, "ms_min": min(ag_ms), "gbs": ag_gbs,
                                               "bytes": by["all_gather"]}}),
            "roofline": {"bound": "hbm",
-                        "kernel": ("fused_step_flat_kernel (one-pass RS+AdamW+AG)" if fused
+                        "kernel": ("fused_step_flat_rounds_kernel (one-pass RS+AdamW+AG, "
+                                   "fused copy-in)" if param_grads is not None else
+                                   "fused_step_flat_kernel (one-pass RS+AdamW+AG)" if fused
                                    else "rs_adamw_bf16_kernel"),
                         "achieved": rs_gbs, "peak": peak,
                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                         if peak_kind == "measured" else "fallback 6.8 TB/s",
                         "unit": "GB/s", "frac": rs_gbs / peak,
                         "traffic": None if N != 8 or (fused and args.n_out != 1) else
-                        ncu_traffic("fused_step_flat_kernel<8>" if fused
+                        ncu_traffic("fused_step_flat_rounds_kernel<8>" if param_grads is not None
+                                    else "fused_step_flat_kernel<8>" if fused
                                     else "rs_adamw_bf16_kernel<8,1,0,1,0>", total),
                         "traffic_source": "ncu capture per element x elements per launch "
                                           "(profiles/ncu_traffic.json)",
@@ -522,7 +531,7 @@ def run_e2e(st: Step, args, stream, dist) -> dict:
                 ev_in[g].record(h2d)
         for g in order:
             stream.wait_event(ev_in[g])
-            if args.step_kind == "fused":
+            if args.step_kind != "two_calls":  # the copy-in kind, too, from packed buffers here
                 st.fused_step(sp, group=g, hp=hp)
             else:
                 st.rs_adamw(sp, group=g, hp=hp)
