@@ -6,9 +6,9 @@
 // FlatParameter chunk may hold the tail of one parameter, pad and the head of
 // the next; FSDP2 rank r holds rows [r*c_i, (r+1)*c_i) of every parameter).
 // The planner splits every segment into 16 KiB tiles; one short-lived CTA
-// copies one tile (two dependent metadata loads, then 4 x 128-bit vectors per
-// thread in flight), and the grid is one CTA per tile, so all SMs stream
-// through a narrow, advancing window of HBM.  A piece moves in 128-bit vectors
+// copies one tile (one load of the tile's entry with its segment inline, then
+// 4 x 128-bit vectors per thread in flight), and the grid is one CTA per
+// tile, so all SMs stream through a narrow, advancing window of HBM.  A piece moves in 128-bit vectors
 // when source and destination are congruent mod 16 bytes; otherwise the stores
 // stay 16-byte aligned and every source vector is rebuilt in registers from the
 // two aligned blocks that cover it (element copies remain only for several
@@ -34,10 +34,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTabSmall = 256;
 constexpr int kTabBig = 2048;
-// When one pointer table covers the call, tiles could be walked in packed-offset
-// order; parameter order measured slightly faster on GB300 (0.823 vs 0.829 ms
-// for the 1.2B all-gather), so it stays off.
-constexpr bool kPackedOrder = false;
 
 template <int CAP>
 struct PtrTab {
@@ -219,11 +215,10 @@ __device__ __forceinline__ void cta_zero(unsigned char* dst, int64_t nelem) {
 // plan and replicas all 16-byte aligned (no realigning code).
 template <int E, int CAP, int DIR>
 __global__ void __launch_bounds__(kThreads, DIR >= 2 ? 2 : 5)
-tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
-                 unsigned char* packed, PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out) {
+tile_copy_kernel(const ss::PmEntry* __restrict__ ext, int64_t t_lo, unsigned char* packed,
+                 PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out) {
     constexpr int64_t T = ss::kTileBytes / E;
-    const ss::Tile tl = tiles[t_lo + blockIdx.x];
-    const ss::Seg sg = segs[tl.seg];
+    const ss::PmEntry sg = ext[t_lo + blockIdx.x];  // the tile's segment, tile index in reserved
     const int slot = sg.param - param_base;
     // The segment's tile starts are moved back by u elements, u = how far the
     // stores' side (the packed buffer for DIR 1, the parameter otherwise --
@@ -235,7 +230,7 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
         DIR != 1 ? reinterpret_cast<uintptr_t>(tab.p[slot]) + (uintptr_t)(sg.param_off * E)
                  : reinterpret_cast<uintptr_t>(packed) + (uintptr_t)(sg.packed_off * E);
     const int64_t u = (int64_t)((side & 15u) / E);
-    const int64_t idx = tl.idx;
+    const int64_t idx = sg.reserved;
     const int64_t off = idx == 0 ? 0 : idx * T - u;
     const int64_t len = ((idx + 1) * T >= sg.len ? sg.len : (idx + 1) * T - u) - off;
     if (DIR == 0) {
@@ -266,14 +261,12 @@ tile_copy_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
 // enough registers for 8 resident CTAs per SM.  DIR 0: all-gather, 1: pack.
 template <int E, int CAP, int DIR>
 __global__ void __launch_bounds__(kThreads, 8)
-tile_copy_fast_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo,
-                      const ss::Seg* __restrict__ segs, unsigned char* packed, PtrTab<CAP> tab,
-                      int param_base) {
+tile_copy_fast_kernel(const ss::PmEntry* __restrict__ ext, int64_t t_lo, unsigned char* packed,
+                      PtrTab<CAP> tab, int param_base) {
     constexpr int64_t T = ss::kTileBytes / E;
     constexpr int kV = ss::kTileBytes / 16 / kThreads;  // vectors per thread
-    const ss::Tile tl = tiles[t_lo + blockIdx.x];
-    const ss::Seg sg = segs[tl.seg];
-    const int64_t off = (int64_t)tl.idx * T;
+    const ss::PmEntry sg = ext[t_lo + blockIdx.x];  // the tile's segment, tile index in reserved
+    const int64_t off = (int64_t)sg.reserved * T;
     const int nv = (int)((sg.len - off < T ? sg.len - off : T) * E / 16);
     unsigned char* pp = static_cast<unsigned char*>(tab.p[sg.param - param_base]) +
                         (sg.param_off + off) * E;
@@ -318,17 +311,17 @@ int for_tile_chunks(int64_t t_lo, int64_t t_hi, Launch launch) {
     return SS_OK;
 }
 
-// Tiles of params [a, b): consecutive in the parameter-ordered table, or, when
-// [a, b) is whole groups [ga, gb), the packed-order table of those groups.
+// Tiles of params [a, b): consecutive in the parameter-ordered table (a
+// packed-offset order measured slightly slower on GB300: 0.829 against
+// 0.823 ms for the 1.2B all-gather).
 template <int CAP>
 int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed,
-                  void* const* ptrs, int n_out, cudaStream_t st, int ga = -1, int gb = -1) {
+                  void* const* ptrs, int n_out, cudaStream_t st) {
     const int s_lo = p->param_seg[a], s_hi = p->param_seg[b];
     if (s_hi <= s_lo) return SS_OK;
-    const bool by_offset = kPackedOrder && ga >= 0;
-    const ss::Tile* tiles = by_offset ? p->d_packed_tiles : p->d_data_tiles;
-    const int64_t t_lo = by_offset ? p->group_ptile[ga] : p->data_seg_tile[s_lo];
-    const int64_t t_hi = by_offset ? p->group_ptile[gb] : p->data_seg_tile[s_hi];
+    const ss::PmEntry* tiles = p->d_data_tiles_ext;
+    const int64_t t_lo = p->data_seg_tile[s_lo];
+    const int64_t t_hi = p->data_seg_tile[s_hi];
     PtrTab<CAP> tab;
     std::memset(&tab, 0, sizeof tab);
     const int w = b - a;
@@ -343,61 +336,48 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
         return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
             if (p->eb == 2) {
                 if (dir == 0)
-                    tile_copy_fast_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
-                                                                                packed, tab, a);
+                    tile_copy_fast_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
                 else
-                    tile_copy_fast_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
-                                                                                packed, tab, a);
+                    tile_copy_fast_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
             } else {
                 if (dir == 0)
-                    tile_copy_fast_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
-                                                                                packed, tab, a);
+                    tile_copy_fast_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
                 else
-                    tile_copy_fast_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data,
-                                                                                packed, tab, a);
+                    tile_copy_fast_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
             }
         });
     }
     return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
         if (p->eb == 2) {
             if (dir == 0 && n_out > 1 && all_aligned)
-                tile_copy_kernel<2, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, n_out);
+                tile_copy_kernel<2, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
             else if (dir == 0 && n_out > 1)
-                tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, n_out);
+                tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
             else if (dir == 0)
-                tile_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, 1);
+                tile_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
             else
-                tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, 1);
+                tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
         } else {
             if (dir == 0 && n_out > 1 && all_aligned)
-                tile_copy_kernel<4, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, n_out);
+                tile_copy_kernel<4, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
             else if (dir == 0 && n_out > 1)
-                tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, n_out);
+                tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
             else if (dir == 0)
-                tile_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, 1);
+                tile_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
             else
-                tile_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, p->d_data, packed,
-                                                                       tab, a, w, 1);
+                tile_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
         }
     });
 }
 
-// Run the segment copy for params [pa, pb) = groups [ga, gb), windowing the
-// pointer table.
-int run_segments(const ss_plan* p, int dir, int pa, int pb, int ga, int gb, unsigned char* packed,
+// Run the segment copy for params [pa, pb), windowing the pointer table.
+int run_segments(const ss_plan* p, int dir, int pa, int pb, unsigned char* packed,
                  void* const* ptrs, int n_out, cudaStream_t st) {
     const int n_ptr = (pb - pa) * n_out;
     if (n_ptr <= kTabSmall)
-        return launch_window<kTabSmall>(p, dir, pa, pb, packed, ptrs, n_out, st, ga, gb);
+        return launch_window<kTabSmall>(p, dir, pa, pb, packed, ptrs, n_out, st);
     if (n_ptr <= kTabBig)
-        return launch_window<kTabBig>(p, dir, pa, pb, packed, ptrs, n_out, st, ga, gb);
+        return launch_window<kTabBig>(p, dir, pa, pb, packed, ptrs, n_out, st);
     const int w = kTabBig / n_out;
     for (int a = pa; a < pb; a += w) {
         int b = a + w < pb ? a + w : pb;
@@ -445,8 +425,7 @@ int fsdp_pack(const ss_plan* plan, const void* const* params, void* packed, int 
     int rc = check_param_ptrs(plan, pa, pb, const_cast<void* const*>(params), 1);
     if (rc) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int ga0 = group < 0 ? 0 : group, gb0 = group < 0 ? plan->G : group + 1;
-    rc = run_segments(plan, 1, pa, pb, ga0, gb0, static_cast<unsigned char*>(packed),
+    rc = run_segments(plan, 1, pa, pb, static_cast<unsigned char*>(packed),
                       const_cast<void* const*>(params), 1, st);
     if (rc) return rc;
     // pads of the selected groups
@@ -478,10 +457,8 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards, void* 
     param_range(plan, group, &pa, &pb);
     int rc = check_param_ptrs(plan, pa, pb, params_out, n_out);
     if (rc) return rc;
-    const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
-    return run_segments(plan, 0, pa, pb, ga, gb,
-                        static_cast<unsigned char*>(const_cast<void*>(param_shards)), params_out,
-                        n_out, reinterpret_cast<cudaStream_t>(stream));
+    return run_segments(plan, 0, pa, pb, static_cast<unsigned char*>(const_cast<void*>(param_shards)),
+                        params_out, n_out, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

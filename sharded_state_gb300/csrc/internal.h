@@ -77,16 +77,15 @@ struct ss_plan {
     // tiles of the data / pad segments; seg_tile[k] = first tile of segment k (size nseg+1)
     std::vector<ss::Tile> data_tiles, zero_tiles;
     std::vector<int64_t> data_seg_tile, zero_seg_tile;
-    // the data tiles again, ordered by packed offset; group g's tiles are
-    // [group_ptile[g], group_ptile[g+1])
-    std::vector<ss::Tile> packed_tiles;
-    std::vector<int64_t> group_ptile;
+    // the data tiles with their segment's fields inline (tile index in
+    // `reserved`): one load places a tile
+    std::vector<ss::PmEntry> data_tiles_ext;
     // device copies
     ss::Seg* d_data = nullptr;
     ss::Seg* d_zero = nullptr;
     ss::Tile* d_data_tiles = nullptr;
     ss::Tile* d_zero_tiles = nullptr;
-    ss::Tile* d_packed_tiles = nullptr;
+    ss::PmEntry* d_data_tiles_ext = nullptr;
     // The data segments in packed-offset order (pm[m], m = 0..M-1).
     // pm_block[B] is the last m whose packed offset is <= B * kMapBlock (0 if
     // none), for every block B in [0, total / kMapBlock + 1]: the segment

@@ -160,24 +160,15 @@ bool build_tiles(const std::vector<ss::Seg>& segs, int eb, std::vector<ss::Tile>
     return true;
 }
 
-// Data tiles in packed-offset order, group by group (segments of one group
-// are disjoint runs of that group's range, so sorting by offset keeps groups
-// contiguous).
-void build_packed_tiles(ss_plan* p) {
-    std::vector<int> order(p->data.size());
-    for (size_t k = 0; k < order.size(); ++k) order[k] = (int)k;
-    std::sort(order.begin(), order.end(),
-              [&](int a, int b) { return p->data[a].packed_off < p->data[b].packed_off; });
-    p->packed_tiles.clear();
-    p->group_ptile.assign(p->G + 1, 0);
-    int g = 0;
-    for (int k : order) {
-        const int pg = p->param_group[p->data[k].param];
-        while (g < pg) p->group_ptile[++g] = (int64_t)p->packed_tiles.size();
-        for (int64_t t = p->data_seg_tile[k]; t < p->data_seg_tile[k + 1]; ++t)
-            p->packed_tiles.push_back(p->data_tiles[t]);
+// The data tiles with their segment's fields inline (the tile index in
+// `reserved`), so one load places a tile.
+void build_tiles_ext(ss_plan* p) {
+    p->data_tiles_ext.resize(p->data_tiles.size());
+    for (size_t t = 0; t < p->data_tiles.size(); ++t) {
+        const ss::Tile& tl = p->data_tiles[t];
+        const ss::Seg& sg = p->data[tl.seg];
+        p->data_tiles_ext[t] = ss::PmEntry{sg.packed_off, sg.param_off, sg.len, sg.param, tl.idx};
     }
-    while (g < p->G) p->group_ptile[++g] = (int64_t)p->packed_tiles.size();
 }
 
 // The packed segment map: data segments by packed offset, and for every
@@ -238,11 +229,11 @@ int upload(ss_plan* p) {
                        cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return ss::cuda_fail(e);
     }
-    e = cudaMalloc(&p->d_packed_tiles, ndt * sizeof(ss::Tile));
+    e = cudaMalloc(&p->d_data_tiles_ext, ndt * sizeof(ss::PmEntry));
     if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
-    if (!p->packed_tiles.empty()) {
-        e = cudaMemcpy(p->d_packed_tiles, p->packed_tiles.data(),
-                       p->packed_tiles.size() * sizeof(ss::Tile), cudaMemcpyHostToDevice);
+    if (!p->data_tiles_ext.empty()) {
+        e = cudaMemcpy(p->d_data_tiles_ext, p->data_tiles_ext.data(),
+                       p->data_tiles_ext.size() * sizeof(ss::PmEntry), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return ss::cuda_fail(e);
     }
     e = cudaMalloc(&p->d_pm, std::max<size_t>(p->pm.size(), 1) * sizeof(ss::PmEntry));
@@ -373,7 +364,7 @@ int fsdp_plan_create(const ss_plan_desc* d, ss_plan** out) {
                      !build_tiles(p->zero, p->eb, &p->zero_tiles, &p->zero_seg_tile))
                 rc = SS_EOVERFLOW;
             else {
-                build_packed_tiles(p);
+                build_tiles_ext(p);
                 build_packed_map(p);
             }
             const int64_t per16 = 16 / p->eb;
@@ -446,7 +437,7 @@ void fsdp_plan_destroy(ss_plan* p) {
     if (p->d_zero) cudaFree(p->d_zero);
     if (p->d_data_tiles) cudaFree(p->d_data_tiles);
     if (p->d_zero_tiles) cudaFree(p->d_zero_tiles);
-    if (p->d_packed_tiles) cudaFree(p->d_packed_tiles);
+    if (p->d_data_tiles_ext) cudaFree(p->d_data_tiles_ext);
     if (p->d_pm) cudaFree(p->d_pm);
     if (p->d_pm_block) cudaFree(p->d_pm_block);
     delete p;
@@ -503,17 +494,16 @@ int fsdp_plan_validate(const ss_plan* p) {
     if (!check_tiles(p->data, p->data_tiles, p->data_seg_tile) ||
         !check_tiles(p->zero, p->zero_tiles, p->zero_seg_tile))
         return SS_EINVAL;
-    // packed-order tiles: a permutation of the data tiles, groups contiguous
-    if (p->packed_tiles.size() != p->data_tiles.size()) return SS_EINVAL;
-    if (p->group_ptile.size() != (size_t)p->G + 1 || p->group_ptile[0] != 0 ||
-        p->group_ptile[p->G] != (int64_t)p->packed_tiles.size())
-        return SS_EINVAL;
-    for (int g = 0; g < p->G; ++g)
-        for (int64_t t = p->group_ptile[g]; t < p->group_ptile[g + 1]; ++t) {
-            const ss::Tile& tl = p->packed_tiles[t];
-            if (tl.seg < 0 || (size_t)tl.seg >= p->data.size()) return SS_EINVAL;
-            if (p->param_group[p->data[tl.seg].param] != g) return SS_EINVAL;
-        }
+    // data tiles with their segment inline: the same tiles, same fields
+    if (p->data_tiles_ext.size() != p->data_tiles.size()) return SS_EINVAL;
+    for (size_t t = 0; t < p->data_tiles.size(); ++t) {
+        const ss::Tile& tl = p->data_tiles[t];
+        const ss::Seg& sg = p->data[tl.seg];
+        const ss::PmEntry& x = p->data_tiles_ext[t];
+        if (x.packed_off != sg.packed_off || x.param_off != sg.param_off || x.len != sg.len ||
+            x.param != sg.param || x.reserved != tl.idx)
+            return SS_EINVAL;
+    }
     // packed segment map: every data segment once, by strictly increasing
     // offset; pm_block[B] is the last segment starting at or before block B
     const size_t M = p->pm.size();
