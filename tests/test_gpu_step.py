@@ -37,6 +37,10 @@ CASES = [("tiny_mlp", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
          ("awkward1d_false_N7", W.awkward_1d(7, W.FLAT_ORIG_FALSE, torch.bfloat16)),
          ("awkward1d_true_N5", W.awkward_1d(5, W.FLAT_ORIG_TRUE, torch.bfloat16)),
          ("awkward2d_N3", W.awkward_2d(3)),
+         # misaligned at N = 1 (one rank: every vector from the single buffer)
+         # and N = 16 (ranks beyond the first 8 read one by one)
+         ("awkward1d_false_N1", W.awkward_1d(1, W.FLAT_ORIG_FALSE, torch.bfloat16, count=60)),
+         ("awkward2d_N16", W.awkward_2d(16, count=60)),
          ("small_llama_N3", W.llama_1b2(world_size=3, layers=3, hidden=40, ffn=72, vocab=100)),
          ("small_llama_N8", W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)),
          # aligned plans for the flat kernel's general instance (N = 12 with pads, N = 1)
