@@ -34,6 +34,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTabSmall = 256;
 constexpr int kTabBig = 2048;
+// CTAs ahead whose tile a multi-replica all-gather CTA prefetches into L2:
+// 2.5 waves at 2 CTAs per SM (304 to 760 measured alike)
+constexpr int kCopyAhead = 760;
 
 template <int CAP>
 struct PtrTab {
@@ -252,6 +255,24 @@ tile_copy_kernel(const ss::PmEntry* __restrict__ ext, int64_t t_lo, unsigned cha
         const unsigned char* src =
             static_cast<const unsigned char*>(tab.p[slot]) + (sg.param_off + off) * E;
         cta_copy<E>(&dst, 1, src, len);
+    }
+    if (DIR >= 2 && blockIdx.x + kCopyAhead < gridDim.x) {
+        // multi-replica CTAs write n_out copies of their tile and live long
+        // enough for the tile kCopyAhead CTAs on to start as they end: its
+        // source lines into L2 (64 bytes per thread cover the 16 KiB tile;
+        // the range is clipped to the segment).  The one-copy forms measured
+        // slower with it.
+        const ss::PmEntry nt = ext[t_lo + blockIdx.x + kCopyAhead];
+        const int64_t a0 = nt.reserved * T;
+        const int64_t a1 = a0 + T < nt.len ? a0 + T : nt.len;
+        const int64_t b = a0 + (int64_t)threadIdx.x * (64 / E);
+        if (b < a1) {
+            const unsigned char* src =
+                DIR == 1 ? static_cast<const unsigned char*>(tab.p[nt.param - param_base]) +
+                               (nt.param_off + b) * E
+                         : packed + (nt.packed_off + b) * E;
+            ss::prefetch_l2(src);
+        }
     }
 }
 
