@@ -955,6 +955,21 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
              st1.info["unpadded_numel"], "params/s", ms, mn,
              (2 * 2 + 26) * st1.info["total_numel"] + 2 * st1.info["unpadded_numel"], peak,
              extra={"us_per_step": ms * 1e3})
+        # the same call with its arguments marshalled once (ss.ShardedStep)
+        call = ss.ShardedStep(st1.plan, st1.master, st1.m, st1.v, st1.shards, st1.next_hp(),
+                              rank_grads=st1._grads_arr, params_out=st1._outs_arr, n_out=1,
+                              stream=torch.cuda.current_stream())
+        step_no = [st1.t]
+
+        def prepared():
+            step_no[0] += 1
+            call(step_no[0])
+        ms, mn = _time_stream(prepared, 200, warmup=20)
+        _row("step on the tiny MLP (16,640 params, N=2): latency, one prepared fsdp_sharded_step "
+             "call (ss.ShardedStep)", st1.info["unpadded_numel"], "params/s", ms, mn,
+             (2 * 2 + 26) * st1.info["total_numel"] + 2 * st1.info["unpadded_numel"], peak,
+             extra={"us_per_step": ms * 1e3})
+        del call
         # the same two C-ABI calls captured once in a CUDA graph and replayed:
         # the launch-bound step without host-side call overhead (the AdamW step
         # count is frozen in the captured arguments, which does not change the

@@ -360,6 +360,44 @@ def fsdp_sharded_step(plan: Plan, master, exp_avg, exp_avg_sq, param_shards, hp:
                                                        _stream(stream)))
 
 
+class ShardedStep:
+    """fsdp_sharded_step with every argument marshalled once, for loops whose
+    steps are short enough that building the call each time shows: a call
+    sets the AdamW step number (the other hyper-parameters are the ones given
+    here) and runs the step on `stream`, an int handle (0: the legacy default
+    stream) fixed here.  Keeps the pointer arrays alive; the tensors must stay
+    alive and in place as long as the object is used."""
+
+    def __init__(self, plan: Plan, master, exp_avg, exp_avg_sq, param_shards, hp: AdamW,
+                 rank_grads: Optional[Sequence] = None,
+                 rank_param_grads: Optional[Sequence] = None, params_out=None, n_out: int = 0,
+                 reduced_grad_out=None, group: int = -1, stream=None):
+        self._plan = plan  # keeps the plan alive
+        self._pp = ctypes.c_void_p(plan.handle)
+        self._hp = AdamW(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step)
+        self._keep = []
+
+        def arr(xs):
+            if xs is None:
+                return None
+            a = _ptr_array(xs)
+            self._keep.append(a)
+            return ctypes.cast(a, ctypes.c_void_p)
+        self._st = _Step(arr(rank_grads), arr(rank_param_grads), _addr(master), _addr(exp_avg),
+                         _addr(exp_avg_sq), _addr(param_shards), ctypes.pointer(self._hp),
+                         _addr(reduced_grad_out), arr(params_out) if n_out > 0 else None, n_out)
+        self._ref = ctypes.byref(self._st)
+        self._group = group
+        self._stream = _stream(stream)
+        self._fn = _lib.fsdp_sharded_step
+
+    def __call__(self, step: int) -> None:
+        self._hp.step = step
+        status = self._fn(self._pp, self._ref, self._group, self._stream)
+        if status != SS_OK:
+            _check("fsdp_sharded_step", status)
+
+
 def ddp_bucket_pack_average(rank_grads: Sequence[Sequence], bucket_cap_bytes: int,
                             avg_out: Sequence, numels: Optional[Sequence[int]] = None,
                             stream=None) -> int:

@@ -88,6 +88,7 @@ def test_sharded_step_matches_two_calls_and_oracle(ss, name, ps):
     sb, mb, mmb, vb = _state(ss, su)
     sc, mc, mmc, vc = _state(ss, su)
     red_b = torch.zeros(total, device="cuda")
+    red_c = torch.zeros(total, device="cuda")
     outs_b, wholes = [], []
     for _ in range(n_out):
         for p in su.params:
@@ -104,9 +105,10 @@ def test_sharded_step_matches_two_calls_and_oracle(ss, name, ps):
         ss.fsdp_sharded_step(su.plan, mb, mmb, vb, sb, hp, rank_grads=packed, params_out=outs_b,
                              n_out=n_out, reduced_grad_out=red_b)
         ss.fsdp_sharded_step(su.plan, mc, mmc, vc, sc, hp, rank_param_grads=flat_param_grads,
-                             params_out=outs_c, n_out=n_out)
+                             params_out=outs_c, n_out=n_out, reduced_grad_out=red_c)
         torch.cuda.synchronize()
         assert all(guards_intact(w) for w in wholes)
+        np.testing.assert_array_equal(to_np(red_b).view(np.uint32), to_np(red_c).view(np.uint32))
         for x, y, z in ((sa, sb, sc), (ma, mb, mc), (mma, mmb, mmc), (va, vb, vc)):
             np.testing.assert_array_equal(to_np(x).view(np.uint8), to_np(y).view(np.uint8))
             np.testing.assert_array_equal(to_np(x).view(np.uint8), to_np(z).view(np.uint8))
@@ -220,6 +222,39 @@ def test_sharded_step_groups_inside_one_vector(ss, kind):
     for j in range(2):
         for i in range(n):
             assert results[1][5 + j * n + i].size == su.params[i].numel()
+
+
+def test_prepared_step_equals_the_call(ss):
+    # ss.ShardedStep marshals the arguments once; its steps must be the plain
+    # call's, bit for bit, for packed and per-parameter gradients
+    ps = W.llama_1b2(world_size=4, layers=2, hidden=48, ffn=136, vocab=96)
+    su = Setup(ss, ps)
+    N = su.N
+    grads = [[g.cuda() for g in rank] for rank in W.make_rank_grads(ps)]
+    flat = [g for rank in grads for g in rank]
+    packed = []
+    for r in range(N):
+        b = torch.empty(su.total, dtype=torch.bfloat16, device="cuda")
+        ss.fsdp_pack(su.plan, grads[r], b)
+        packed.append(b)
+    for src in ("packed", "per_param"):
+        kw = {"rank_grads": packed} if src == "packed" else {"rank_param_grads": flat}
+        sa, ma, mma, va = _state(ss, su)
+        sb, mb, mmb, vb = _state(ss, su)
+        outs_a = [torch.empty_like(p) for p in su.params]
+        outs_b = [torch.empty_like(p) for p in su.params]
+        call = ss.ShardedStep(su.plan, mb, mmb, vb, sb, ss.adamw_params(step=1, **_hp(1)),
+                              params_out=outs_b, n_out=1, **kw)
+        for step in (1, 2, 3):
+            ss.fsdp_sharded_step(su.plan, ma, mma, va, sa, ss.adamw_params(step=step, **_hp(1)),
+                                 params_out=outs_a, n_out=1, **kw)
+            call(step)
+        torch.cuda.synchronize()
+        for x, y in zip([sa, ma, mma, va] + outs_a, [sb, mb, mmb, vb] + outs_b):
+            np.testing.assert_array_equal(to_np(x).view(np.uint8), to_np(y).view(np.uint8))
+    with pytest.raises(ss.ShardStateError):
+        ss.ShardedStep(su.plan, mb, mmb, vb, sb, ss.adamw_params(step=1, **_hp(1)),
+                       rank_grads=packed, params_out=outs_b, n_out=1)(0)  # step 0: EINVAL
 
 
 def test_sharded_step_state_against_oracle(ss):
