@@ -52,7 +52,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama_1b2",
-                    choices=["llama_1b2", "llama_block_4096", "probe", "tiny_mlp"])
+                    choices=["llama_1b2", "llama_block_4096", "probe", "tiny_mlp"],
+                    help="step mode: the timed model; rows mode: the model of the llama rows "
+                         "(llama_1b2, or probe for a few-GB profiling case)")
     ap.add_argument("--n-out", type=int, default=1, help="all-gather replicas (1 or N)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
@@ -761,8 +763,9 @@ def run_rows(args):
 
 
 def _rows_llama(args, ss, oracle, peak, used, K, bits):
-    # -- a1/a2/a3/a4 on the 1.2B model ---------------------------------------
-    ps = W.llama_1b2()
+    # -- a1/a2/a3/a4 on the 1.2B model (or a smaller Llama for profiling) ---
+    ps = make_workload(args.workload) if args.workload != "llama_1b2" else W.llama_1b2()
+    tag = "1.2B" if args.workload == "llama_1b2" else args.workload
     d0_, inner_ = ps.dim0_inner()
     t0 = time.perf_counter()
     for _ in range(5):
@@ -775,11 +778,12 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
                                      for a, g in zip(np.cumsum([0] + ps.groups[:-1]), ps.groups)],
                             1.0)
     print(json.dumps({"row": "a1 plan: layout, segment and tile tables + device upload "
-                             "(1.2B model, 219 params, 25 groups, N=8)",
+                             f"({tag} model, {ps.num_params} params, {len(ps.groups)} groups, "
+                             f"N={ps.world_size})",
                       "value": 1.0 / t_plan, "unit": "plans/s", "ms": t_plan * 1e3,
                       "host_only": "runs once per model; not on the per-step path",
                       "cpu_baseline": {"value": 1.0 / t_cpu, "unit": "layouts/s", "cores": 1,
-                                       "kind": "oracle", "sample": f"the 25 group layouts, {reps} reps"}}),
+                                       "kind": "oracle", "sample": f"the {len(ps.groups)} group layouts, {reps} reps"}}),
           flush=True)
     st = Step(ss, ps, 1)
     P, total, N = st.info["unpadded_numel"], st.info["total_numel"], st.N
@@ -793,7 +797,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     t_cpu, reps = _time_cpu(lambda: oracle.pack(ps.layout, N, 2, d0[:g0], inner[:g0], sample),
                             args.cpu_seconds / 4)
     p0 = sum(ps.numels()[:g0])
-    _row("a2 pack (one rank's gradients, 1.2B model, N=8)", P, "params/s", ms, mn, 4 * P, peak,
+    _row(f"a2 pack (one rank's gradients, {tag} model, N=8)", P, "params/s", ms, mn, 4 * P, peak,
          {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
           "sample": f"block group 0 ({p0:,} params), {reps} packs"})
     del grad_params
@@ -802,7 +806,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     rs_ms, rs_mn = _time_stream(lambda: st.rs_adamw(), K)
     smp = _oracle_sample_from_step(st)
     t_cpu, reps = _time_cpu(lambda: _oracle_step(ps, smp, 10_000), args.cpu_seconds / 2)
-    _row("a3 reduce-scatter + AdamW (1.2B model, N=8)", P, "params/s", rs_ms, rs_mn,
+    _row(f"a3 reduce-scatter + AdamW ({tag} model, N=8)", P, "params/s", rs_ms, rs_mn,
          (2 * N + 26) * total, peak,
          {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
           "sample": f"block group 0, {reps} oracle RS+AdamW+AG steps"})
@@ -812,17 +816,17 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     t_cpu, reps = _time_cpu(lambda: oracle.all_gather_unpack(ps.layout, N, 2, d0[:g0p],
                                                              inner[:g0p], shards0),
                             args.cpu_seconds / 4)
-    _row("a4 all-gather + unpack, n_out=1 (1.2B model, N=8)", P, "params/s", ag_ms, ag_mn, 4 * P,
+    _row(f"a4 all-gather + unpack, n_out=1 ({tag} model, N=8)", P, "params/s", ag_ms, ag_mn, 4 * P,
          peak, {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
                 "sample": f"block group 0, {reps} oracle unpacks"})
     ms, mn = _time_stream(lambda: st.fused_step(), K)
-    _row("one-pass step: packed grads -> RS+AdamW -> shards + unpacked params (1.2B, N=8)", P,
+    _row(f"one-pass step: packed grads -> RS+AdamW -> shards + unpacked params ({tag}, N=8)", P,
          "params/s", ms, mn, (2 * N + 28) * P, peak)
     rank_sets = list(st._rank_grad_iter("cuda"))  # N distinct per-parameter gradient sets
     flat_pg = ss.ptr_array([g for rank in rank_sets for g in rank])
     ms, mn = _time_stream(lambda: st.fused_step(param_grads=flat_pg), K)
     _row("one-pass step with fused copy-in: N per-parameter grad sets -> RS+AdamW -> shards + "
-         "unpacked params (1.2B, N=8)", P, "params/s", ms, mn, (2 * N + 28) * P, peak)
+         f"unpacked params ({tag}, N=8)", P, "params/s", ms, mn, (2 * N + 28) * P, peak)
     # its unfused counterpart: pack each rank's set (the copy-in), then the two calls
     set_arrs = [ss.ptr_array(rank) for rank in rank_sets]
 
@@ -833,7 +837,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
         st.all_gather()
     ms, mn = _time_stream(pack_then_step, max(K // 4, 5))
     _row("F1 counterpart: N packs of the per-parameter grad sets, then RS+AdamW and all-gather "
-         "(1.2B, N=8)", P, "params/s", ms, mn, 4 * N * P + (2 * N + 26) * total + 4 * P, peak)
+         f"({tag}, N=8)", P, "params/s", ms, mn, 4 * N * P + (2 * N + 26) * total + 4 * P, peak)
     del rank_sets, flat_pg, set_arrs
     # F2: FULL_SHARD gathers the parameters twice per iteration (forward and
     # backward), SHARD_GRAD_OP once ("FSDP1 vs FSDP2", strategy table)
@@ -847,7 +851,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
         st.rs_adamw()
     for name, fn, nag in (("FULL_SHARD", full_shard, 2), ("SHARD_GRAD_OP", shard_grad_op, 1)):
         ms, mn = _time_stream(fn, K)
-        _row(f"strategy {name}: {nag} all-gather(s) + RS+AdamW per iteration (1.2B, N=8)", P,
+        _row(f"strategy {name}: {nag} all-gather(s) + RS+AdamW per iteration ({tag}, N=8)", P,
              "params/s", ms, mn, (2 * N + 26) * total + nag * 4 * P, peak,
              extra={"all_gathers": nag})
     # F3: gradient accumulation over 4 micro-batches (same gradients each time)
@@ -872,7 +876,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
         oracle.adamw(g, smp["master"], smp["m"], smp["v"], lr=1e-3, beta1=0.9, beta2=0.999,
                      eps=1e-8, weight_decay=0.01, step=20_000)
     t_cpu, reps = _time_cpu(oracle_accumulate, args.cpu_seconds / 4)
-    _row(f"gradient accumulation: {kmic} micro-batches per optimizer step (1.2B, N=8)", P,
+    _row(f"gradient accumulation: {kmic} micro-batches per optimizer step ({tag}, N=8)", P,
          "params/s", ms, mn, acc_bytes * total, peak,
          {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
           "sample": f"block group 0, {reps} oracle optimizer steps of {kmic} micro-batches"},
@@ -884,7 +888,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
         ss.fsdp_reduce_scatter_adamw(st.plan, st._grads_arr, None, st.m, st.v, st.shards,
                                      ss.adamw_params(step=st.t))
     ms, mn = _time_stream(no_master, K)
-    _row("RS + AdamW without fp32 master (2 B params + 8 B moments, 1.2B, N=8)", P, "params/s",
+    _row(f"RS + AdamW without fp32 master (2 B params + 8 B moments, {tag}, N=8)", P, "params/s",
          ms, mn, (2 * N + 20) * total, peak)
     st8 = st
     outs8 = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for _ in range(N)
@@ -906,11 +910,11 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
         ss.fsdp_sharded_step(st8.plan, st8.master, st8.m, st8.v, st8.shards, st8.next_hp(),
                              rank_grads=st8._grads_arr, params_out=outs8_arr, n_out=N)
     ms, mn = _time_stream(zero12_two_calls, K)
-    _row("ZeRO-1/2 step: RS+AdamW, then all-gather to all N=8 ranks (two calls, 1.2B)", P,
+    _row(f"ZeRO-1/2 step: RS+AdamW, then all-gather to all N=8 ranks (two calls, {tag})", P,
          "params/s", ms, mn, (2 * N + 26) * total + (2 + 2 * N) * P, peak, extra={"n_out": N})
     ms, mn = _time_stream(zero12_one_pass, K)
     _row("ZeRO-1/2 step: RS+AdamW writing all N=8 ranks' parameters in the same pass "
-         "(fsdp_sharded_step, 1.2B)", P, "params/s", ms, mn,
+         f"(fsdp_sharded_step, {tag})", P, "params/s", ms, mn,
          (2 * N + 26) * total + 2 * N * P, peak, extra={"n_out": N})
     del outs8, outs8_arr, st, st8
     torch.cuda.empty_cache()
