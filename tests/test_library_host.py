@@ -81,6 +81,21 @@ def test_plan_tables_validate(ss, kind):
                 plan.destroy()
 
 
+def test_random_plans_validate(ss):
+    # the random plans the GPU fuzz cases run (every layout, N up to 12,
+    # empty parameters and groups): every table the kernels index through
+    # passes the library's own checks, in bf16 and fp32
+    from tests.test_gpu_fuzz import _draw
+    for seed in range(64):
+        ps, _ = _draw(seed)
+        d0, inner = ps.dim0_inner()
+        for eb in (2, 4):
+            plan = ss.fsdp_plan_create(ps.layout, ps.world_size, eb, d0, inner,
+                                       group_num_params=ps.groups, host_only=True)
+            ss.fsdp_plan_validate(plan)
+            plan.destroy()
+
+
 def test_worked_example_through_the_library(ss):
     for kind, per_rank in ((ss.SS_FLAT_ORIG_FALSE, 2), (ss.SS_FLAT_ORIG_TRUE, 4),
                            (ss.SS_PER_PARAM_DIM0, 3)):
