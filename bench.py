@@ -919,7 +919,20 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     _row("ZeRO-1/2 step: RS+AdamW writing all N=8 ranks' parameters in the same pass "
          f"(fsdp_sharded_step, {tag})", P, "params/s", ms, mn,
          (2 * N + 26) * total + 2 * N * P, peak, extra={"n_out": N})
-    del outs8, outs8_arr, st, st8
+    # the same with the fused copy-in: N + N pointers per parameter exceed one
+    # kernel-parameter table, so the call runs in windows of parameters
+    rank_sets = list(st8._rank_grad_iter("cuda"))
+    flat_pg = ss.ptr_array([g for rank in rank_sets for g in rank])
+
+    def zero12_copy_in():
+        ss.fsdp_sharded_step(st8.plan, st8.master, st8.m, st8.v, st8.shards, st8.next_hp(),
+                             rank_param_grads=flat_pg, params_out=outs8_arr, n_out=N)
+    ms, mn = _time_stream(zero12_copy_in, K)
+    _row("ZeRO-1/2 step with the fused copy-in: N per-parameter grad sets -> RS+AdamW -> all N=8 "
+         f"ranks' parameters in one pass, in parameter windows (fsdp_sharded_step, {tag})", P,
+         "params/s", ms, mn, (2 * N + 26) * total + 2 * N * P, peak,
+         extra={"n_out": N, "windows": -(-ps.num_params // (2048 // (2 * N)))})
+    del outs8, outs8_arr, st, st8, rank_sets, flat_pg
     torch.cuda.empty_cache()
 
 

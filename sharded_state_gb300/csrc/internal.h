@@ -81,9 +81,7 @@ struct ss_plan {
     // `reserved`): one load places a tile
     std::vector<ss::PmEntry> data_tiles_ext;
     // device copies
-    ss::Seg* d_data = nullptr;
     ss::Seg* d_zero = nullptr;
-    ss::Tile* d_data_tiles = nullptr;
     ss::Tile* d_zero_tiles = nullptr;
     ss::PmEntry* d_data_tiles_ext = nullptr;
     // The data segments in packed-offset order (pm[m], m = 0..M-1).

@@ -199,31 +199,21 @@ void build_packed_map(ss_plan* p) {
 int upload(ss_plan* p) {
     cudaError_t e = cudaGetDevice(&p->device);
     if (e != cudaSuccess) return ss::cuda_fail(e);
-    size_t nd = std::max<size_t>(p->data.size(), 1), nz = std::max<size_t>(p->zero.size(), 1);
-    e = cudaMalloc(&p->d_data, nd * sizeof(ss::Seg));
-    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    // on the device: the pad segments and their tiles (pack's zero fill), the
+    // data tiles with their segments inline (pack, all-gather) and the packed
+    // segment map (the one-pass step); the plain data tables stay on the host
+    const size_t nz = std::max<size_t>(p->zero.size(), 1);
     e = cudaMalloc(&p->d_zero, nz * sizeof(ss::Seg));
     if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
-    if (!p->data.empty()) {
-        e = cudaMemcpy(p->d_data, p->data.data(), p->data.size() * sizeof(ss::Seg),
-                       cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) return ss::cuda_fail(e);
-    }
     if (!p->zero.empty()) {
         e = cudaMemcpy(p->d_zero, p->zero.data(), p->zero.size() * sizeof(ss::Seg),
                        cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return ss::cuda_fail(e);
     }
-    size_t ndt = std::max<size_t>(p->data_tiles.size(), 1), nzt = std::max<size_t>(p->zero_tiles.size(), 1);
-    e = cudaMalloc(&p->d_data_tiles, ndt * sizeof(ss::Tile));
-    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
+    const size_t ndt = std::max<size_t>(p->data_tiles.size(), 1);
+    const size_t nzt = std::max<size_t>(p->zero_tiles.size(), 1);
     e = cudaMalloc(&p->d_zero_tiles, nzt * sizeof(ss::Tile));
     if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
-    if (!p->data_tiles.empty()) {
-        e = cudaMemcpy(p->d_data_tiles, p->data_tiles.data(), p->data_tiles.size() * sizeof(ss::Tile),
-                       cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) return ss::cuda_fail(e);
-    }
     if (!p->zero_tiles.empty()) {
         e = cudaMemcpy(p->d_zero_tiles, p->zero_tiles.data(), p->zero_tiles.size() * sizeof(ss::Tile),
                        cudaMemcpyHostToDevice);
@@ -433,9 +423,7 @@ int fsdp_plan_group(const ss_plan* p, int group, int64_t* base_out, int64_t* sha
 
 void fsdp_plan_destroy(ss_plan* p) {
     if (!p) return;
-    if (p->d_data) cudaFree(p->d_data);
     if (p->d_zero) cudaFree(p->d_zero);
-    if (p->d_data_tiles) cudaFree(p->d_data_tiles);
     if (p->d_zero_tiles) cudaFree(p->d_zero_tiles);
     if (p->d_data_tiles_ext) cudaFree(p->d_data_tiles_ext);
     if (p->d_pm) cudaFree(p->d_pm);

@@ -6,14 +6,15 @@
 // kernels here know for every element both its packed index f (gradient
 // buffers, optimizer state, shards) and its place k inside the parameter
 // tensor ("FSDP1 vs FSDP2" section 03 / 04: a run of one parameter inside one
-// rank's shard).  Two forms: the flat kernels stream f like the
-// reduce-scatter and place each vector through the plan's packed segment
-// map (fused_step_flat_kernel and, for the copy-in, its rounds form
-// fused_step_flat_rounds_kernel: runs all whole 16-byte vectors;
-// fused_step_flat_any_kernel: packed gradients, any alignment;
-// fused_step_flat_copyin_kernel: per-parameter gradients, any alignment);
-// fused_step_kernel walks the plan's data tiles (any alignment, used when
-// the parameters need more than one pointer table).  That lets one pass
+// rank's shard).  The kernels stream f like the reduce-scatter and place
+// each vector through the plan's packed segment map:
+// fused_step_flat_kernel and, for the copy-in, its rounds form
+// fused_step_flat_rounds_kernel when the runs are all whole 16-byte vectors;
+// fused_step_flat_any_kernel (packed gradients) and
+// fused_step_flat_copyin_kernel (per-parameter gradients) at any alignment.
+// Per-parameter pointers ride in the kernel parameters; when a call's
+// parameters need more than one table, each window of parameters runs over
+// the packed ranges its segments form.  That lets one pass
 //   - read the N gradients either from the packed rank buffers (the
 //     reduce-scatter input FSDP builds by copy-in) or directly from the N
 //     per-parameter gradient sets, which fuses the copy-in away;
@@ -30,8 +31,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <utility>
+#include <vector>
 
 #include "device_utils.cuh"
 #include "internal.h"
@@ -174,132 +178,6 @@ __device__ __forceinline__ uint4 adam_vec(const StepArgs& a, int64_t f, const fl
     return p;
 }
 
-// NR > 0: exactly NR ranks, fully unrolled; NR == 0: any N, the first 8 ranks'
-// loads predicated and kept in flight together, the rest one by one.
-// f is 8-aligned (packed side); ANY: the per-parameter side (gradients read
-// at k, outputs written at k) may be misaligned and is read / written through
-// ld_any16 / st_any16.
-// The reduced-gradient output (a.gout) and the n_out per-parameter outputs
-// are runtime options: one pointer test and a loop of n_out stores.
-// OUTS false: the n_out outputs are left to the caller (the returned vector is
-// the new bf16 parameter vector).
-template <int NR, bool UNPACKED, bool ANY = false, bool OUTS = true>
-__device__ __forceinline__ uint4 step_vec(const StepArgs& a, const PtrTab& tab, int slot,
-                                          int64_t f, int64_t k) {
-    const int n = NR > 0 ? NR : a.N;
-    uint4 w[kMaxVec];
-#pragma unroll
-    for (int r = 0; r < kMaxVec; ++r)
-        if (r < n)
-            w[r] = (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
-                                     : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k));
-    const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
-    const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
-    const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
-    float s[8];
-    sum_ranks<NR>(w, n, s);
-    for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
-        add_rank(s, (ANY && UNPACKED) ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r, slot, f, k))
-                                      : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k)));
-    const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
-    const int goff = UNPACKED ? n * a.w : 0;
-    for (int j = 0; OUTS && j < a.n_out; ++j) {
-        uint16_t* o = static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k;
-        if (ANY)
-            ss::st_any16(o, p);
-        else
-            ss::st_stream_u4(o, p);
-    }
-    return p;
-}
-
-// Fused copy-in at any gradient offset, N <= 8, one vector per thread q of
-// the CTA part; every lane of a warp holding a vector calls it.  Rank r's
-// gradient run starts sh_r bytes past a 16-byte boundary; block b of the run
-// is the 16 bytes at (run start - sh_r + 16b), and vector q is blocks q and
-// q + 1 joined by funnel shifts.  Thread q loads only block q of each rank
-// and takes block q + 1 from lane + 1 by a shuffle.  Lane 31 fetches its
-// successor blocks with cp.async into its own slots of shared memory -- no
-// registers, issued with the other loads -- and waits only for its own
-// copies, so warps stay independent.  A thread thus holds one 16-byte
-// register group per rank, as the aligned path does (two per rank before the
-// join would not fit all loads in flight).  Block q is loaded only for
-// q <= nvec and block q + 1 only for a vector q < nvec; each holds bytes of
-// the run, so no load leaves the run's 16-byte blocks.  Returns the new bf16
-// vector (valid threads).
-template <int NR>
-__device__ __forceinline__ uint4 step_vec_copyin_warp(const StepArgs& a, const PtrTab& tab,
-                                                      int slot, int64_t f0, int64_t k0, int q,
-                                                      int nvec) {
-    __shared__ uint4 s_next[kThreads / 32][kMaxVec];
-    const int n = NR > 0 ? NR : a.N;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const bool valid = q < nvec;
-    const int64_t f = f0 + 8 * (int64_t)q;
-    auto run_of = [&](int r) {
-        return reinterpret_cast<const unsigned char*>(
-            static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k0);
-    };
-    uint4 w[kMaxVec];
-    uint32_t shs = 0;  // sh_r / 2 of every rank, 3 bits each
-#pragma unroll
-    for (int r = 0; r < kMaxVec; ++r) {
-        if (r < n) {
-            const unsigned char* run = run_of(r);
-            const int sh = (int)(reinterpret_cast<uintptr_t>(run) & 15u);
-            shs |= (uint32_t)(sh >> 1) << (3 * r);
-            w[r] = (sh ? q <= nvec : valid) ? ss::ld_stream_u4(run - sh + 16 * (int64_t)q)
-                                            : make_uint4(0, 0, 0, 0);
-        }
-    }
-    if (lane == 31 && valid) {
-#pragma unroll
-        for (int r = 0; r < kMaxVec; ++r) {
-            if (r < n) {
-                const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
-                if (sh) {
-                    const unsigned char* run = run_of(r);
-                    const unsigned dst = (unsigned)__cvta_generic_to_shared(&s_next[warp][r]);
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                                 "l"(run - sh + 16 * (int64_t)(q + 1))
-                                 : "memory");
-                }
-            }
-        }
-    }
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 t0 = z4, t1 = z4, m0 = z4, m1 = z4, v0 = z4, v1 = z4;
-    if (valid) {
-        t0 = ss::ld_rw_f4(a.master + f);
-        t1 = ss::ld_rw_f4(a.master + f + 4);
-        m0 = ss::ld_rw_f4(a.exp_avg + f);
-        m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
-        v0 = ss::ld_rw_f4(a.exp_avg_sq + f);
-        v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
-    }
-    if (lane == 31) asm volatile("cp.async.wait_all;" ::: "memory");
-#pragma unroll
-    for (int r = 0; r < kMaxVec; ++r) {
-        if (r < n) {
-            uint4 nb;
-            nb.x = __shfl_down_sync(0xFFFFFFFFu, w[r].x, 1);
-            nb.y = __shfl_down_sync(0xFFFFFFFFu, w[r].y, 1);
-            nb.z = __shfl_down_sync(0xFFFFFFFFu, w[r].z, 1);
-            nb.w = __shfl_down_sync(0xFFFFFFFFu, w[r].w, 1);
-            const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
-            if (lane == 31 && sh && valid) nb = s_next[warp][r];
-            if (sh) w[r] = ss::realign16(w[r], nb, sh);
-        }
-    }
-    uint4 p = make_uint4(0, 0, 0, 0);
-    if (valid) {
-        float s[8];
-        sum_ranks<NR>(w, n, s);
-        p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
-    }
-    return p;
-}
-
 // Store bytes [lo, hi) of the 16-byte value v to blk + lo (blk 16-byte
 // aligned, lo and hi even), two bytes at a time.
 __device__ __forceinline__ void st_bytes(unsigned char* blk, uint4 v, int lo, int hi) {
@@ -309,47 +187,6 @@ __device__ __forceinline__ void st_bytes(unsigned char* blk, uint4 v, int lo, in
             const uint32_t w = b < 4 ? v.x : b < 8 ? v.y : b < 12 ? v.z : v.w;
             *reinterpret_cast<uint16_t*>(blk + b) = (uint16_t)(w >> ((b & 2) * 8));
         }
-    }
-}
-
-// The n_out per-parameter outputs of vectors q = 0..nvec-1 (one per thread,
-// thread q, nvec <= the CTA's threads), where output j's vector q goes to the
-// 16 bytes at o_j + 16q and o_j sits sh_j bytes past a 16-byte boundary.
-// Lane L takes vector q + 1 from lane L + 1 by a shuffle and writes the aligned
-// block that follows its own vector's start -- the last sh bytes of vector q
-// and the first 16 - sh of vector q + 1 -- with one 16-byte store.  Lane 31
-// and the last vector write only their own sh bytes of that block; lane 0 also
-// writes its first 16 - sh bytes into the block before, whose first sh bytes
-// belong to the previous warp's last vector (or to the scalar head).  Every
-// lane of a warp holding a vector calls this (invalid lanes pass p unused).
-template <bool UNPACKED>
-__device__ __forceinline__ void store_outputs_realigned(const StepArgs& a, const PtrTab& tab,
-                                                        int slot, int64_t k0, int q, int nvec,
-                                                        uint4 p) {
-    const int lane = threadIdx.x & 31;
-    uint4 nx;
-    nx.x = __shfl_down_sync(0xFFFFFFFFu, p.x, 1);
-    nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
-    nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
-    nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
-    if (q >= nvec) return;
-    const int goff = UNPACKED ? a.N * a.w : 0;
-    for (int j = 0; j < a.n_out; ++j) {
-        unsigned char* ob =
-            reinterpret_cast<unsigned char*>(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k0) +
-            16 * (int64_t)q;
-        const int sh = (int)(reinterpret_cast<uintptr_t>(ob) & 15u);
-        if (sh == 0) {
-            ss::st_stream_u4(ob, p);
-            continue;
-        }
-        unsigned char* blk = ob - sh + 16;  // the aligned block after this vector's start
-        const uint4 v = ss::realign16(p, nx, 16 - sh);
-        if (lane < 31 && q + 1 < nvec)
-            ss::st_stream_u4(blk, v);
-        else
-            st_bytes(blk, v, 0, sh);
-        if (lane == 0) st_bytes(blk - 16, ss::realign16(p, p, 16 - sh), sh, 16);
     }
 }
 
@@ -370,87 +207,6 @@ __device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab
     a.shards[f] = p;
     const int goff = UNPACKED ? n * a.w : 0;
     for (int j = 0; j < a.n_out; ++j) static_cast<uint16_t*>(tab.p[goff + j * a.w + slot])[k] = p;
-}
-
-// kSub CTAs per data tile (blockIdx.y): each takes one 8-element vector per
-// thread of its quarter of the tile, so CTAs stay short-lived like the flat
-// reduce-scatter kernel's.
-constexpr int kSub = ss::kTileBytes / 2 / 8 / kThreads;  // 4 for 16 KiB bf16 tiles
-static_assert(kSub * kThreads * 8 * 2 == ss::kTileBytes, "tile split");
-
-// GEN false: the host has checked that every segment is whole 16-byte vectors
-// on both sides and every per-parameter pointer is 16-byte aligned, so each
-// CTA part is aligned vectors only.  GEN true: any alignment.
-template <int NR, bool UNPACKED, bool GEN>
-__global__ void __launch_bounds__(kThreads, 3)
-fused_step_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg* __restrict__ segs,
-                  StepArgs a, PtrTab tab) {
-    constexpr int64_t T = ss::kTileBytes / 2;
-    const ss::Tile tl = tiles[t_lo + blockIdx.x];
-    const ss::Seg sg = segs[tl.seg];
-    const int64_t tile_idx = tl.idx;
-    const int64_t off = tile_idx * T;
-    const int64_t len = sg.len - off < T ? sg.len - off : T;
-    constexpr int64_t kPart = T / kSub;  // elements of this CTA's part of the tile
-    const int slot = sg.param - a.param_base;
-    const int64_t f0 = sg.packed_off + off;  // packed index of the tile's first element
-    const int64_t k0 = sg.param_off + off;   // index inside the parameter tensor
-    // this CTA's part [p0, p1) of the tile
-    const int64_t p0 = (int64_t)blockIdx.y * kPart;
-    const int64_t p1 = p0 + kPart < len ? p0 + kPart : len;
-    if (p0 >= p1) return;
-    if (!GEN) {
-        const int64_t nv = (p1 - p0) / 8;
-        for (int64_t q = threadIdx.x; q < nv; q += kThreads)
-            step_vec<NR, UNPACKED>(a, tab, slot, f0 + p0 + 8 * q, k0 + p0 + 8 * q);
-        return;
-    }
-    // GEN: the part boundaries of a segment are moved back by u = packed_off
-    // mod 8 elements, so every part but the segment's first starts on an
-    // 8-aligned packed index and every part but its last is whole vectors;
-    // the scalar head and tail (< 8 elements each) occur once per segment, not
-    // once per part, and the head runs on the last threads, which have no
-    // vector in a segment's first part.  Vectors: packed side aligned,
-    // per-parameter side aligned or realigned in registers.
-    const int64_t j = tile_idx * kSub + blockIdx.y;  // part index within the segment
-    const int64_t u = sg.packed_off & 7;
-    const int64_t e0 = j == 0 ? 0 : j * kPart - u;
-    const int64_t e1 = (j + 1) * kPart >= sg.len ? sg.len : (j + 1) * kPart - u;
-    const int64_t fs = sg.packed_off, ks = sg.param_off;
-    int64_t h = (8 - ((fs + e0) & 7)) & 7;
-    if (h > e1 - e0) h = e1 - e0;
-    const int hi_t = kThreads - 1 - (int)threadIdx.x;
-    if (hi_t < h) step_scalar<UNPACKED>(a, tab, slot, fs + e0 + hi_t, ks + e0 + hi_t);
-    const int64_t b0 = e0 + h;
-    const int64_t nvec = (e1 - b0) / 8;
-    bool aligned = true;  // every per-parameter pointer 16-byte aligned at ks + b0
-    if (UNPACKED)
-        for (int r = 0; r < a.N; ++r)
-            aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + ks + b0) & 15u) == 0);
-    const int goff = UNPACKED ? a.N * a.w : 0;
-    for (int jj = 0; jj < a.n_out; ++jj)
-        aligned &= ((reinterpret_cast<uintptr_t>(static_cast<const uint16_t*>(tab.p[goff + jj * a.w + slot]) + ks + b0) & 15u) == 0);
-    if (aligned) {
-        for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
-    } else if (nvec <= kThreads) {
-        // one vector per thread; warps holding a vector take part whole, for
-        // the shuffles of the realigned output stores
-        const int q = threadIdx.x;
-        if ((q & ~31) < nvec) {
-            uint4 p = make_uint4(0, 0, 0, 0);
-            if (UNPACKED && a.N <= kMaxVec)
-                p = step_vec_copyin_warp<NR>(a, tab, slot, fs + b0, ks + b0, q, (int)nvec);
-            else if (q < nvec)
-                p = step_vec<NR, UNPACKED, true, false>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
-            store_outputs_realigned<UNPACKED>(a, tab, slot, ks + b0, q, (int)nvec, p);
-        }
-    } else {
-        for (int64_t q = threadIdx.x; q < nvec; q += kThreads)
-            step_vec<NR, UNPACKED, true>(a, tab, slot, fs + b0 + 8 * q, ks + b0 + 8 * q);
-    }
-    for (int64_t e = b0 + 8 * nvec + threadIdx.x; e < e1; e += kThreads)
-        step_scalar<UNPACKED>(a, tab, slot, fs + e, ks + e);
 }
 
 // The plan's packed segment map on the device.
@@ -956,28 +712,6 @@ FlatAnyKern pick_flat_any(int N) {
     }
 }
 
-using Kern = void (*)(const ss::Tile*, int64_t, const ss::Seg*, StepArgs, PtrTab);
-
-template <int NR, bool U>
-Kern pick_gen(bool gen) {
-    return gen ? fused_step_kernel<NR, U, true> : fused_step_kernel<NR, U, false>;
-}
-
-// N = 2..8 get a fully unrolled instance; other N take the general one.
-template <bool U>
-Kern pick_n(int N, bool gen) {
-    switch (N) {
-        case 2: return pick_gen<2, U>(gen);
-        case 3: return pick_gen<3, U>(gen);
-        case 4: return pick_gen<4, U>(gen);
-        case 5: return pick_gen<5, U>(gen);
-        case 6: return pick_gen<6, U>(gen);
-        case 7: return pick_gen<7, U>(gen);
-        case 8: return pick_gen<8, U>(gen);
-        default: return pick_gen<0, U>(gen);
-    }
-}
-
 AdamCoef make_coef(const ss_adamw* hp) {
     AdamCoef c;
     const double t = (double)hp->step;
@@ -1055,19 +789,8 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     const int per_param = (unpacked ? N : 0) + s->n_out;
     if (per_param > kTab) return SS_EINVAL;
     const int wmax = per_param > 0 ? kTab / per_param : (pb - pa > 0 ? pb - pa : 1);
-    Kern fn = unpacked ? pick_n<true>(N, gen) : pick_n<false>(N, gen);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     PtrTab tab;
-    constexpr int64_t kMaxGrid = (int64_t)1 << 30;
-    auto launch = [&](const ss::Tile* tiles, int64_t t_lo, int64_t t_hi) -> int {
-        for (int64_t t = t_lo; t < t_hi; t += kMaxGrid) {
-            const int64_t cnt = t_hi - t < kMaxGrid ? t_hi - t : kMaxGrid;
-            fn<<<dim3((unsigned)cnt, kSub), kThreads, 0, st>>>(tiles, t, plan->d_data, a, tab);
-            int rc = ss::check_launch();
-            if (rc) return rc;
-        }
-        return SS_OK;
-    };
     auto fill = [&](int wa, int wb) {
         a.param_base = wa;
         a.w = wb - wa;
@@ -1080,56 +803,53 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                 tab.p[goff + j * a.w + (i - wa)] = s->params_out[(size_t)j * n + i];
         }
     };
-    if (!gen && pb - pa <= wmax && lo % 8 == 0 && hi % 8 == 0) {
-        // everything aligned, one pointer table: the flat form, one thread
-        // per packed vector
-        if (hi <= lo || plan->pm.empty()) return SS_OK;
-        fill(pa, pb);
-        const int64_t nvec = (hi - lo) / 8;
-        FlatRoundsKern fr = unpacked && kFlatRounds > 0 ? pick_flat_rounds(N) : nullptr;
-        if (fr) {
-            // rounds of 32 vectors per warp, as many as keep kCopyinWaves
-            // waves of CTAs (at most kFlatRounds)
-            int64_t it = nvec / ((int64_t)kThreads * kCopyinWaves * 3 * 152);
-            const int iters = (int)(it < 1 ? 1 : it > kFlatRounds ? kFlatRounds : it);
-            const int64_t span = 32 * (int64_t)iters;  // vectors per warp
-            const int64_t nw = (nvec + span - 1) / span;
-            constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
-            for (int64_t w0 = 0; w0 < nw; w0 += kChunkW) {
-                const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
-                const int64_t cv = w0 + cw >= nw ? nvec - span * w0 : span * cw;
-                fr<<<(unsigned)((cw + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
-                    plan->d_pm, plan->d_pm_block, lo + 8 * span * w0, cv, iters, a, tab);
+    // The step over packed range [rlo, rhi), whose data segments all belong to
+    // the parameters in the pointer table.
+    auto run = [&](int64_t rlo, int64_t rhi) -> int {
+        if (rhi <= rlo) return SS_OK;
+        if (!gen && rlo % 8 == 0 && rhi % 8 == 0) {
+            // everything aligned: one thread per packed vector
+            const int64_t nvec = (rhi - rlo) / 8;
+            FlatRoundsKern fr = unpacked && kFlatRounds > 0 ? pick_flat_rounds(N) : nullptr;
+            if (fr) {
+                // rounds of 32 vectors per warp, as many as keep kCopyinWaves
+                // waves of CTAs (at most kFlatRounds)
+                int64_t it = nvec / ((int64_t)kThreads * kCopyinWaves * 3 * 152);
+                const int iters = (int)(it < 1 ? 1 : it > kFlatRounds ? kFlatRounds : it);
+                const int64_t span = 32 * (int64_t)iters;  // vectors per warp
+                const int64_t nw = (nvec + span - 1) / span;
+                constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
+                for (int64_t w0 = 0; w0 < nw; w0 += kChunkW) {
+                    const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
+                    const int64_t cv = w0 + cw >= nw ? nvec - span * w0 : span * cw;
+                    fr<<<(unsigned)((cw + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
+                        plan->d_pm, plan->d_pm_block, rlo + 8 * span * w0, cv, iters, a, tab);
+                    int rc = ss::check_launch();
+                    if (rc) return rc;
+                }
+                return SS_OK;
+            }
+            FlatKern ff = unpacked ? pick_flat<true>(N) : pick_flat<false>(N);
+            constexpr int64_t kMaxBlocks = 0x7FFFFFFF;
+            for (int64_t v0 = 0; v0 < nvec; v0 += kMaxBlocks * kThreads) {
+                const int64_t cnt = nvec - v0 < kMaxBlocks * kThreads ? nvec - v0 : kMaxBlocks * kThreads;
+                ff<<<(unsigned)((cnt + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+                    plan->d_pm, plan->d_pm_block, rlo + 8 * v0, cnt, a, tab);
                 int rc = ss::check_launch();
                 if (rc) return rc;
             }
             return SS_OK;
         }
-        FlatKern ff = unpacked ? pick_flat<true>(N) : pick_flat<false>(N);
-        constexpr int64_t kMaxBlocks = 0x7FFFFFFF;
-        for (int64_t v0 = 0; v0 < nvec; v0 += kMaxBlocks * kThreads) {
-            const int64_t cnt = nvec - v0 < kMaxBlocks * kThreads ? nvec - v0 : kMaxBlocks * kThreads;
-            ff<<<(unsigned)((cnt + kThreads - 1) / kThreads), kThreads, 0, st>>>(
-                plan->d_pm, plan->d_pm_block, lo + 8 * v0, cnt, a, tab);
-            int rc = ss::check_launch();
-            if (rc) return rc;
-        }
-        return SS_OK;
-    }
-    if (pb - pa <= wmax) {
-        // any alignment, one pointer table: the flat forms with per-lane
-        // realigned output stores; whole vectors [lo8, hi8), the edges one by
-        // one
-        if (hi <= lo || plan->pm.empty()) return SS_OK;
-        fill(pa, pb);
-        const int64_t lo8 = (lo + 7) / 8 * 8, hi8 = hi / 8 * 8;
+        // any alignment: per-lane realigned output stores; whole vectors
+        // [lo8, hi8), the edges one by one
+        const int64_t lo8 = (rlo + 7) / 8 * 8, hi8 = rhi / 8 * 8;
         EdgeElems ed;
         int64_t nvec = 0;
         if (lo8 <= hi8) {
             nvec = (hi8 - lo8) / 8;
-            ed = EdgeElems{lo, hi8, (int)(lo8 - lo), (int)(hi - hi8)};
+            ed = EdgeElems{rlo, hi8, (int)(lo8 - rlo), (int)(rhi - hi8)};
         } else {  // the range lies inside one 8-element vector
-            ed = EdgeElems{lo, hi, (int)(hi - lo), 0};
+            ed = EdgeElems{rlo, rhi, (int)(rhi - rlo), 0};
         }
         const EdgeElems none{0, 0, 0, 0};
         if (unpacked) {
@@ -1173,14 +893,62 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             v0 += cnt;
         } while (v0 < nvec);
         return SS_OK;
+    };
+    if (hi <= lo || plan->pm.empty()) return SS_OK;
+    if (pb - pa <= wmax) {  // one pointer table: the whole range at once
+        fill(pa, pb);
+        return run(lo, hi);
     }
-    for (int wa = pa; wa < pb; wa += wmax) {
-        const int wb = wa + wmax < pb ? wa + wmax : pb;
-        const int s_lo = plan->param_seg[wa], s_hi = plan->param_seg[wb];
-        if (s_hi <= s_lo) continue;
+    // More parameters than one pointer table: windows of consecutive
+    // parameters, whole groups packed greedily into each (a group larger than
+    // a window is cut into windows of its own).  In packed order a window's
+    // data segments form runs broken only by segments of other parameters; a
+    // window of whole groups is one run, since groups lie side by side, while
+    // a cut group gives a run per rank shard.  Each run, pads included, is one
+    // range.
+    std::vector<std::pair<int, int>> windows;
+    {
+        const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
+        int wa = pa, wb = pa;  // the window being filled: [wa, wb)
+        for (int g = ga; g < gb; ++g) {
+            const int g0 = plan->gfirst[g], g1 = g0 + plan->gnp[g];
+            if (g1 - wa > wmax && wb > wa) {  // the group does not fit: close the window
+                windows.emplace_back(wa, wb);
+                wa = wb;
+            }
+            while (g1 - wa > wmax) {  // a group larger than a window
+                windows.emplace_back(wa, wa + wmax);
+                wa += wmax;
+            }
+            wb = g1;
+        }
+        if (wb > wa) windows.emplace_back(wa, wb);
+    }
+    const std::vector<ss::PmEntry>& pm = plan->pm;
+    const size_t m0 = (size_t)(std::lower_bound(pm.begin(), pm.end(), lo,
+                                                [](const ss::PmEntry& e, int64_t v) {
+                                                    return e.packed_off < v;
+                                                }) -
+                               pm.begin());
+    for (const auto& wnd : windows) {
+        const int wa = wnd.first, wb = wnd.second;
         fill(wa, wb);
-        int rc = launch(plan->d_data_tiles, plan->data_seg_tile[s_lo], plan->data_seg_tile[s_hi]);
-        if (rc) return rc;
+        int64_t rl = -1, rh = -1;
+        for (size_t m = m0; m < pm.size() && pm[m].packed_off < hi; ++m) {
+            if (pm[m].param >= wa && pm[m].param < wb) {
+                if (rl < 0) rl = pm[m].packed_off;
+                rh = pm[m].packed_off + pm[m].len;
+            } else if (rl >= 0) {
+                int rc = run(rl, rh);
+                if (rc) return rc;
+                rl = -1;
+            }
+        }
+        if (rl >= 0) {
+            int rc = run(rl, rh);
+            if (rc) return rc;
+        }
     }
     return SS_OK;
 }
+

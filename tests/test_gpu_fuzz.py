@@ -161,3 +161,46 @@ def test_random_plan(ss, seed):
                 np.testing.assert_array_equal(to_np(x), y, err_msg=m)
     for v, w in wholes:
         assert _intact(v, w)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_plan_parameter_windows(ss, seed):
+    # more parameters x pointers than one kernel-parameter table holds (2048):
+    # the one pass runs window by window over the packed runs of each window's
+    # segments, and must still equal the two calls bit for bit
+    rng = random.Random(5000 + seed)
+    N = rng.choice([2, 3, 7, 8, 12])
+    layout = rng.choice([W.FLAT_ORIG_FALSE, W.FLAT_ORIG_TRUE, W.PER_PARAM_DIM0])
+    n = rng.randint(90, 160)
+    shapes = [(rng.choice([0, 1, 3, 8, 17, rng.randint(1, 3000)]),) for _ in range(n)]
+    shapes[0] = (rng.randint(100, 3000),)
+    cuts = sorted(rng.sample(range(1, n), rng.randint(0, 6)))
+    groups = [b - a for a, b in zip([0] + cuts, cuts + [n])]
+    ps = W.ParamSet([f"w{i}" for i in range(n)], shapes, groups, N, layout, torch.bfloat16,
+                    seed=seed + 77)
+    su = Setup(ss, ps)
+    n_out = 24  # 24 (packed) or N + 24 (copy-in) pointers per parameter: windows of <= 85
+    numels = [p.numel() for p in su.params]
+    grads_cpu = W.make_rank_grads(ps)
+    gpk = []
+    for r in range(N):
+        b = torch.empty(su.total, dtype=torch.bfloat16, device="cuda")
+        ss.fsdp_pack(su.plan, [g.cuda() for g in grads_cpu[r]], b)
+        gpk.append(b)
+    gpp = [g.cuda().reshape(-1) for rank in grads_cpu for g in rank]
+    hp = _hp(ss, 1)
+    sa = _state(ss, su)
+    outs_a = [torch.empty(k, dtype=torch.bfloat16, device="cuda") for _ in range(n_out) for k in numels]
+    ss.fsdp_reduce_scatter_adamw(su.plan, gpk, sa[1], sa[2], sa[3], sa[0], hp)
+    ss.fsdp_all_gather_unpack(su.plan, sa[0], outs_a, n_out=n_out)
+    for src in ({"rank_grads": gpk}, {"rank_param_grads": gpp}):
+        sb = _state(ss, su)
+        outs_b = [torch.empty(k, dtype=torch.bfloat16, device="cuda") for _ in range(n_out)
+                  for k in numels]
+        ss.fsdp_sharded_step(su.plan, sb[1], sb[2], sb[3], sb[0], hp, params_out=outs_b,
+                             n_out=n_out, **src)
+        torch.cuda.synchronize()
+        for x, y in zip(sa, sb):
+            np.testing.assert_array_equal(to_np(x).view(np.uint8), to_np(y).view(np.uint8))
+        for x, y in zip(outs_a, outs_b):
+            np.testing.assert_array_equal(to_np(x), to_np(y))
