@@ -68,7 +68,7 @@ __device__ __forceinline__ void adamw_elem(float g, float& theta, float& m, floa
     theta = __fmaf_rn(-c.step_size, __fdiv_rn(m, denom), theta);
 }
 
-// Kernel arguments that do not change per tile.
+// Kernel arguments that do not change within a launch.
 struct StepArgs {
     RankPtrs packed_grads;  // [N] packed rank buffers (UNPACKED == false)
     float* master;
