@@ -159,16 +159,27 @@ ddp_bucket_kernel(const int64_t* __restrict__ prefix, const void* const* __restr
     const int64_t u_lo = prefix[o_lo], u_hi = prefix[o_hi];
     int64_t u = u_lo + (int64_t)blockIdx.x * kTile;
     const int64_t u_end = u + kTile < u_hi ? u + kTile : u_hi;
-    if (u >= u_end) return;
-    int o = warp_find(prefix, o_lo, o_hi, u);
-    while (u < u_end && o < o_hi) {
-        const int64_t t_end = prefix[o + 1];
-        const int64_t piece_end = t_end < u_end ? t_end : u_end;
-        if (piece_end > u)
-            avg_piece<NR, ANY>(ptrs + (size_t)o * (N + 1), N, u - prefix[o], piece_end - prefix[o]);
-        u = piece_end > u ? piece_end : u;
-        ++o;
+    if (u < u_end) {
+        int o = warp_find(prefix, o_lo, o_hi, u);
+        while (u < u_end && o < o_hi) {
+            const int64_t t_end = prefix[o + 1];
+            const int64_t piece_end = t_end < u_end ? t_end : u_end;
+            if (piece_end > u)
+                avg_piece<NR, ANY>(ptrs + (size_t)o * (N + 1), N, u - prefix[o],
+                                   piece_end - prefix[o]);
+            u = piece_end > u ? piece_end : u;
+            ++o;
+        }
     }
+    // This grid completes only after the previous bucket's has: its last CTA
+    // waits for that grid once its own work is done.  Completion is thus
+    // ordered along the call's buckets, and stream work after the call sees
+    // every output.  The previous grid's CTAs are all resident or finished
+    // by the time this grid starts (it launches once each of them has
+    // triggered), so the wait ends; one waiting CTA per grid costs at most
+    // one CTA slot at the tail.
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 using DdpKernel = void (*)(const int64_t*, const void* const*, int, int, int);
