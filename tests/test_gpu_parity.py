@@ -351,6 +351,33 @@ def test_ddp_full_size_sampled(ss):
     torch.cuda.empty_cache()
 
 
+def test_ddp_outputs_complete_for_work_after_the_call(ss):
+    # buckets go in reverse registration order, so the large tensor registered
+    # last is the first bucket and a tiny one the last; the next bucket's
+    # kernel starts before the previous one finishes, and work queued on the
+    # stream right after the call must still see every output complete
+    N = 8
+    numels = [3, 5, 7, 4096, 1 << 24]
+    g = torch.Generator(device="cuda").manual_seed(5)
+    grads = [[(torch.randn(n, generator=g, device="cuda") * 1e-3).to(torch.bfloat16) for n in numels]
+             for _ in range(N)]
+    for fn in (ss.ddp_bucket_pack_average, ss.ddp_bucket_pack_average_noalloc):
+        outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for n in numels]
+        for o in outs:
+            o.view(torch.int16).fill_(0x7FBF)
+        torch.cuda.synchronize()
+        cap = 64 * 1024 if fn is ss.ddp_bucket_pack_average else 1 << 20
+        nb = fn(grads, cap, outs)
+        assert nb >= 2
+        snap = [o.clone() for o in outs]   # queued behind the call, no synchronize
+        torch.cuda.synchronize()
+        for a, b in zip(snap, outs):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        want = oracle.ddp_average([[to_np(t) for t in rank] for rank in grads])
+        for o, w in zip(outs, want):
+            np.testing.assert_array_equal(to_np(o), w)
+
+
 def test_ddp_misaligned_and_odd_sizes(ss):
     # views offset by one element: pointers congruent across ranks, and not
     rng = np.random.default_rng(1)
