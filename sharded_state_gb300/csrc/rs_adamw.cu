@@ -127,16 +127,27 @@ rs_adamw_bf16_kernel(RankPtrs grads, int N, int64_t vbeg, int64_t nvec, float* _
             }
         }
         if (NR == 0) {
-            for (int r = 8; r < n; ++r) {  // ranks beyond the first 8 (N > 8)
-                uint4 x = ss::ld_stream_u4(static_cast<const uint16_t*>(grads.p[r]) + f);
-                s[0] = __fadd_rn(s[0], ss::bf16_lo(x.x));
-                s[1] = __fadd_rn(s[1], ss::bf16_hi(x.x));
-                s[2] = __fadd_rn(s[2], ss::bf16_lo(x.y));
-                s[3] = __fadd_rn(s[3], ss::bf16_hi(x.y));
-                s[4] = __fadd_rn(s[4], ss::bf16_lo(x.z));
-                s[5] = __fadd_rn(s[5], ss::bf16_hi(x.z));
-                s[6] = __fadd_rn(s[6], ss::bf16_lo(x.w));
-                s[7] = __fadd_rn(s[7], ss::bf16_hi(x.w));
+            // ranks beyond the first 8 (N > 8), 8 at a time: each batch's
+            // loads go out together into the first batch's registers, then
+            // add in rank order
+            for (int r0 = 8; r0 < n; r0 += 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (r0 + j < n)
+                        w[j] = ss::ld_stream_u4(static_cast<const uint16_t*>(grads.p[r0 + j]) + f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (r0 + j < n) {
+                        s[0] = __fadd_rn(s[0], ss::bf16_lo(w[j].x));
+                        s[1] = __fadd_rn(s[1], ss::bf16_hi(w[j].x));
+                        s[2] = __fadd_rn(s[2], ss::bf16_lo(w[j].y));
+                        s[3] = __fadd_rn(s[3], ss::bf16_hi(w[j].y));
+                        s[4] = __fadd_rn(s[4], ss::bf16_lo(w[j].z));
+                        s[5] = __fadd_rn(s[5], ss::bf16_hi(w[j].z));
+                        s[6] = __fadd_rn(s[6], ss::bf16_lo(w[j].w));
+                        s[7] = __fadd_rn(s[7], ss::bf16_hi(w[j].w));
+                    }
+                }
             }
         }
         float g[8];
@@ -213,12 +224,21 @@ rs_adamw_f32_kernel(RankPtrs grads, int N, int64_t vbeg, int64_t nvec, float* __
                 s[3] = __fadd_rn(s[3], __uint_as_float(w[r].w));
             }
         }
-        for (int r = 8; NR == 0 && r < n; ++r) {  // ranks beyond the first 8 (N > 8)
-            const uint4 x = ss::ld_stream_u4(static_cast<const float*>(grads.p[r]) + f);
-            s[0] = __fadd_rn(s[0], __uint_as_float(x.x));
-            s[1] = __fadd_rn(s[1], __uint_as_float(x.y));
-            s[2] = __fadd_rn(s[2], __uint_as_float(x.z));
-            s[3] = __fadd_rn(s[3], __uint_as_float(x.w));
+        // ranks beyond the first 8 (N > 8), 8 loads in flight at a time,
+        // added in rank order
+        for (int r0 = 8; NR == 0 && r0 < n; r0 += 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (r0 + j < n) w[j] = ss::ld_stream_u4(static_cast<const float*>(grads.p[r0 + j]) + f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (r0 + j < n) {
+                    s[0] = __fadd_rn(s[0], __uint_as_float(w[j].x));
+                    s[1] = __fadd_rn(s[1], __uint_as_float(w[j].y));
+                    s[2] = __fadd_rn(s[2], __uint_as_float(w[j].z));
+                    s[3] = __fadd_rn(s[3], __uint_as_float(w[j].w));
+                }
+            }
         }
         float g[4];
 #pragma unroll
@@ -553,16 +573,25 @@ rs_accum_kernel(RankPtrs grads, int N, int64_t vbeg, int64_t nvec, float* __rest
                 s[7] = __fadd_rn(s[7], ss::bf16_hi(w[r].w));
             }
         }
-        for (int r = 8; NR == 0 && r < n; ++r) {
-            const uint4 x = ss::ld_stream_u4(static_cast<const uint16_t*>(grads.p[r]) + f);
-            s[0] = __fadd_rn(s[0], ss::bf16_lo(x.x));
-            s[1] = __fadd_rn(s[1], ss::bf16_hi(x.x));
-            s[2] = __fadd_rn(s[2], ss::bf16_lo(x.y));
-            s[3] = __fadd_rn(s[3], ss::bf16_hi(x.y));
-            s[4] = __fadd_rn(s[4], ss::bf16_lo(x.z));
-            s[5] = __fadd_rn(s[5], ss::bf16_hi(x.z));
-            s[6] = __fadd_rn(s[6], ss::bf16_lo(x.w));
-            s[7] = __fadd_rn(s[7], ss::bf16_hi(x.w));
+        // ranks beyond the first 8 (N > 8), 8 loads in flight at a time,
+        // added in rank order
+        for (int r0 = 8; NR == 0 && r0 < n; r0 += 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (r0 + j < n) w[j] = ss::ld_stream_u4(static_cast<const uint16_t*>(grads.p[r0 + j]) + f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (r0 + j < n) {
+                    s[0] = __fadd_rn(s[0], ss::bf16_lo(w[j].x));
+                    s[1] = __fadd_rn(s[1], ss::bf16_hi(w[j].x));
+                    s[2] = __fadd_rn(s[2], ss::bf16_lo(w[j].y));
+                    s[3] = __fadd_rn(s[3], ss::bf16_hi(w[j].y));
+                    s[4] = __fadd_rn(s[4], ss::bf16_lo(w[j].z));
+                    s[5] = __fadd_rn(s[5], ss::bf16_hi(w[j].z));
+                    s[6] = __fadd_rn(s[6], ss::bf16_lo(w[j].w));
+                    s[7] = __fadd_rn(s[7], ss::bf16_hi(w[j].w));
+                }
+            }
         }
         float o[8];
 #pragma unroll

@@ -125,6 +125,25 @@ __device__ __forceinline__ void add_rank(float (&s)[8], uint4 x) {
     s[7] = __fadd_rn(s[7], ss::bf16_hi(x.w));
 }
 
+// Ranks 8 .. n-1 (N > 8) added to s in rank order, 8 loads in flight at a
+// time in w (free once the first 8 ranks are summed).  ANY: the
+// per-parameter gradients may sit at any 2-byte offset.
+template <bool UNPACKED, bool ANY = false>
+__device__ __forceinline__ void add_ranks_beyond_8(const StepArgs& a, const PtrTab& tab, int slot,
+                                                   int64_t f, int64_t k, int n,
+                                                   uint4 (&w)[kMaxVec], float (&s)[8]) {
+    for (int r0 = kMaxVec; r0 < n; r0 += kMaxVec) {
+#pragma unroll
+        for (int j = 0; j < kMaxVec; ++j)
+            if (r0 + j < n)
+                w[j] = ANY ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r0 + j, slot, f, k))
+                           : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r0 + j, slot, f, k));
+#pragma unroll
+        for (int j = 0; j < kMaxVec; ++j)
+            if (r0 + j < n) add_rank(s, w[j]);
+    }
+}
+
 // The rank sum s of 8 elements divided by n (g) and AdamW on the state loaded
 // as t/m/v, giving the new master, moments th/mm/vv.
 __device__ __forceinline__ void adam_compute(const StepArgs& a, const float (&s)[8], int n, float4 t0,
@@ -297,8 +316,7 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     }
     float s[8];
     sum_ranks<NR>(w, n, s);
-    for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
-        add_rank(s, ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r, slot, f, k)));
+    if (NR == 0) add_ranks_beyond_8<UNPACKED>(a, tab, slot, f, k, n, w, s);
     const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
     const int goff = UNPACKED ? n * a.w : 0;
     for (int j = 0; j < a.n_out; ++j)
@@ -476,8 +494,7 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         locate(mp, B, f, m, e);
         float s[8];
         sum_ranks<NR>(w, n, s);
-        for (int r = kMaxVec; NR == 0 && r < n; ++r)
-            add_rank(s, ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f));
+        if (NR == 0) add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
         if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
             key = m;
@@ -646,8 +663,7 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
         if (computes && key >= 0) {
             float s[8];
             sum_ranks<NR>(w, n, s);
-            for (int r = kMaxVec; NR == 0 && r < n; ++r)  // ranks beyond the first 8
-                add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
+            if (NR == 0) add_ranks_beyond_8<true, true>(a, tab, slot, f, k, n, w, s);
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
         } else if (computes) {  // the vector meets a segment end: element by element
             for (int i = 0; i < 8; ++i) {
