@@ -58,16 +58,25 @@ __device__ __forceinline__ uint4 mean8(const void* const* in, int N, int64_t k) 
             s[7] = __fadd_rn(s[7], ss::bf16_hi(w[r - 1].w));
         }
     } else {
-        for (int r = 1; r < n; ++r) {
-            uint4 w = ld(r);
-            s[0] = __fadd_rn(s[0], ss::bf16_lo(w.x));
-            s[1] = __fadd_rn(s[1], ss::bf16_hi(w.x));
-            s[2] = __fadd_rn(s[2], ss::bf16_lo(w.y));
-            s[3] = __fadd_rn(s[3], ss::bf16_hi(w.y));
-            s[4] = __fadd_rn(s[4], ss::bf16_lo(w.z));
-            s[5] = __fadd_rn(s[5], ss::bf16_hi(w.z));
-            s[6] = __fadd_rn(s[6], ss::bf16_lo(w.w));
-            s[7] = __fadd_rn(s[7], ss::bf16_hi(w.w));
+        // any N: ranks 1.. in batches of 8 loads in flight, added in rank order
+        for (int r0 = 1; r0 < n; r0 += 8) {
+            uint4 w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (r0 + j < n) w[j] = ld(r0 + j);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (r0 + j < n) {
+                    s[0] = __fadd_rn(s[0], ss::bf16_lo(w[j].x));
+                    s[1] = __fadd_rn(s[1], ss::bf16_hi(w[j].x));
+                    s[2] = __fadd_rn(s[2], ss::bf16_lo(w[j].y));
+                    s[3] = __fadd_rn(s[3], ss::bf16_hi(w[j].y));
+                    s[4] = __fadd_rn(s[4], ss::bf16_lo(w[j].z));
+                    s[5] = __fadd_rn(s[5], ss::bf16_hi(w[j].z));
+                    s[6] = __fadd_rn(s[6], ss::bf16_lo(w[j].w));
+                    s[7] = __fadd_rn(s[7], ss::bf16_hi(w[j].w));
+                }
+            }
         }
     }
     const float fN = (float)n;
