@@ -57,6 +57,13 @@ def _small_sets():
     big_n = W.ParamSet([f"p{i}" for i in range(5)], [(130, 3), (64,), (0, 4), (1,), (257, 2)], [5],
                        64, W.PER_PARAM_DIM0, torch.bfloat16, seed=10)
     sets.append(("per_param_N64", big_n))
+    # N > 8: the general instances read ranks beyond the first 8 in batches of
+    # 8 (one further batch at N = 12, two at N = 17), bf16 and fp32
+    for N in (12, 17):
+        for dt in (torch.bfloat16, torch.float32):
+            tag = "bf16" if dt == torch.bfloat16 else "f32"
+            sets.append((f"awkward1d_false_N{N}_{tag}", W.awkward_1d(N, W.FLAT_ORIG_FALSE, dt,
+                                                                     count=60)))
     return sets
 
 
@@ -311,9 +318,10 @@ def test_llama_1b2_full_size(ss):
 # DDP
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("N", [8, 12, 17])
 @pytest.mark.parametrize("cap", [64 << 10, 1 << 20, 25 << 20, 1 << 30])
-def test_ddp_bucket_average_bit_exact(ss, cap):
-    ds = W.ddp_grads(world_size=8, n_small=70, small=2048, n_large=6, large=65536 + 8, seed=3)
+def test_ddp_bucket_average_bit_exact(ss, cap, N):
+    ds = W.ddp_grads(world_size=N, n_small=70, small=2048, n_large=6, large=65536 + 8, seed=3)
     grads = W.make_ddp_grads(ds, device="cuda")
     outs, wholes = [], []
     for n in ds.numels:

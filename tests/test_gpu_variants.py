@@ -82,8 +82,11 @@ def test_no_master_recipe(ss, name, ps):
                                                                     ffn=136, vocab=96)),
                                      ("awkward1d_false_N3", W.awkward_1d(3, W.FLAT_ORIG_FALSE,
                                                                          torch.bfloat16, count=40,
-                                                                         max_len=300))],
-                         ids=["small_llama_N8", "awkward1d_false_N3"])
+                                                                         max_len=300)),
+                                     ("awkward1d_false_N17", W.awkward_1d(17, W.FLAT_ORIG_FALSE,
+                                                                          torch.bfloat16, count=40,
+                                                                          max_len=300))],
+                         ids=["small_llama_N8", "awkward1d_false_N3", "awkward1d_false_N17"])
 def test_gradient_accumulation(ss, name, ps, num_micro):
     su = Setup(ss, ps)
     total = su.total
