@@ -546,7 +546,7 @@ def test_dp_mlp_grads_match_autograd_and_fd():
     y = torch.nn.functional.layer_norm(o, (o.shape[1],), eps=dp_equivalence.LN_EPS) * tp["ln_w"]
     tl = 0.5 * ((y - torch.from_numpy(t)) ** 2).sum() / x.shape[0]
     tl.backward()
-    assert abs(float(tl) - loss) < 1e-12 * max(1.0, abs(loss))
+    assert abs(float(tl.detach()) - loss) < 1e-12 * max(1.0, abs(loss))
     for k in grads:
         np.testing.assert_allclose(grads[k], tp[k].grad.numpy(), rtol=1e-10, atol=1e-13)
     # one finite-difference probe per parameter tensor
