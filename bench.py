@@ -66,8 +66,9 @@ def parse_args():
     ap.add_argument("--mode", choices=["step", "rows"], default="step",
                     help="step: the one-line headline; rows: one JSON line per hot-path row")
     ap.add_argument("--rows", default="all",
-                    help="rows mode: comma list of llama,block4096,tiny,awkward,awkward_large,ddp "
-                         "(default all; awkward_large: only the large awkward sets)")
+                    help="rows mode: comma list of llama,block4096,tiny,awkward,awkward_large,"
+                         "awkward_n16,ddp (default all; awkward_large: only the large awkward "
+                         "sets; awkward_n16: the 1-D awkward set at N = 16)")
     ap.add_argument("--step-kind", default="fused", choices=["two_calls", "fused", "copy_in"],
                     help="timed step: the one-pass fsdp_sharded_step from packed gradients "
                          "(default), RS+AdamW then all-gather as two calls, or the one pass "
@@ -754,13 +755,15 @@ def run_rows(args):
     K = max(args.steps, 5)
     bits = lambda t: t.reshape(-1).cpu().view(torch.int16).numpy().view(np.uint16).copy()
     want = set(args.rows.split(",")) if args.rows != "all" else {"llama", "block4096", "tiny",
-                                                                 "awkward", "ddp"}
+                                                                 "awkward", "awkward_n16", "ddp"}
     if "llama" in want:
         _rows_llama(args, ss, oracle, peak, used, K, bits)
     if "block4096" in want:
         _rows_block4096(ss, peak, K)
     if want & {"tiny", "awkward", "awkward_large"}:
         _rows_small(ss, peak, want, args.awkward_scale)
+    if "awkward_n16" in want:
+        _rows_awkward_wide(ss, peak, args.awkward_scale)
     if "ddp" in want:
         _rows_ddp(args, ss, oracle, peak, used, K, bits)
 
@@ -1094,6 +1097,26 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
         del st5
         torch.cuda.empty_cache()
 
+
+
+def _rows_awkward_wide(ss, peak, awkward_scale=1.0):
+    # -- the 1-D awkward set at N = 16: misaligned runs with ranks beyond the
+    # first 8, which the kernels' general instances read in further batches
+    N = 16
+    ps = W.awkward_1d(N, W.FLAT_ORIG_FALSE, torch.bfloat16, count=200,
+                      max_len=int(2_000_000 * awkward_scale))
+    st = Step(ss, ps, 1)
+    P, tot = st.info["unpadded_numel"], st.info["total_numel"]
+    ms, mn = _time_stream(lambda: st.fused_step(), 20)
+    _row(f"large awkward (flat_orig_false, {P:,} params, N={N}): one-pass step", P, "params/s",
+         ms, mn, (2 * N + 26) * tot + 2 * P, peak)
+    rank_sets = list(st._rank_grad_iter("cuda"))
+    flat_pg = ss.ptr_array([g for rank in rank_sets for g in rank])
+    ms, mn = _time_stream(lambda: st.fused_step(param_grads=flat_pg), 20)
+    _row(f"large awkward (flat_orig_false, N={N}): one-pass step with fused copy-in", P,
+         "params/s", ms, mn, (2 * N + 2) * P + 26 * tot, peak)
+    del rank_sets, flat_pg, st
+    torch.cuda.empty_cache()
 
 
 def _rows_ddp(args, ss, oracle, peak, used, K, bits):
