@@ -47,6 +47,7 @@ constexpr int kTab = 2048;
 constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
 constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the flat copy-in
 constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) it keeps
+constexpr int64_t kPartVecs = (int64_t)1 << 23;  // vectors per two-pass chunk (N > 8): 256 MiB of sums
 constexpr int kFlatRounds = 4;    // most rounds per warp of the aligned flat copy-in
 
 struct RankPtrs {
@@ -564,17 +565,24 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
 // tensor's 16-byte blocks.  A vector that meets a segment end runs element by
 // element; the range's edge elements run on lanes 0..15 of warp nwarps.
 // Outputs as in fused_step_flat_any_kernel, lane 31 storing nothing.
-template <int NR>
+// PART splits the step in two passes for N > 8 (NR = 0), so that neither holds
+// more than 8 ranks' blocks beside the state: PART 1 writes the fp32 sum of
+// ranks 0..7 of each whole vector to part[f - vbeg ..] and nothing else;
+// PART 2 adds ranks 8.. to it in rank order and does the rest of the step.
+// The sum keeps its fp32 value between the passes, so the result is the
+// one-pass rank-order sum bit for bit.
+template <int NR, int PART = 0>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
                               int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, EdgeElems ed,
-                              StepArgs a, PtrTab tab) {
+                              StepArgs a, PtrTab tab, float* __restrict__ part) {
     const SegMap mp{pm, pm_block, 0};
     constexpr int kVpw = 31;  // vectors per warp and round
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int n = NR > 0 ? NR : a.N;
-    const int nr = n < kMaxVec ? n : kMaxVec;
+    const int rb = PART == 2 ? kMaxVec : 0;  // first rank this pass reads
+    const int nr = n - rb < kMaxVec ? n - rb : kMaxVec;
     const int goff = n * a.w;
     const int64_t fend = vbeg + 8 * nvec;
     // the segment of this lane's last whole vector: its end, k - f and
@@ -588,7 +596,7 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
         const bool computes = has && lane < kVpw;
         const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 t0 = z4, t1 = z4, m0 = z4, m1 = z4, v0 = z4, v1 = z4;
-        if (computes) {
+        if (PART != 1 && computes) {
             t0 = ss::ld_rw_f4(a.master + f);
             t1 = ss::ld_rw_f4(a.master + f + 4);
             m0 = ss::ld_rw_f4(a.exp_avg + f);
@@ -620,7 +628,7 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
                 w[r] = make_uint4(0, 0, 0, 0);
                 if (key >= 0) {
                     const unsigned char* g = reinterpret_cast<const unsigned char*>(
-                        static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k);
+                        static_cast<const uint16_t*>(tab.p[(rb + r) * a.w + slot]) + k);
                     const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
                     shs |= (uint32_t)(sh >> 1) << (3 * r);
                     w[r] = ss::ld_stream_u4(g - sh);
@@ -632,7 +640,7 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
         // computes, so the next round's loads wait for L2 rather than DRAM
         const int64_t fn = f + 8 * kVpw;
         if (it > 1 && fn < fend) {
-            if (lane < kVpw) {
+            if (PART != 1 && lane < kVpw) {
                 ss::prefetch_l2(a.master + fn);
                 ss::prefetch_l2(a.exp_avg + fn);
                 ss::prefetch_l2(a.exp_avg_sq + fn);
@@ -640,7 +648,7 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
             if (key >= 0 && fn + 8 <= hend) {
 #pragma unroll
                 for (int r = 0; r < kMaxVec; ++r)
-                    if (r < nr) ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + fn + hdelta);
+                    if (r < nr) ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[(rb + r) * a.w + slot]) + fn + hdelta);
             }
         }
 #pragma unroll
@@ -654,16 +662,37 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
                 const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
                 if (sh && computes && key >= 0 && !gnext)
                     nb = ss::ld_stream_u4(reinterpret_cast<const unsigned char*>(
-                                              static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k) -
+                                              static_cast<const uint16_t*>(tab.p[(rb + r) * a.w + slot]) + k) -
                                           sh + 16);
                 if (sh) w[r] = ss::realign16(w[r], nb, sh);
             }
         }
         uint4 p = make_uint4(0, 0, 0, 0);
+        if (PART == 1) {
+            if (computes && key >= 0) {
+                float s[8];
+                sum_ranks<NR>(w, n, s);
+                ss::st_stream_f4(part + (f - vbeg), make_float4(s[0], s[1], s[2], s[3]));
+                ss::st_stream_f4(part + (f - vbeg) + 4, make_float4(s[4], s[5], s[6], s[7]));
+            }
+            continue;  // vectors meeting a segment end and the edges: PART 2
+        }
         if (computes && key >= 0) {
             float s[8];
-            sum_ranks<NR>(w, n, s);
-            if (NR == 0) add_ranks_beyond_8<true, true>(a, tab, slot, f, k, n, w, s);
+            if (PART == 2) {
+                const float4 s0 = ss::ld_rw_f4(part + (f - vbeg));
+                const float4 s1 = ss::ld_rw_f4(part + (f - vbeg) + 4);
+                s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+                s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+#pragma unroll
+                for (int r = 0; r < kMaxVec; ++r)
+                    if (r < nr) add_rank(s, w[r]);
+                for (int r = 2 * kMaxVec; r < n; ++r)
+                    add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
+            } else {
+                sum_ranks<NR>(w, n, s);
+                if (NR == 0) add_ranks_beyond_8<true, true>(a, tab, slot, f, k, n, w, s);
+            }
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
         } else if (computes) {  // the vector meets a segment end: element by element
             for (int i = 0; i < 8; ++i) {
@@ -684,7 +713,7 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
             store_outputs_lane(a, tab, goff, slot, k, p, nx, lane < kVpw - 1 && nkey == key,
                                lane > 0 && pkey == key);
     }
-    if (gw == nwarps && lane < 16) {
+    if (PART != 1 && gw == nwarps && lane < 16) {
         const int i = lane;
         if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
             const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
@@ -697,7 +726,7 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
 }
 
 using FlatCopyinKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int,
-                                EdgeElems, StepArgs, PtrTab);
+                                EdgeElems, StepArgs, PtrTab, float*);
 
 FlatCopyinKern pick_flat_copyin(int N) {
     switch (N) {
@@ -872,27 +901,49 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             // rounds of 31 vectors per warp, as many rounds per warp as keep
             // kCopyinWaves waves of CTAs (at most kCopyinIters), and one
             // extra warp for the edges
+            // Beyond 8 ranks, two passes per chunk of warps (kPartVecs vectors,
+            // 32 B of fp32 partial sums each, in a stream-ordered scratch).
+            const bool two = N > kMaxVec;
             FlatCopyinKern fc = pick_flat_copyin(N);
             const int64_t per_round = 31 * (int64_t)(kThreads / 32);  // vectors per CTA round
             int64_t it = nvec / (per_round * kCopyinWaves * 3 * 152);
             const int iters = (int)(it < 1 ? 1 : it > kCopyinIters ? kCopyinIters : it);
             const int64_t span = 31 * (int64_t)iters;  // vectors per warp
             const int64_t nw = (nvec + span - 1) / span;
-            constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
+            const int64_t kChunkW = two ? (kPartVecs + span - 1) / span : (int64_t)1 << 32;
+            float* part = nullptr;
+            if (two && nvec > 0) {
+                const int64_t pv = nvec < span * kChunkW ? nvec : span * kChunkW;
+                cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&part), (size_t)pv * 32, st);
+                if (e != cudaSuccess) return ss::cuda_fail(e);
+            }
             int64_t w0 = 0;
+            int rc = SS_OK;
             do {
                 const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
                 const bool last = w0 + cw >= nw;
                 const int64_t cv = last ? nvec - span * w0 : span * cw;
                 const int64_t warps = cw + (last ? 1 : 0);
-                fc<<<(unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32)), kThreads, 0, st>>>(
+                const unsigned grid = (unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32));
+                if (two && cv > 0) {
+                    fused_step_flat_copyin_kernel<0, 1><<<grid, kThreads, 0, st>>>(
+                        plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv, cw, iters, none, a,
+                        tab, part);
+                    rc = ss::check_launch();
+                    if (rc) break;
+                }
+                (two ? fused_step_flat_copyin_kernel<0, 2> : fc)<<<grid, kThreads, 0, st>>>(
                     plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv, cw, iters,
-                    last ? ed : none, a, tab);
-                int rc = ss::check_launch();
-                if (rc) return rc;
+                    last ? ed : none, a, tab, part);
+                rc = ss::check_launch();
+                if (rc) break;
                 w0 += cw;
             } while (w0 < nw);
-            return SS_OK;
+            if (part) {
+                cudaError_t e = cudaFreeAsync(part, st);
+                if (e != cudaSuccess && rc == SS_OK) rc = ss::cuda_fail(e);
+            }
+            return rc;
         }
         FlatAnyKern ff = pick_flat_any(N);
         constexpr int64_t kChunk = (int64_t)0x7FFFFFF0 * kThreads;  // vectors per launch
