@@ -362,6 +362,54 @@ def test_sharded_step_full_size_copy_in_equals_pack_and_two_calls(ss):
     torch.cuda.empty_cache()
 
 
+def test_sharded_step_copy_in_two_pass_chunks_equal_pack_and_two_calls(ss):
+    """Per-parameter gradients at N = 9 on a misaligned plan of about 80M
+    params: the copy-in runs in two passes (ranks 0..7 summed into fp32
+    scratch, then rank 8 and AdamW) over more than one chunk of 8M vectors,
+    and must equal packing each set and running the two calls bit for bit."""
+    ps = W.awkward_1d(9, W.FLAT_ORIG_FALSE, torch.bfloat16, count=40, max_len=4_500_000)
+    su = Setup(ss, ps, make_values=False)
+    total, N = su.total, su.N
+    assert total // 8 > (1 << 23) + 248  # more than one chunk
+    gen = torch.Generator(device="cuda").manual_seed(45)
+    init = (torch.randn(total, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+    sets = [[(torch.randn(s, device="cuda", generator=gen) * 1e-3).to(torch.bfloat16)
+             for s in ps.shapes] for _ in range(N)]
+    res = []
+    for mode in ("pack_two_calls", "copy_in"):
+        shards = init.clone()
+        master = torch.empty(total, device="cuda")
+        m = torch.empty_like(master)
+        v = torch.empty_like(master)
+        ss.fsdp_init_master(su.plan, shards, master, m, v)
+        outs = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in ps.shapes]
+        hp = ss.adamw_params(step=1)
+        if mode == "pack_two_calls":
+            packed = []
+            for r in range(N):
+                b = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+                ss.fsdp_pack(su.plan, sets[r], b)
+                packed.append(b)
+            ss.fsdp_reduce_scatter_adamw(su.plan, packed, master, m, v, shards, hp)
+            ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+            torch.cuda.synchronize()
+            del packed
+        else:
+            ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp,
+                                 rank_param_grads=[g for rank in sets for g in rank],
+                                 params_out=outs, n_out=1)
+            torch.cuda.synchronize()
+        res.append((shards, master, m, v, outs))
+    a, b = res
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    for x, y in zip(a[1:4], b[1:4]):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    for x, y in zip(a[4], b[4]):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    del res, a, b, sets
+    torch.cuda.empty_cache()
+
+
 def test_sharded_step_argument_errors(ss):
     su = Setup(ss, W.tiny_mlp())
     shards, master, m, v = _state(ss, su)
