@@ -259,13 +259,23 @@ def accumulated_grad(accum: np.ndarray, num_micro: int) -> np.ndarray:
     return out[:acc.size]
 
 
-def init_master(param_shards: np.ndarray):
+def init_master(param_shards: np.ndarray, out=None):
+    """Fresh optimizer state of a shard: (master, exp_avg, exp_avg_sq).
+    out: optional three contiguous float32 arrays of the shard's size, written
+    in place (and returned) instead of new ones."""
     lib = _load()
     eb = 2 if param_shards.dtype == np.uint16 else 4
     n = param_shards.size
-    master = np.empty(max(n, 1), np.float32)
-    m = np.empty(max(n, 1), np.float32)
-    v = np.empty(max(n, 1), np.float32)
+    if out is None:
+        master = np.empty(max(n, 1), np.float32)
+        m = np.empty(max(n, 1), np.float32)
+        v = np.empty(max(n, 1), np.float32)
+    else:
+        master, m, v = out
+        for a in out:
+            if a.dtype != np.float32 or a.size != n or not a.flags.c_contiguous:
+                raise ValueError("init_master: out must be three contiguous float32 arrays of "
+                                 "the shard's size")
     ps = np.ascontiguousarray(param_shards)
     lib.sso_init_master(n, _vp(ps), eb, _vp(master), _vp(m), _vp(v))
     return master[:n], m[:n], v[:n]

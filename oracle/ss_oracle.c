@@ -390,8 +390,10 @@ void sso_adamw(int64_t count, const float* grad, float* master, float* exp_avg,
     }
 }
 
-/* Optimizer-state initialisation for a fresh shard: the fp32 master copy is
- * the widened parameter shard, both moments start at zero. */
+/* Optimizer-state initialisation for a fresh shard ("Scaling data parallel",
+ * sections 1 and 9.1: bf16 parameters beside an fp32 master copy and fp32
+ * Adam moments; Adam's moments start at zero): the fp32 master copy is the
+ * widened parameter shard, both moments start at zero. */
 void sso_init_master(int64_t count, const void* param_shards, int elem_bytes, float* master,
                      float* exp_avg, float* exp_avg_sq) {
     for (int64_t k = 0; k < count; ++k) {

@@ -94,6 +94,19 @@ MUTANTS = [
     ("AdamW with eps inside the square root",
      "        theta = theta - lr * mhat / (sqrt(vhat) + eps);",
      "        theta = theta - lr * mhat / sqrt(vhat + eps);"),
+    # optimizer-state initialisation
+    ("init: exp_avg left as it was, not zeroed",
+     "        exp_avg[k] = 0.0f;",
+     "        (void)exp_avg;"),
+    ("init: exp_avg_sq left as it was, not zeroed",
+     "        exp_avg_sq[k] = 0.0f;",
+     "        (void)exp_avg_sq;"),
+    ("init: master widened from the bf16's upper byte only",
+     "        master[k] = elem_bytes == 2 ? bf16_to_f32(((const uint16_t*)param_shards)[k])",
+     "        master[k] = elem_bytes == 2 ? bf16_to_f32(((const uint16_t*)param_shards)[k] & 0xFF00u)"),
+    ("init: master as the integer value of the bf16 bits",
+     "        master[k] = elem_bytes == 2 ? bf16_to_f32(((const uint16_t*)param_shards)[k])",
+     "        master[k] = elem_bytes == 2 ? (float)((const uint16_t*)param_shards)[k]"),
     # accumulation
     ("accumulation returns the sum, not the mean, over micro-batches",
      "    for (int64_t f = 0; f < count; ++f) grad[f] = accum[f] / k;",

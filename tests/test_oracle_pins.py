@@ -383,6 +383,36 @@ def test_adamw_pad_stays_zero():
         assert not np.any(vv.view(np.uint32)) and not np.any(p)
 
 
+def test_init_master_widens_every_bf16_pattern_and_zeroes_the_moments():
+    """Optimizer-state initialisation ("Scaling data parallel", sections 1 and
+    9.1: an fp32 master copy of the bf16 parameters, fp32 Adam moments that
+    start at zero), pinned outside the oracle: the master is torch's bf16 ->
+    fp32 widening of every one of the 2^16 bf16 bit patterns, NaNs included,
+    bit for bit; both moments are +0.0 bit patterns, written over buffers that
+    held something else."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = (torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+            .view(np.uint32))
+    n = bits.size
+    poison = [np.full(n, np.float32(x)) for x in (np.nan, -1.5, 3.0)]
+    master, m, v = oracle.init_master(bits, out=poison)
+    np.testing.assert_array_equal(master.view(np.uint32), want)
+    assert not np.any(m.view(np.uint32)) and not np.any(v.view(np.uint32))
+
+
+def test_init_master_of_an_fp32_shard_is_the_identity():
+    """fp32 plans: the master is the shard itself, bit for bit (any pattern,
+    NaNs and signed zeros included), and the moments are +0.0."""
+    rng = np.random.default_rng(21)
+    x = rng.integers(0, 1 << 32, 1 << 16, dtype=np.uint64).astype(np.uint32)
+    x[:4] = [0x00000000, 0x80000000, 0x7F800001, 0xFFC00000]
+    shard = x.view(np.float32)
+    poison = [np.full(x.size, np.float32(x0)) for x0 in (2.0, np.nan, -7.0)]
+    master, m, v = oracle.init_master(shard, out=poison)
+    np.testing.assert_array_equal(master.view(np.uint32), x)
+    assert not np.any(m.view(np.uint32)) and not np.any(v.view(np.uint32))
+
+
 # ---------------------------------------------------------------------------
 # sharded step == unsharded step (ZeRO changes where state lives, not the math)
 # ---------------------------------------------------------------------------
