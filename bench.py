@@ -451,7 +451,10 @@ def run_native(args, world, rank, local, dist):
                         "traffic_source": "ncu capture per element x elements per launch "
                                           "(profiles/ncu_traffic.json)",
                         "per_unit_bytes": 2 * N + 26 + (2 * args.n_out if fused else 0),
-                        "units_per_launch": total},
+                        "units_per_launch": total,
+                        # how many times the K steps were timed again after a
+                        # host stall (0: this is the first timing)
+                        "retimed": retimed},
            "gpu_launches": launches, "clocks": clk, "retimed": retimed}
     if retimed:
         out["retime_reason"] = ("a step in an earlier timing took over 5x the median step: a host "
@@ -581,80 +584,130 @@ def _host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def _oracle_sample_from_step(st: Step):
-    """Block group 0 of the workload, copied from the device buffers."""
+def _host_free_bytes() -> int:
+    try:
+        return os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 0
+
+
+def _oracle_group0_from_step(st: Step) -> dict:
+    """Group 0 of a step's device buffers, copied to the host, in the form
+    _oracle_step takes (the rows' per-row oracle timings)."""
     import sharded_state_gb300 as ss
     grp = ss.fsdp_plan_group(st.plan, 0)
     base, span = grp["base"], st.N * grp["shard_numel"]
     a, b = grp["first_param"], grp["first_param"] + grp["num_params"]
     sl = slice(base, base + span)
     to_u16 = lambda t: t[sl].cpu().view(torch.int16).numpy().view(np.uint16).copy()
-    return {"grads": [to_u16(g) for g in st.grads], "master": st.master[sl].cpu().numpy().copy(),
-            "m": st.m[sl].cpu().numpy().copy(), "v": st.v[sl].cpu().numpy().copy(),
-            "shard_numel": grp["shard_numel"], "params": a, "params_end": b, "span": span}
+    g0 = {"grads": [to_u16(g) for g in st.grads], "master": st.master[sl].cpu().numpy().copy(),
+          "m": st.m[sl].cpu().numpy().copy(), "v": st.v[sl].cpu().numpy().copy(),
+          "shard_numel": grp["shard_numel"], "params": a, "params_end": b, "span": span}
+    return {"groups": [g0], "whole": False, "params": int(sum(st.ps.numels()[a:b]))}
 
 
-def _oracle_sample_cpu(ps: W.ParamSet):
-    """Block group 0 of the workload, drawn on the host (reference arm)."""
+def _oracle_config(ps: W.ParamSet) -> dict:
+    """The whole workload on the host for the oracle: every group with its own
+    fp32 master (the widened bf16 parameters), exp_avg and exp_avg_sq, so one
+    oracle step touches every parameter of the model once.  Inputs are drawn
+    once per distinct group shape and shared by the groups of that shape (the
+    24 blocks of the Llama-shaped model share one draw): the oracle's work and
+    bytes per step are the whole model's, only the random values repeat.  If
+    the state would take more than half the host's free memory, only the
+    first group is kept, and `whole` says so."""
     import oracle
-    g0 = ps.groups[0]
     d0, inner = ps.dim0_inner()
-    lay = oracle.layout(ps.layout, ps.world_size, 2, d0[:g0], inner[:g0])
-    span = lay["total_numel"]
+    N = ps.world_size
+    spans, first = [], 0
+    for cnt in ps.groups:
+        lay = oracle.layout(ps.layout, N, 2, d0[first:first + cnt], inner[first:first + cnt])
+        spans.append((first, first + cnt, lay["shard_numel"], lay["total_numel"]))
+        first += cnt
+    state_bytes = 14 * sum(sp[3] for sp in spans)
+    whole = state_bytes <= _host_free_bytes() // 2
+    if not whole:
+        spans = spans[:1]
     gen = torch.Generator().manual_seed(ps.seed)
-    params = (torch.randn(span, generator=gen) * ps.param_std).to(ps.dtype)
-    master = params.float().numpy().copy()
-    grads = [(torch.randn(span, generator=gen) * ps.grad_std).to(ps.dtype)
-             .view(torch.int16).numpy().view(np.uint16).copy() for _ in range(ps.world_size)]
-    return {"grads": grads, "master": master, "m": np.zeros(span, np.float32),
-            "v": np.zeros(span, np.float32), "shard_numel": lay["shard_numel"], "params": 0,
-            "params_end": g0, "span": span}
+    drawn, groups = {}, []
+    for a, b, shard, span in spans:
+        key = (tuple(d0[a:b]), tuple(inner[a:b]))
+        if key not in drawn:
+            params = (torch.randn(span, generator=gen) * ps.param_std).to(ps.dtype)
+            grads = [(torch.randn(span, generator=gen) * ps.grad_std).to(ps.dtype)
+                     .view(torch.int16).numpy().view(np.uint16) for _ in range(N)]
+            drawn[key] = (params.float().numpy(), grads)
+        master0, grads = drawn[key]
+        groups.append({"params": a, "params_end": b, "shard_numel": shard, "span": span,
+                       "grads": grads, "master": master0.copy(), "m": np.zeros(span, np.float32),
+                       "v": np.zeros(span, np.float32)})
+    P = sum(int(sum(ps.numels()[g["params"]:g["params_end"]])) for g in groups)
+    return {"groups": groups, "whole": whole, "params": P}
 
 
-def _oracle_step(ps: W.ParamSet, smp: dict, t: int):
+def _oracle_step(ps: W.ParamSet, cfg: dict, t: int, groups=None) -> int:
+    """One oracle step over the kept groups: reduce-scatter + AdamW of every
+    rank's shard, then the all-gather + unpack.  Returns the parameters it
+    updated."""
     import oracle
     hp = W.adamw_hparams(t)
     d0, inner = ps.dim0_inner()
-    a, b = smp["params"], smp["params_end"]
-    shards, _ = oracle.reduce_scatter_adamw(
-        ps.world_size, smp["shard_numel"], smp["grads"], smp["master"], smp["m"], smp["v"],
-        **{k: hp[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")})
-    oracle.all_gather_unpack(ps.layout, ps.world_size, 2, d0[a:b], inner[a:b], shards)
-    return int(sum(ps.numels()[a:b]))
+    done = 0
+    for g in (cfg["groups"] if groups is None else groups):
+        a, b = g["params"], g["params_end"]
+        shards, _ = oracle.reduce_scatter_adamw(
+            ps.world_size, g["shard_numel"], g["grads"], g["master"], g["m"], g["v"],
+            **{k: hp[k] for k in ("lr", "beta1", "beta2", "eps", "weight_decay", "step")})
+        oracle.all_gather_unpack(ps.layout, ps.world_size, 2, d0[a:b], inner[a:b], shards)
+        done += int(sum(ps.numels()[a:b]))
+    return done
+
+
+def _oracle_sample_text(ps: W.ParamSet, cfg: dict) -> str:
+    if cfg["whole"]:
+        return (f"the whole workload per step: all {len(cfg['groups'])} groups, "
+                f"{cfg['params']:,} params, each group with its own optimizer state; "
+                f"inputs drawn on the host once per group shape")
+    return (f"group 0 only ({cfg['params']:,} params) per step: the whole workload's state "
+            f"would take more than half the host's free memory")
 
 
 def cpu_baseline(st: Step, ps: W.ParamSet, args) -> dict:
+    """The oracle as written on the host's cores: whole-workload steps for
+    args.cpu_seconds (at least one), then the definitional single-thread run
+    on group 0 of the same inputs for half that time."""
     import oracle
     cores = _host_cores()
     oracle.set_threads(cores)
-    smp = _oracle_sample_from_step(st)
     used = cores if oracle.has_openmp() else 1
+    cfg = _oracle_config(ps)
     t0 = time.perf_counter()
     reps, params = 0, 0
     while True:
-        params += _oracle_step(ps, smp, 1000 + reps)
+        params += _oracle_step(ps, cfg, 1000 + reps)
         reps += 1
         if time.perf_counter() - t0 >= args.cpu_seconds:
             break
     dt = time.perf_counter() - t0
-    out = {"value": params / dt, "unit": "params/s", "cores": used, "kind": "oracle",
-           "sample": f"block group 0 ({params // reps:,} params, N={ps.world_size}) of the same "
-                     f"workload, {reps} oracle RS+AdamW+AG steps, inputs copied from the device "
-                     f"buffers, {dt:.1f} s"}
-    # the definitional oracle on one thread, on the same sample (half the budget)
+    # the definitional oracle on one thread, on group 0 (half the budget)
     oracle.set_threads(1)
-    t0 = time.perf_counter()
+    g0 = cfg["groups"][:1]
+    t1 = time.perf_counter()
     reps1, params1 = 0, 0
     while True:
-        params1 += _oracle_step(ps, smp, 5000 + reps1)
+        params1 += _oracle_step(ps, cfg, 5000 + reps1, groups=g0)
         reps1 += 1
-        if time.perf_counter() - t0 >= args.cpu_seconds / 2:
+        if time.perf_counter() - t1 >= args.cpu_seconds / 2:
             break
-    dt1 = time.perf_counter() - t0
+    dt1 = time.perf_counter() - t1
     oracle.set_threads(cores)
-    out["single_thread"] = {"value": params1 / dt1, "unit": "params/s", "cores": 1,
-                            "sample": f"the same sample, {reps1} steps, {dt1:.1f} s"}
-    return out
+    single = params1 / dt1
+    return {"value": params / dt, "unit": "params/s", "cores": used, "kind": "oracle",
+            "sample": f"{_oracle_sample_text(ps, cfg)}; {reps} oracle RS+AdamW+AG steps in "
+                      f"{dt:.1f} s on {used} threads. One thread (the definitional oracle): "
+                      f"{single:.4g} params/s on group 0 ({params1 // reps1:,} params), "
+                      f"{reps1} steps in {dt1:.1f} s",
+            "single_thread": {"value": single, "unit": "params/s", "cores": 1,
+                              "sample": f"group 0, {reps1} steps, {dt1:.1f} s"}}
 
 
 def run_reference(args, world, rank):
@@ -665,29 +718,40 @@ def run_reference(args, world, rank):
     cores = _host_cores()
     oracle.set_threads(cores)
     used = cores if oracle.has_openmp() else 1
-    smp = _oracle_sample_cpu(ps)
+    cfg = _oracle_config(ps)
     for w in range(max(args.warmup, 0)):
-        _oracle_step(ps, smp, w + 1)
+        _oracle_step(ps, cfg, w + 1)
     t0 = time.perf_counter()
     params = 0
     for k in range(args.steps):
-        params += _oracle_step(ps, smp, args.warmup + k + 1)
+        params += _oracle_step(ps, cfg, args.warmup + k + 1)
     dt = time.perf_counter() - t0
-    d0, inner = ps.dim0_inner()
-    info = {"unpadded_numel": ps.total_unpadded(), "total_numel": ps.total_unpadded()}
+    info = {"unpadded_numel": ps.total_unpadded(), "total_numel": _packed_numel(ps)}
     value = params / dt
-    sample = (f"block group 0 ({params // max(args.steps, 1):,} params, N={ps.world_size}) per "
-              f"step, drawn on the host; {args.steps} timed oracle RS+AdamW+AG steps")
+    sample = f"{_oracle_sample_text(ps, cfg)}; {args.steps} timed oracle RS+AdamW+AG steps"
     out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": dt / max(args.steps, 1) * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-           "impl": "reference", "config": workload_config(ps, info, args.n_out),
+           "impl": "reference",
+           "config": dict(workload_config(ps, info, args.n_out), step_kind=args.step_kind),
            "cpu_baseline": {"value": value, "unit": "params/s", "cores": used, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
+
+
+def _packed_numel(ps: W.ParamSet) -> int:
+    """Elements of one packed buffer of the workload's plan (the oracle's layout)."""
+    import oracle
+    d0, inner = ps.dim0_inner()
+    total, first = 0, 0
+    for cnt in ps.groups:
+        total += oracle.layout(ps.layout, ps.world_size, 2, d0[first:first + cnt],
+                               inner[first:first + cnt])["total_numel"]
+        first += cnt
+    return total
 
 
 # ---------------------------------------------------------------------------
@@ -810,7 +874,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
 
     del packed
     rs_ms, rs_mn = _time_stream(lambda: st.rs_adamw(), K)
-    smp = _oracle_sample_from_step(st)
+    smp = _oracle_group0_from_step(st)
     t_cpu, reps = _time_cpu(lambda: _oracle_step(ps, smp, 10_000), args.cpu_seconds / 2)
     _row(f"a3 reduce-scatter + AdamW ({tag} model, N=8)", P, "params/s", rs_ms, rs_mn,
          (2 * N + 26) * total, peak,

@@ -377,7 +377,9 @@ int fsdp_sharded_step(const ss_plan* plan, const ss_step* step, int group, ss_st
  *   num_buckets_out   nullable: receives the bucket count.
  * The call stages a per-call table of pointers and sizes in device memory
  * obtained with cudaMallocAsync on `stream` and released with cudaFreeAsync
- * after the launches.
+ * after the launches.  The table is copied there from host memory that lives
+ * only for the call, so a stream that is being captured into a CUDA graph is
+ * refused with SS_EINVAL before anything is queued.
  * Errors: SS_EINVAL, SS_EALIGN, SS_ENOMEM, SS_ECUDA.
  */
 int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* numels,
@@ -403,12 +405,16 @@ int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* nume
  *
  * The call allocates no device memory and calls no allocating library
  * routine.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  Every call overwrites the whole
- * table it uses, so nothing has to be cleared between calls, but all calls
- * share the one array: calls whose work can overlap on the GPU (different
- * streams without ordering between them, or several host threads) race on
- * it and must be serialised by the caller.
+ * (cudaGetSymbolAddress, with that device current) and keeps it together with
+ * the id of the current CUDA context; a call under another context (after
+ * cudaDeviceReset, say) looks it up again.  As for ddp_bucket_pack_average,
+ * the table is copied from host memory that lives only for the call, so a
+ * stream that is being captured is refused with SS_EINVAL.  Every call
+ * overwrites the whole table it uses, so nothing has to be cleared between
+ * calls, and calls queued one after another on one stream are ordered by it.
+ * All calls share the one array, though: calls whose work can overlap on the
+ * GPU (different streams without ordering between them, or several host
+ * threads) race on it and must be serialised by the caller.
  */
 #define SS_DDP_NOALLOC_TABLE_BYTES (256u * 1024u)
 int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors, const int64_t* numels,

@@ -16,6 +16,7 @@
 // first tensor with a warp-level search over the bucket-order prefix sums of
 // the tensor sizes.  The per-tensor pointers and those prefix sums go to the
 // device in a per-call table.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -240,6 +241,21 @@ bool needs_realign(const void* const* ptrs, int N, int o) {
 
 }  // namespace
 
+namespace {
+
+// The bucket table goes to the device with a copy from host memory that lives
+// only for the call.  A stream capture would record that copy with the host
+// address and replay it after the memory is gone, so both entry points refuse
+// a capturing stream: SS_EINVAL, before any work is queued.
+int refuse_capture(cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return ss::cuda_fail(e);
+    return cs == cudaStreamCaptureStatusNone ? SS_OK : SS_EINVAL;
+}
+
+}  // namespace
+
 extern "C" {
 
 int ddp_bucket_assign(int num_tensors, const int64_t* numels, int elem_bytes,
@@ -278,6 +294,8 @@ int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* nume
             if (!ss::aligned(q, 2)) return SS_EALIGN;
         }
     }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (int crc = refuse_capture(st)) return crc;
     std::vector<int> bucket_of((size_t)(T > 0 ? T : 1));
     const int nb = ddp_bucket_assign(T, numels, 2, bucket_cap_bytes, bucket_of.data());
     if (nb < 0) return nb;
@@ -301,7 +319,6 @@ int ddp_bucket_pack_average(int world_size, int num_tensors, const int64_t* nume
     }
     bucket_start[nb] = T;
 
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void* d_table = nullptr;
     cudaError_t e = cudaMallocAsync(&d_table, host.size(), st);
     if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? SS_ENOMEM : ss::cuda_fail(e);
@@ -344,10 +361,48 @@ namespace {
 
 constexpr int kMaxDevicesNoalloc = 64;
 
-// Device address of the array, looked up once per device (host code cannot use
-// the symbol itself: on the host it names a stand-in, not device memory).
+// Device address of the array, looked up with the device current and kept per
+// device together with the unique id of the CUDA context it was looked up in
+// (host code cannot use the symbol itself: on the host it names a stand-in,
+// not device memory).  A different context on the same device -- after
+// cudaDeviceReset, or a context the caller made current -- loads its own copy
+// of the library's module at another address, so a changed id means a new
+// lookup.
+struct NoallocAddr {
+    unsigned long long ctx_id;
+    void* addr;
+};
 std::mutex g_noalloc_mutex;
-void* g_noalloc_addr[kMaxDevicesNoalloc] = {nullptr};
+NoallocAddr g_noalloc_addr[kMaxDevicesNoalloc] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context, 0 if there is none or the
+// driver cannot tell (then the address is looked up again on every call).
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 int noalloc_table_address(void** out) {
     int dev = -1;
@@ -355,13 +410,17 @@ int noalloc_table_address(void** out) {
     if (e != cudaSuccess) return ss::cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevicesNoalloc) return SS_EINVAL;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
+    const unsigned long long id = current_ctx_id();
+    NoallocAddr& c = g_noalloc_addr[dev];
+    if (id == 0 || c.ctx_id != id || !c.addr) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_ddp_noalloc_table);
         if (e != cudaSuccess) return ss::cuda_fail(e);
-        g_noalloc_addr[dev] = p;
+        // the lookup makes the device's context current if none was
+        c.ctx_id = current_ctx_id();
+        c.addr = p;
     }
-    *out = g_noalloc_addr[dev];
+    *out = c.addr;
     return SS_OK;
 }
 
@@ -391,6 +450,8 @@ extern "C" int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors,
             if (!ss::aligned(q, 2)) return SS_EALIGN;
         }
     }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (int crc = refuse_capture(st)) return crc;
     void* d_table = nullptr;
     int rc = noalloc_table_address(&d_table);
     if (rc) return rc;
@@ -416,7 +477,6 @@ extern "C" int ddp_bucket_pack_average_noalloc(int world_size, int num_tensors,
     }
     bucket_start[nb] = T;
 
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(d_table, host.data(), table_bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return ss::cuda_fail(e);
     const int64_t* d_prefix = static_cast<const int64_t*>(d_table);

@@ -48,6 +48,18 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Asynchronous 16-byte copy global -> shared (cp.async, L2 only, 256-byte
+// L2 fetch); smem is a shared-window address, both 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* g) {
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(smem), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most K of this thread's committed groups are still in flight.
+template <int K>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
+}
+
 // Streaming 128-bit stores (evict-first).
 __device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
     asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),

@@ -34,6 +34,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <utility>
 #include <vector>
 
@@ -47,7 +48,6 @@ constexpr int kTab = 2048;
 constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
 constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the flat copy-in
 constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) it keeps
-constexpr int64_t kPartVecs = (int64_t)1 << 23;  // vectors per two-pass chunk (N > 8): 256 MiB of sums
 constexpr int kFlatRounds = 4;    // most rounds per warp of the aligned flat copy-in
 
 struct RankPtrs {
@@ -548,55 +548,65 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
     }
 }
 
+// Shared-memory staging of the fused copy-in: per warp, rank and round, the
+// aligned 16-byte blocks that cover the warp's 32 vectors (33 when the
+// gradient tensor's run is not 16-byte aligned), ranks in batches of 8.
+constexpr int kStageBlocks = 33;
+constexpr int kStageBatch = 8;
+constexpr int kStagedWarps = kThreads / 32;
+
+__host__ __device__ constexpr int staged_bufs(int NR) { return NR > 0 ? 1 : 2; }
+__host__ __device__ constexpr int staged_smem_bytes(int NR) {
+    return kStagedWarps * staged_bufs(NR) * kStageBatch * kStageBlocks * 16;
+}
+
 // Flat form of the one-pass step with per-parameter gradients (fused
-// copy-in) at any alignment.  Warp gw takes `iters` rounds of 31 consecutive
-// 8-aligned packed vectors, round it holding q = 31 * (gw * iters + it) +
-// lane; lane 31 looks up and loads the next round's first vector without
-// computing it.  A lane keeps the segment of its last vector: while the next
-// vector lies inside it, the vector is placed with no lookup, so its
-// gradient loads go out with its state loads; otherwise it looks the segment
-// up in the packed segment map.  A lane whose vector lies inside one segment
-// loads, per rank, the one aligned 16-byte block that holds the vector's
-// first bytes; when the next lane's vector is the next one of the same
-// segment, that lane's block is this vector's second block and arrives by a
-// shuffle, so a warp inside one segment reads each gradient block once.  Only
-// a lane at a segment end loads its second block itself, after the shuffle.
-// Both blocks hold bytes of the vector, so no load leaves the gradient
-// tensor's 16-byte blocks.  A vector that meets a segment end runs element by
-// element; the range's edge elements run on lanes 0..15 of warp nwarps.
-// Outputs as in fused_step_flat_any_kernel, lane 31 storing nothing.
-// PART splits the step in two passes for N > 8 (NR = 0), so that neither holds
-// more than 8 ranks' blocks beside the state: PART 1 writes the fp32 sum of
-// ranks 0..7 of each whole vector to part[f - vbeg ..] and nothing else;
-// PART 2 adds ranks 8.. to it in rank order and does the rest of the step.
-// The sum keeps its fp32 value between the passes, so the result is the
-// one-pass rank-order sum bit for bit.
-template <int NR, int PART = 0>
+// copy-in) at any alignment of the runs and the pointers, for any N, in one
+// pass.  Warp gw takes `iters` rounds of 32 consecutive 8-aligned packed
+// vectors, lane = vector; a lane keeps the segment of its last vector and
+// looks it up in the packed segment map only when it leaves it.  When every
+// vector of the round lies in one segment (all but the rounds that meet a
+// segment end), the warp's gradient bytes of rank r are one contiguous run of
+// the rank's tensor: the warp copies the aligned 16-byte blocks covering it
+// into shared memory with cp.async -- lane l block l, lane 0 also the 33rd --
+// so nothing is held in registers per rank, and each lane reads its own 16
+// bytes back from its two blocks, shifted into place.  Ranks go in batches of
+// 8 (NR = N <= 8: one batch); with more, two batches are in flight while the
+// earlier one is summed, and a buffer is refilled only after every lane has
+// read it.  The sum runs in rank order from rank 0's value, as everywhere.
+// Rounds that meet a segment end load each vector inside one segment
+// straight from global memory (ld_any16) and run the others element by
+// element.  Every block read holds at least one byte of the run, so no load
+// leaves the gradient tensor's 16-byte blocks.  Outputs as in
+// fused_step_flat_any_kernel; the range's edge elements run on lanes 0..15 of
+// warp nwarps.
+template <int NR>
 __global__ void __launch_bounds__(kThreads, 3)
-fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
-                              int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, EdgeElems ed,
-                              StepArgs a, PtrTab tab, float* __restrict__ part) {
+fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
+                                int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, EdgeElems ed,
+                                StepArgs a, PtrTab tab) {
+    extern __shared__ uint4 stage[];
     const SegMap mp{pm, pm_block, 0};
-    constexpr int kVpw = 31;  // vectors per warp and round
+    constexpr unsigned kAll = 0xFFFFFFFFu;
+    constexpr int kBufBlocks = kStageBatch * kStageBlocks;  // one batch of ranks
     const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int wib = threadIdx.x >> 5;
+    const int64_t gw = (int64_t)blockIdx.x * kStagedWarps + wib;
     const int n = NR > 0 ? NR : a.N;
-    const int rb = PART == 2 ? kMaxVec : 0;  // first rank this pass reads
-    const int nr = n - rb < kMaxVec ? n - rb : kMaxVec;
+    const int nbat = (n + kStageBatch - 1) / kStageBatch;
+    const uint4* wst = stage + (size_t)wib * staged_bufs(NR) * kBufBlocks;
+    const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
     const int goff = n * a.w;
     const int64_t fend = vbeg + 8 * nvec;
-    // the segment of this lane's last whole vector: its end, k - f and
-    // parameter slot, and its map index (hkey < 0: none)
-    int64_t hend = 0, hdelta = 0;
-    int hslot = 0, hkey = -1;
-    int64_t f = vbeg + 8 * (gw * iters * kVpw + lane);
-    for (int it = gw < nwarps ? iters : 0; it > 0; --it, f += 8 * kVpw) {
-        if (__shfl_sync(0xFFFFFFFFu, f, 0) >= fend) break;  // the same for the whole warp
+    int64_t hend = 0, hdelta = 0;  // the lane's last segment: its end and k - f,
+    int hslot = 0, hkey = -1;      // its parameter slot and map index (-1: none)
+    int64_t f = vbeg + 8 * (gw * iters * 32 + lane);
+    for (int it = gw < nwarps ? iters : 0; it > 0; --it, f += 8 * 32) {
+        if (__shfl_sync(kAll, f, 0) >= fend) break;  // the same for the whole warp
         const bool has = f < fend;
-        const bool computes = has && lane < kVpw;
         const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 t0 = z4, t1 = z4, m0 = z4, m1 = z4, v0 = z4, v1 = z4;
-        if (PART != 1 && computes) {
+        if (has) {
             t0 = ss::ld_rw_f4(a.master + f);
             t1 = ss::ld_rw_f4(a.master + f + 4);
             m0 = ss::ld_rw_f4(a.exp_avg + f);
@@ -616,85 +626,96 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
             }
         }
         const int key = has ? hkey : -1, slot = hslot;
-        const int64_t k = f + hdelta;
-        const int nkey = __shfl_down_sync(0xFFFFFFFFu, key, 1);
-        const int pkey = __shfl_up_sync(0xFFFFFFFFu, key, 1);
-        const bool gnext = lane < 31 && key >= 0 && nkey == key;
-        uint4 w[kMaxVec];
-        uint32_t shs = 0;  // sh_r / 2 of every rank, 3 bits each
+        const int64_t k = f + hdelta;  // index inside the parameter tensor
+        const int key0 = __shfl_sync(kAll, key, 0);
+        const bool uniform = __all_sync(kAll, !has || (key0 >= 0 && key == key0));
+        uint4 p = make_uint4(0, 0, 0, 0);
+        if (uniform) {
+            const int nl = __popc(__ballot_sync(kAll, has));  // lanes 0..nl-1 hold vectors
+            const int64_t k0 = __shfl_sync(kAll, k, 0);
+            const int slot0 = __shfl_sync(kAll, slot, 0);
+            // ranks 8b .. 8b+7 into buffer b % 2: the blocks under the warp's run
+            auto issue = [&](int b) {
+                const uint32_t buf = wst_s + (uint32_t)((b % staged_bufs(NR)) * kBufBlocks * 16);
 #pragma unroll
-        for (int r = 0; r < kMaxVec; ++r) {
-            if (r < nr) {
-                w[r] = make_uint4(0, 0, 0, 0);
-                if (key >= 0) {
-                    const unsigned char* g = reinterpret_cast<const unsigned char*>(
-                        static_cast<const uint16_t*>(tab.p[(rb + r) * a.w + slot]) + k);
-                    const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
-                    shs |= (uint32_t)(sh >> 1) << (3 * r);
-                    w[r] = ss::ld_stream_u4(g - sh);
+                for (int j = 0; j < kStageBatch; ++j) {
+                    const int r = b * kStageBatch + j;
+                    if (r < n) {
+                        const unsigned char* g = reinterpret_cast<const unsigned char*>(
+                            static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) + k0);
+                        const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
+                        const unsigned char* base = g - sh;
+                        const int nblk = nl + (sh ? 1 : 0);
+                        const uint32_t dst = buf + (uint32_t)(j * kStageBlocks * 16);
+                        if (lane < nblk) ss::cp_async16(dst + 16 * lane, base + 16 * lane);
+                        if (lane + 32 < nblk) ss::cp_async16(dst + 16 * (lane + 32), base + 16 * (lane + 32));
+                    }
                 }
-            }
-        }
-        // the lane's next vector, 31 vectors on: its state and (when it stays
-        // in this segment) its first gradient blocks into L2 while this round
-        // computes, so the next round's loads wait for L2 rather than DRAM
-        const int64_t fn = f + 8 * kVpw;
-        if (it > 1 && fn < fend) {
-            if (PART != 1 && lane < kVpw) {
+                ss::cp_async_commit();
+            };
+            float s[8];
+            __syncwarp();  // every lane has read the last round's buffers
+            issue(0);
+            if (NR == 0 && nbat > 1) issue(1);
+            // the lane's next vector, 32 on: its state and (when it stays in
+            // this segment) its first batch's gradient lines into L2 while
+            // this round computes, so the next round's copies wait for L2
+            // rather than DRAM
+            const int64_t fn = f + 8 * 32;
+            if (it > 1 && fn < fend) {
                 ss::prefetch_l2(a.master + fn);
                 ss::prefetch_l2(a.exp_avg + fn);
                 ss::prefetch_l2(a.exp_avg_sq + fn);
-            }
-            if (key >= 0 && fn + 8 <= hend) {
+                if (fn + 8 <= hend) {
 #pragma unroll
-                for (int r = 0; r < kMaxVec; ++r)
-                    if (r < nr) ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[(rb + r) * a.w + slot]) + fn + hdelta);
+                    for (int r = 0; r < kStageBatch; ++r)
+                        if (r < n)
+                            ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) + fn +
+                                            hdelta);
+                }
             }
-        }
+            for (int b = 0; b < (NR > 0 ? 1 : nbat); ++b) {
+                if (NR == 0 && b + 1 < nbat)
+                    ss::cp_async_wait<1>();
+                else
+                    ss::cp_async_wait<0>();
+                __syncwarp();
+                const uint4* buf = wst + (b % staged_bufs(NR)) * kBufBlocks;
 #pragma unroll
-        for (int r = 0; r < kMaxVec; ++r) {
-            if (r < nr) {
-                uint4 nb;
-                nb.x = __shfl_down_sync(0xFFFFFFFFu, w[r].x, 1);
-                nb.y = __shfl_down_sync(0xFFFFFFFFu, w[r].y, 1);
-                nb.z = __shfl_down_sync(0xFFFFFFFFu, w[r].z, 1);
-                nb.w = __shfl_down_sync(0xFFFFFFFFu, w[r].w, 1);
-                const int sh = (int)((shs >> (3 * r)) & 7u) * 2;
-                if (sh && computes && key >= 0 && !gnext)
-                    nb = ss::ld_stream_u4(reinterpret_cast<const unsigned char*>(
-                                              static_cast<const uint16_t*>(tab.p[(rb + r) * a.w + slot]) + k) -
-                                          sh + 16);
-                if (sh) w[r] = ss::realign16(w[r], nb, sh);
+                for (int j = 0; j < kStageBatch; ++j) {
+                    const int r = b * kStageBatch + j;
+                    if (r < n && lane < nl) {
+                        const unsigned char* g = reinterpret_cast<const unsigned char*>(
+                            static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) + k0);
+                        const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
+                        const uint4* blk = buf + j * kStageBlocks + lane;
+                        uint4 x = blk[0];
+                        if (sh) x = ss::realign16(x, blk[1], sh);
+                        if (r == 0) {
+                            s[0] = ss::bf16_lo(x.x); s[1] = ss::bf16_hi(x.x);
+                            s[2] = ss::bf16_lo(x.y); s[3] = ss::bf16_hi(x.y);
+                            s[4] = ss::bf16_lo(x.z); s[5] = ss::bf16_hi(x.z);
+                            s[6] = ss::bf16_lo(x.w); s[7] = ss::bf16_hi(x.w);
+                        } else {
+                            add_rank(s, x);
+                        }
+                    }
+                }
+                if (NR == 0 && b + 2 < nbat) {
+                    __syncwarp();  // every lane has read the buffer it refills
+                    issue(b + 2);
+                }
             }
-        }
-        uint4 p = make_uint4(0, 0, 0, 0);
-        if (PART == 1) {
-            if (computes && key >= 0) {
-                float s[8];
-                sum_ranks<NR>(w, n, s);
-                ss::st_stream_f4(part + (f - vbeg), make_float4(s[0], s[1], s[2], s[3]));
-                ss::st_stream_f4(part + (f - vbeg) + 4, make_float4(s[4], s[5], s[6], s[7]));
-            }
-            continue;  // vectors meeting a segment end and the edges: PART 2
-        }
-        if (computes && key >= 0) {
-            float s[8];
-            if (PART == 2) {
-                const float4 s0 = ss::ld_rw_f4(part + (f - vbeg));
-                const float4 s1 = ss::ld_rw_f4(part + (f - vbeg) + 4);
-                s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
-                s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
-#pragma unroll
-                for (int r = 0; r < kMaxVec; ++r)
-                    if (r < nr) add_rank(s, w[r]);
-                for (int r = 2 * kMaxVec; r < n; ++r)
-                    add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
-            } else {
-                sum_ranks<NR>(w, n, s);
-                if (NR == 0) add_ranks_beyond_8<true, true>(a, tab, slot, f, k, n, w, s);
-            }
+            if (lane < nl) p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
+        } else if (key >= 0) {  // a round that meets a segment end: this vector is inside one
+            const uint16_t* g0 = static_cast<const uint16_t*>(tab.p[slot]) + k;
+            const uint4 x = ss::ld_any16(g0);
+            float s[8] = {ss::bf16_lo(x.x), ss::bf16_hi(x.x), ss::bf16_lo(x.y), ss::bf16_hi(x.y),
+                          ss::bf16_lo(x.z), ss::bf16_hi(x.z), ss::bf16_lo(x.w), ss::bf16_hi(x.w)};
+            for (int r = 1; r < n; ++r)
+                add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
-        } else if (computes) {  // the vector meets a segment end: element by element
+        } else if (has) {  // the vector meets a segment end: element by element
             for (int i = 0; i < 8; ++i) {
                 const int64_t x = f + i;
                 int c;
@@ -704,16 +725,18 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
                                       ex.param_off + (x - ex.packed_off));
             }
         }
+        const int nkey = __shfl_down_sync(kAll, key, 1);
+        const int pkey = __shfl_up_sync(kAll, key, 1);
         uint4 nx;
-        nx.x = __shfl_down_sync(0xFFFFFFFFu, p.x, 1);
-        nx.y = __shfl_down_sync(0xFFFFFFFFu, p.y, 1);
-        nx.z = __shfl_down_sync(0xFFFFFFFFu, p.z, 1);
-        nx.w = __shfl_down_sync(0xFFFFFFFFu, p.w, 1);
-        if (computes && key >= 0)
-            store_outputs_lane(a, tab, goff, slot, k, p, nx, lane < kVpw - 1 && nkey == key,
+        nx.x = __shfl_down_sync(kAll, p.x, 1);
+        nx.y = __shfl_down_sync(kAll, p.y, 1);
+        nx.z = __shfl_down_sync(kAll, p.z, 1);
+        nx.w = __shfl_down_sync(kAll, p.w, 1);
+        if (key >= 0)
+            store_outputs_lane(a, tab, goff, slot, k, p, nx, lane < 31 && nkey == key,
                                lane > 0 && pkey == key);
     }
-    if (PART != 1 && gw == nwarps && lane < 16) {
+    if (gw == nwarps && lane < 16) {
         const int i = lane;
         if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
             const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
@@ -725,20 +748,46 @@ fused_step_flat_copyin_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
     }
 }
 
-using FlatCopyinKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int,
-                                EdgeElems, StepArgs, PtrTab, float*);
+using StagedKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int,
+                            EdgeElems, StepArgs, PtrTab);
 
-FlatCopyinKern pick_flat_copyin(int N) {
+StagedKern pick_staged(int N, int* smem) {
+    StagedKern k;
     switch (N) {
-        case 2: return fused_step_flat_copyin_kernel<2>;
-        case 3: return fused_step_flat_copyin_kernel<3>;
-        case 4: return fused_step_flat_copyin_kernel<4>;
-        case 5: return fused_step_flat_copyin_kernel<5>;
-        case 6: return fused_step_flat_copyin_kernel<6>;
-        case 7: return fused_step_flat_copyin_kernel<7>;
-        case 8: return fused_step_flat_copyin_kernel<8>;
-        default: return fused_step_flat_copyin_kernel<0>;
+        case 1: k = fused_step_copyin_staged_kernel<1>; break;
+        case 2: k = fused_step_copyin_staged_kernel<2>; break;
+        case 3: k = fused_step_copyin_staged_kernel<3>; break;
+        case 4: k = fused_step_copyin_staged_kernel<4>; break;
+        case 5: k = fused_step_copyin_staged_kernel<5>; break;
+        case 6: k = fused_step_copyin_staged_kernel<6>; break;
+        case 7: k = fused_step_copyin_staged_kernel<7>; break;
+        case 8: k = fused_step_copyin_staged_kernel<8>; break;
+        default: k = fused_step_copyin_staged_kernel<0>; break;
     }
+    *smem = N <= kStageBatch ? staged_smem_bytes(1) : staged_smem_bytes(0);
+    return k;
+}
+
+// Opt the staged kernels into their shared memory (above the 48 KiB default
+// for N > 8) and the largest shared-memory carveout, once per device.
+int staged_prepare(StagedKern k, int smem) {
+    static std::mutex mu;
+    static std::vector<std::pair<int, StagedKern>> done;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return ss::cuda_fail(e);
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& d : done)
+        if (d.first == dev && d.second == k) return SS_OK;
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return ss::cuda_fail(e);
+    done.emplace_back(dev, k);
+    return SS_OK;
 }
 
 using FlatAnyKern = void (*)(const ss::PmEntry*, const int*, int, int64_t, int64_t, EdgeElems,
@@ -898,52 +947,33 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         }
         const EdgeElems none{0, 0, 0, 0};
         if (unpacked) {
-            // rounds of 31 vectors per warp, as many rounds per warp as keep
+            // rounds of 32 vectors per warp, as many rounds per warp as keep
             // kCopyinWaves waves of CTAs (at most kCopyinIters), and one
             // extra warp for the edges
-            // Beyond 8 ranks, two passes per chunk of warps (kPartVecs vectors,
-            // 32 B of fp32 partial sums each, in a stream-ordered scratch).
-            const bool two = N > kMaxVec;
-            FlatCopyinKern fc = pick_flat_copyin(N);
-            const int64_t per_round = 31 * (int64_t)(kThreads / 32);  // vectors per CTA round
+            int smem = 0;
+            const StagedKern fk = pick_staged(N, &smem);
+            int rc = staged_prepare(fk, smem);
+            if (rc) return rc;
+            const int64_t per_round = 32 * (int64_t)kStagedWarps;  // vectors per CTA round
             int64_t it = nvec / (per_round * kCopyinWaves * 3 * 152);
             const int iters = (int)(it < 1 ? 1 : it > kCopyinIters ? kCopyinIters : it);
-            const int64_t span = 31 * (int64_t)iters;  // vectors per warp
+            const int64_t span = 32 * (int64_t)iters;  // vectors per warp
             const int64_t nw = (nvec + span - 1) / span;
-            const int64_t kChunkW = two ? (kPartVecs + span - 1) / span : (int64_t)1 << 32;
-            float* part = nullptr;
-            if (two && nvec > 0) {
-                const int64_t pv = nvec < span * kChunkW ? nvec : span * kChunkW;
-                cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&part), (size_t)pv * 32, st);
-                if (e != cudaSuccess) return ss::cuda_fail(e);
-            }
+            constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
             int64_t w0 = 0;
-            int rc = SS_OK;
             do {
                 const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
                 const bool last = w0 + cw >= nw;
                 const int64_t cv = last ? nvec - span * w0 : span * cw;
                 const int64_t warps = cw + (last ? 1 : 0);
-                const unsigned grid = (unsigned)((warps + kThreads / 32 - 1) / (kThreads / 32));
-                if (two && cv > 0) {
-                    fused_step_flat_copyin_kernel<0, 1><<<grid, kThreads, 0, st>>>(
-                        plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv, cw, iters, none, a,
-                        tab, part);
-                    rc = ss::check_launch();
-                    if (rc) break;
-                }
-                (two ? fused_step_flat_copyin_kernel<0, 2> : fc)<<<grid, kThreads, 0, st>>>(
-                    plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv, cw, iters,
-                    last ? ed : none, a, tab, part);
+                const unsigned grid = (unsigned)((warps + kStagedWarps - 1) / kStagedWarps);
+                fk<<<grid, kThreads, smem, st>>>(plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv,
+                                                 cw, iters, last ? ed : none, a, tab);
                 rc = ss::check_launch();
-                if (rc) break;
+                if (rc) return rc;
                 w0 += cw;
             } while (w0 < nw);
-            if (part) {
-                cudaError_t e = cudaFreeAsync(part, st);
-                if (e != cudaSuccess && rc == SS_OK) rc = ss::cuda_fail(e);
-            }
-            return rc;
+            return SS_OK;
         }
         FlatAnyKern ff = pick_flat_any(N);
         constexpr int64_t kChunk = (int64_t)0x7FFFFFF0 * kThreads;  // vectors per launch

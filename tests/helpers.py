@@ -45,11 +45,41 @@ def header_functions() -> list:
 # fp32 ulps can differ by at most one bf16 ulp.
 RTOL = 1e-6
 
+# How much of the tolerance each check used, one record per call, printed by
+# the terminal summary in conftest.py: per array the largest error relative to
+# the oracle's result, and how many elements lie beyond a strict 1e-6 of the
+# result (the bound the operand-relative one replaces where terms cancel) or
+# beyond one bf16 ulp.
+MARGINS = []
+
+
+def _case() -> str:
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+
+
+def _result_relative(gpu, ref):
+    """|gpu - ref| / |ref| per element (0 where both are equal, inf where ref
+    is 0 and gpu is not)."""
+    d = np.abs(gpu - ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(d == 0, 0.0, d / np.abs(ref))
+    return np.nan_to_num(r, nan=np.inf)
+
+
+def _record(kind, n, **fields):
+    MARGINS.append(dict(case=_case(), kind=kind, n=int(n), **fields))
+
 
 def check_adamw_state(gpu_master, gpu_m, gpu_v, ref_master, ref_m, ref_v, prev_master, prev_m,
                       grad):
     gm = np.asarray(gpu_master, np.float64)
     rm = np.asarray(ref_master, np.float64)
+    rel = {name: _result_relative(np.asarray(g, np.float64), np.asarray(r, np.float64))
+           for name, g, r in (("master", gpu_master, ref_master), ("exp_avg", gpu_m, ref_m),
+                              ("exp_avg_sq", gpu_v, ref_v))}
+    _record("state", gm.size,
+            **{f"max_rel_{k}": float(v.max(initial=0.0)) for k, v in rel.items()},
+            **{f"n_beyond_1e-6_{k}": int((v > RTOL).sum()) for k, v in rel.items()})
     scale = np.abs(np.asarray(prev_master, np.float64)) + np.abs(rm)
     bad = np.abs(gm - rm) > RTOL * scale
     assert not bad.any(), f"master: {bad.sum()} elements beyond tolerance, first at {np.argmax(bad)}"
@@ -109,6 +139,8 @@ def check_bf16_close(gpu_bits, ref_bits, ref_master, prev_master):
     gpu_bits = np.asarray(gpu_bits, np.uint16)
     d = bf16_ulp_distance(gpu_bits, np.asarray(ref_bits, np.uint16))
     far = d > 1
+    _record("bf16", d.size, max_ulp=int(d.max(initial=0)), n_beyond_1_ulp=int(far.sum()),
+            n_off_by_1_ulp=int((d == 1).sum()))
     if not far.any():
         return 0
     rm = np.asarray(ref_master, np.float64)[far]

@@ -41,6 +41,9 @@ CASES = [("tiny_mlp", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
          # and N = 16 (ranks beyond the first 8 read one by one)
          ("awkward1d_false_N1", W.awkward_1d(1, W.FLAT_ORIG_FALSE, torch.bfloat16, count=60)),
          ("awkward2d_N16", W.awkward_2d(16, count=60)),
+         # misaligned at N = 17 and 24: ranks beyond the first 16 as well
+         ("awkward1d_false_N17", W.awkward_1d(17, W.FLAT_ORIG_FALSE, torch.bfloat16, count=60)),
+         ("awkward1d_true_N24", W.awkward_1d(24, W.FLAT_ORIG_TRUE, torch.bfloat16, count=60)),
          ("small_llama_N3", W.llama_1b2(world_size=3, layers=3, hidden=40, ffn=72, vocab=100)),
          ("small_llama_N8", W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)),
          # aligned plans for the flat kernel's general instance (N = 12 with pads, N = 1)
@@ -257,8 +260,17 @@ def test_prepared_step_equals_the_call(ss):
                        rank_grads=packed, params_out=outs_b, n_out=1)(0)  # step 0: EINVAL
 
 
-def test_sharded_step_state_against_oracle(ss):
-    ps = W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)
+ORACLE_STATE_CASES = [
+    ("small_llama_N8", W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)),
+    ("awkward1d_false_N7", W.awkward_1d(7, W.FLAT_ORIG_FALSE, torch.bfloat16, count=80)),
+    ("awkward1d_false_N17", W.awkward_1d(17, W.FLAT_ORIG_FALSE, torch.bfloat16, count=60)),
+    ("awkward1d_true_N24", W.awkward_1d(24, W.FLAT_ORIG_TRUE, torch.bfloat16, count=60))]
+
+
+@pytest.mark.parametrize("name,ps", ORACLE_STATE_CASES, ids=[c[0] for c in ORACLE_STATE_CASES])
+def test_sharded_step_state_against_oracle(ss, name, ps):
+    """The fused copy-in (per-parameter gradients) against the oracle over
+    three steps: aligned (N = 8) and misaligned runs (N = 7, 17, 24)."""
     su = Setup(ss, ps)
     N, total = su.N, su.total
     shards, master, m, v = _state(ss, su)
@@ -313,6 +325,96 @@ def test_sharded_step_full_size_equals_two_calls(ss):
     for x, y in zip(a[4], b[4]):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
     del res, a, b, grads
+    torch.cuda.empty_cache()
+
+
+def _per_param_places(su, idx: np.ndarray):
+    """Parameter and element index of packed elements idx (sorted) of a
+    PER_PARAM_DIM0 plan, from the oracle's layout of each group: rank r's chunk
+    of parameter i holds rows r*c_i .. r*c_i + c_i - 1 from shard offset off_i
+    on ("FSDP1 vs FSDP2", section 03: FSDP2's per-parameter dim-0 chunks).
+    Returns (param, k), param -1 for a pad element."""
+    assert su.kind == W.PER_PARAM_DIM0
+    param = np.full(idx.size, -1, np.int64)
+    k = np.zeros(idx.size, np.int64)
+    for g, grp in enumerate(su.groups):
+        a, b, d0, inner = su._group_args(g)
+        lay = oracle.layout(su.kind, su.N, 2, d0, inner)
+        S = lay["shard_numel"]
+        lo, hi = np.searchsorted(idx, [grp["base"], grp["base"] + su.N * S])
+        rel = idx[lo:hi] - grp["base"]
+        r, local = rel // S, rel % S
+        off = np.asarray(lay["offsets"], np.int64)
+        rows = np.asarray(lay["chunk_rows"], np.int64)
+        inn = np.asarray(inner, np.int64)
+        d0 = np.asarray(d0, np.int64)
+        i = np.searchsorted(off, local, side="right") - 1
+        # empty parameters share their offset with the next one: take the
+        # last parameter starting at or before `local` that holds elements
+        j = local - off[i]
+        row = r * rows[i] + j // np.maximum(inn[i], 1)
+        inside = (j < rows[i] * inn[i]) & (row < d0[i])
+        param[lo:hi] = np.where(inside, a + i, -1)
+        k[lo:hi] = np.where(inside, row * inn[i] + j % np.maximum(inn[i], 1), 0)
+    return param, k
+
+
+def test_headline_step_full_size_against_the_oracle(ss):
+    """The launch the benchmark times -- fsdp_sharded_step over the whole
+    1.2B-shaped model (N = 8, packed gradients, n_out = 1) -- checked against
+    the oracle in one test, over two steps: on 2M sampled packed elements the
+    reduce-scatter + AdamW state and bf16 shard against
+    oracle.reduce_scatter_adamw applied to the sampled inputs ("Scaling data
+    parallel", sections 9.1-9.3: reduce-scatter, then AdamW on each rank's own
+    shard in fp32, then the cast), and the unpacked output of every sampled
+    data element against the same bf16 value ("FSDP1 vs FSDP2", section 04:
+    the group all-gather returns every parameter whole)."""
+    ps = W.llama_1b2()
+    su = Setup(ss, ps, make_values=False)
+    total, N = su.total, su.N
+    assert total == 1_364_297_728 and N == 8
+    gen = torch.Generator(device="cuda").manual_seed(4)
+    shards = (torch.randn(total, device="cuda", generator=gen) * ps.param_std).to(torch.bfloat16)
+    master = torch.empty(total, device="cuda")
+    m = torch.empty_like(master)
+    v = torch.empty_like(master)
+    ss.fsdp_init_master(su.plan, shards, master, m, v)
+    grads = W.make_packed_rank_grads(N, total, ps.grad_std, ps.seed, device="cuda")
+    outs = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in ps.shapes]
+    sgen = torch.Generator(device="cuda").manual_seed(4242)
+    idx_t = torch.unique(torch.randint(0, total, (1 << 21,), device="cuda", generator=sgen))
+    idx_t = idx_t[:idx_t.numel() // N * N]
+    idx = idx_t.cpu().numpy()
+    param, k = _per_param_places(su, idx)
+    data = param >= 0
+    assert data.all()  # every dim0 of this model divides by 8: no pads
+    for step in (1, 2):
+        in_master = master[idx_t].cpu().numpy()
+        in_m = m[idx_t].cpu().numpy()
+        in_v = v[idx_t].cpu().numpy()
+        in_g = [to_np(gr[idx_t]) for gr in grads]
+        launches = ss.ss_launch_count()
+        ss.fsdp_sharded_step(su.plan, master, m, v, shards, ss.adamw_params(step=step, **_hp(step)),
+                             rank_grads=grads, params_out=outs, n_out=1)
+        torch.cuda.synchronize()
+        assert ss.ss_launch_count() - launches == 1  # the one flat launch
+        om, omm, ov = in_master.copy(), in_m.copy(), in_v.copy()
+        o_params, o_red = oracle.reduce_scatter_adamw(N, idx.size // N, in_g, om, omm, ov,
+                                                      step=step, **_hp(step))
+        g_master = master[idx_t].cpu().numpy()
+        check_adamw_state(g_master, m[idx_t].cpu().numpy(), v[idx_t].cpu().numpy(), om, omm, ov,
+                          in_master, in_m, o_red)
+        g_shard = to_np(shards[idx_t])
+        check_bf16_params(g_shard, o_params, g_master, om, in_master)
+        # the unpacked outputs hold the same bf16 values, parameter by parameter
+        got = np.empty(idx.size, np.uint16)
+        for i in np.unique(param):
+            sel = np.nonzero(param == i)[0]
+            flat = outs[i].reshape(-1)
+            assert k[sel].min() >= 0 and k[sel].max() < flat.numel()  # checked on the host
+            got[sel] = to_np(flat[torch.from_numpy(k[sel]).to("cuda")])
+        np.testing.assert_array_equal(got, g_shard)
+    del grads, outs
     torch.cuda.empty_cache()
 
 
