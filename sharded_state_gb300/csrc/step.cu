@@ -81,6 +81,8 @@ struct StepArgs {
     int n_out;
     int param_base;  // first parameter of this launch's window
     int w;           // parameters in the window
+    int congruent;   // per-parameter gradients: every rank's pointer of every
+                     // parameter in the window has the same address mod 16
     AdamCoef c;
 };
 
@@ -560,6 +562,116 @@ __host__ __device__ constexpr int staged_smem_bytes(int NR) {
     return kStagedWarps * staged_bufs(NR) * kStageBatch * kStageBlocks * 16;
 }
 
+// Element E (0..15) of the 32 bytes x0:x1 as fp32: the low or high half of
+// word E / 2 (bf16 -> fp32 is exact).
+template <int E>
+__device__ __forceinline__ float elem_at(const uint4& x0, const uint4& x1) {
+    constexpr int w = E >> 1;
+    const uint32_t v = w == 0 ? x0.x : w == 1 ? x0.y : w == 2 ? x0.z : w == 3 ? x0.w
+                     : w == 4 ? x1.x : w == 5 ? x1.y : w == 6 ? x1.z : x1.w;
+    return (E & 1) ? ss::bf16_hi(v) : ss::bf16_lo(v);
+}
+
+// A lane's 8 gradient elements of one rank, read from its staged blocks
+// blk[0], blk[1] at element offset H (the run's address mod 16, over 2),
+// added to s in rank order (FIRST: rank 0, s starts from its values).
+template <int H, bool FIRST>
+__device__ __forceinline__ void add_staged(float (&s)[8], const uint4* blk) {
+    const uint4 x0 = blk[0];
+    const uint4 x1 = H ? blk[1] : x0;
+#define SS_ADD_STAGED(E)                                   \
+    {                                                      \
+        const float v = elem_at<H + E>(x0, x1);            \
+        s[E] = FIRST ? v : __fadd_rn(s[E], v);             \
+    }
+    SS_ADD_STAGED(0) SS_ADD_STAGED(1) SS_ADD_STAGED(2) SS_ADD_STAGED(3)
+    SS_ADD_STAGED(4) SS_ADD_STAGED(5) SS_ADD_STAGED(6) SS_ADD_STAGED(7)
+#undef SS_ADD_STAGED
+}
+
+// The rank sum of one round of the staged copy-in, every vector of the warp
+// inside one segment: rank r's gradient bytes of the warp are the run at
+// tab[r][slot0] + k0 of 8 * nl elements.  The aligned 16-byte blocks that
+// cover it go to shared memory by cp.async (lane l block l, lane 0 also the
+// 33rd), ranks in batches of 8 (two in flight above N = 8; a buffer is
+// refilled only after every lane has read it); each lane then reads its own
+// two blocks back and adds its 8 elements to s in rank order, from rank 0's
+// value.  H >= 0: every rank's run sits at element offset H of its first
+// block (the host checked the pointers' addresses mod 16), so the elements
+// are picked straight out of the two blocks; H = -1: each rank's own offset,
+// realigned with funnel shifts.  prefetch_next runs once the first copies
+// are out.
+template <int NR, int H, typename Pre>
+__device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab, int slot0,
+                                           int64_t k0, int nl, int lane, uint32_t wst_s,
+                                           const uint4* wst, float (&s)[8], Pre prefetch_next) {
+    constexpr int kBufBlocks = kStageBatch * kStageBlocks;
+    const int n = NR > 0 ? NR : a.N;
+    const int nbat = NR > 0 ? 1 : (n + kStageBatch - 1) / kStageBatch;
+    auto run = [&](int r) {
+        return reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) +
+                                                      k0);
+    };
+    auto issue = [&](int b) {
+        const uint32_t buf = wst_s + (uint32_t)((b % staged_bufs(NR)) * kBufBlocks * 16);
+#pragma unroll
+        for (int j = 0; j < kStageBatch; ++j) {
+            const int r = b * kStageBatch + j;
+            if (r < n) {
+                const unsigned char* g = run(r);
+                const int sh = H >= 0 ? 2 * H : (int)(reinterpret_cast<uintptr_t>(g) & 15u);
+                const unsigned char* base = g - sh;
+                const int nblk = nl + (sh ? 1 : 0);
+                const uint32_t dst = buf + (uint32_t)(j * kStageBlocks * 16);
+                if (lane < nblk) ss::cp_async16(dst + 16 * lane, base + 16 * lane);
+                if (lane + 32 < nblk) ss::cp_async16(dst + 16 * (lane + 32), base + 16 * (lane + 32));
+            }
+        }
+        ss::cp_async_commit();
+    };
+    __syncwarp();  // every lane has read the last round's buffers
+    issue(0);
+    if (NR == 0 && nbat > 1) issue(1);
+    prefetch_next();
+    for (int b = 0; b < nbat; ++b) {
+        if (NR == 0 && b + 1 < nbat)
+            ss::cp_async_wait<1>();
+        else
+            ss::cp_async_wait<0>();
+        __syncwarp();
+        const uint4* buf = wst + (b % staged_bufs(NR)) * kBufBlocks;
+#pragma unroll
+        for (int j = 0; j < kStageBatch; ++j) {
+            const int r = b * kStageBatch + j;
+            if (r < n && lane < nl) {
+                const uint4* blk = buf + j * kStageBlocks + lane;
+                if constexpr (H >= 0) {
+                    if (r == 0)
+                        add_staged<H, true>(s, blk);
+                    else
+                        add_staged<H, false>(s, blk);
+                } else {
+                    const int sh = (int)(reinterpret_cast<uintptr_t>(run(r)) & 15u);
+                    uint4 x = blk[0];
+                    if (sh) x = ss::realign16(x, blk[1], sh);
+                    if (r == 0) {
+                        s[0] = ss::bf16_lo(x.x); s[1] = ss::bf16_hi(x.x);
+                        s[2] = ss::bf16_lo(x.y); s[3] = ss::bf16_hi(x.y);
+                        s[4] = ss::bf16_lo(x.z); s[5] = ss::bf16_hi(x.z);
+                        s[6] = ss::bf16_lo(x.w); s[7] = ss::bf16_hi(x.w);
+                    } else {
+                        add_rank(s, x);
+                    }
+                }
+            }
+        }
+        if (NR == 0 && b + 2 < nbat) {
+            __syncwarp();  // every lane has read the buffer it refills
+            issue(b + 2);
+        }
+    }
+}
+
 // Flat form of the one-pass step with per-parameter gradients (fused
 // copy-in) at any alignment of the runs and the pointers, for any N, in one
 // pass.  Warp gw takes `iters` rounds of 32 consecutive 8-aligned packed
@@ -593,7 +705,6 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
     const int wib = threadIdx.x >> 5;
     const int64_t gw = (int64_t)blockIdx.x * kStagedWarps + wib;
     const int n = NR > 0 ? NR : a.N;
-    const int nbat = (n + kStageBatch - 1) / kStageBatch;
     const uint4* wst = stage + (size_t)wib * staged_bufs(NR) * kBufBlocks;
     const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
     const int goff = n * a.w;
@@ -634,77 +745,41 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
             const int nl = __popc(__ballot_sync(kAll, has));  // lanes 0..nl-1 hold vectors
             const int64_t k0 = __shfl_sync(kAll, k, 0);
             const int slot0 = __shfl_sync(kAll, slot, 0);
-            // ranks 8b .. 8b+7 into buffer b % 2: the blocks under the warp's run
-            auto issue = [&](int b) {
-                const uint32_t buf = wst_s + (uint32_t)((b % staged_bufs(NR)) * kBufBlocks * 16);
-#pragma unroll
-                for (int j = 0; j < kStageBatch; ++j) {
-                    const int r = b * kStageBatch + j;
-                    if (r < n) {
-                        const unsigned char* g = reinterpret_cast<const unsigned char*>(
-                            static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) + k0);
-                        const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
-                        const unsigned char* base = g - sh;
-                        const int nblk = nl + (sh ? 1 : 0);
-                        const uint32_t dst = buf + (uint32_t)(j * kStageBlocks * 16);
-                        if (lane < nblk) ss::cp_async16(dst + 16 * lane, base + 16 * lane);
-                        if (lane + 32 < nblk) ss::cp_async16(dst + 16 * (lane + 32), base + 16 * (lane + 32));
-                    }
-                }
-                ss::cp_async_commit();
-            };
-            float s[8];
-            __syncwarp();  // every lane has read the last round's buffers
-            issue(0);
-            if (NR == 0 && nbat > 1) issue(1);
             // the lane's next vector, 32 on: its state and (when it stays in
             // this segment) its first batch's gradient lines into L2 while
             // this round computes, so the next round's copies wait for L2
             // rather than DRAM
-            const int64_t fn = f + 8 * 32;
-            if (it > 1 && fn < fend) {
-                ss::prefetch_l2(a.master + fn);
-                ss::prefetch_l2(a.exp_avg + fn);
-                ss::prefetch_l2(a.exp_avg_sq + fn);
-                if (fn + 8 <= hend) {
+            auto prefetch_next = [&]() {
+                const int64_t fn = f + 8 * 32;
+                if (it > 1 && fn < fend) {
+                    ss::prefetch_l2(a.master + fn);
+                    ss::prefetch_l2(a.exp_avg + fn);
+                    ss::prefetch_l2(a.exp_avg_sq + fn);
+                    if (fn + 8 <= hend) {
 #pragma unroll
-                    for (int r = 0; r < kStageBatch; ++r)
-                        if (r < n)
-                            ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) + fn +
-                                            hdelta);
-                }
-            }
-            for (int b = 0; b < (NR > 0 ? 1 : nbat); ++b) {
-                if (NR == 0 && b + 1 < nbat)
-                    ss::cp_async_wait<1>();
-                else
-                    ss::cp_async_wait<0>();
-                __syncwarp();
-                const uint4* buf = wst + (b % staged_bufs(NR)) * kBufBlocks;
-#pragma unroll
-                for (int j = 0; j < kStageBatch; ++j) {
-                    const int r = b * kStageBatch + j;
-                    if (r < n && lane < nl) {
-                        const unsigned char* g = reinterpret_cast<const unsigned char*>(
-                            static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) + k0);
-                        const int sh = (int)(reinterpret_cast<uintptr_t>(g) & 15u);
-                        const uint4* blk = buf + j * kStageBlocks + lane;
-                        uint4 x = blk[0];
-                        if (sh) x = ss::realign16(x, blk[1], sh);
-                        if (r == 0) {
-                            s[0] = ss::bf16_lo(x.x); s[1] = ss::bf16_hi(x.x);
-                            s[2] = ss::bf16_lo(x.y); s[3] = ss::bf16_hi(x.y);
-                            s[4] = ss::bf16_lo(x.z); s[5] = ss::bf16_hi(x.z);
-                            s[6] = ss::bf16_lo(x.w); s[7] = ss::bf16_hi(x.w);
-                        } else {
-                            add_rank(s, x);
-                        }
+                        for (int r = 0; r < kStageBatch; ++r)
+                            if (r < n)
+                                ss::prefetch_l2(static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) + fn +
+                                                hdelta);
                     }
                 }
-                if (NR == 0 && b + 2 < nbat) {
-                    __syncwarp();  // every lane has read the buffer it refills
-                    issue(b + 2);
+            };
+            float s[8];
+            if (a.congruent) {  // one element offset H for every rank: a template constant
+                const int h = (int)((reinterpret_cast<uintptr_t>(
+                                         static_cast<const uint16_t*>(tab.p[slot0]) + k0) & 15u) >> 1);
+                switch (h) {
+                    case 0: staged_sum<NR, 0>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
+                    case 1: staged_sum<NR, 1>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
+                    case 2: staged_sum<NR, 2>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
+                    case 3: staged_sum<NR, 3>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
+                    case 4: staged_sum<NR, 4>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
+                    case 5: staged_sum<NR, 5>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
+                    case 6: staged_sum<NR, 6>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
+                    default: staged_sum<NR, 7>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next); break;
                 }
+            } else {
+                staged_sum<NR, -1>(a, tab, slot0, k0, nl, lane, wst_s, wst, s, prefetch_next);
             }
             if (lane < nl) p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
         } else if (key >= 0) {  // a round that meets a segment end: this vector is inside one
@@ -888,8 +963,14 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     auto fill = [&](int wa, int wb) {
         a.param_base = wa;
         a.w = wb - wa;
+        a.congruent = 1;
         std::memset(&tab, 0, sizeof tab);
         for (int i = wa; i < wb; ++i) {
+            for (int r = 1; unpacked && r < N; ++r)
+                if (plan->numel[i] > 0 &&
+                    ((reinterpret_cast<uintptr_t>(s->rank_param_grads[(size_t)r * n + i]) ^
+                      reinterpret_cast<uintptr_t>(s->rank_param_grads[i])) & 15u))
+                    a.congruent = 0;
             for (int r = 0; unpacked && r < N; ++r)
                 tab.p[r * a.w + (i - wa)] = const_cast<void*>(s->rank_param_grads[(size_t)r * n + i]);
             const int goff = unpacked ? N * a.w : 0;
