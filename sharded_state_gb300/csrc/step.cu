@@ -83,6 +83,7 @@ struct StepArgs {
     int w;           // parameters in the window
     int congruent;   // per-parameter gradients: every rank's pointer of every
                      // parameter in the window has the same address mod 16
+    int M;           // entries of the packed segment map
     AdamCoef c;
 };
 
@@ -228,6 +229,39 @@ __device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab
     const uint16_t p = ss::f32_to_bf16(th);
     a.shards[f] = p;
     const int goff = UNPACKED ? n * a.w : 0;
+    for (int j = 0; j < a.n_out; ++j) static_cast<uint16_t*>(tab.p[goff + j * a.w + slot])[k] = p;
+}
+
+// Element x (index k of parameter slot) of a vector that meets a segment end,
+// with per-parameter gradients: the rank-order sum of its N gradients (every
+// rank's load issued before the adds, 8 at a time), then AdamW on
+// the state values th/m/v loaded with the vector, and the stores.  The same
+// operations as step_scalar.
+template <int NR>
+__device__ __forceinline__ void step_elem(const StepArgs& a, const PtrTab& tab, int slot, int64_t x,
+                                          int64_t k, float th, float m, float v) {
+    const int n = NR > 0 ? NR : a.N;
+    constexpr int kB = kMaxVec;  // loads in flight
+    float s = 0.f;
+#pragma unroll
+    for (int r0 = 0; r0 < (NR > 0 ? NR : n); r0 += kB) {
+        uint16_t h[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+            if (r0 + j < n) h[j] = static_cast<const uint16_t*>(tab.p[(r0 + j) * a.w + slot])[k];
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+            if (r0 + j < n) s = r0 + j == 0 ? ss::bf16_to_f32(h[j]) : __fadd_rn(s, ss::bf16_to_f32(h[j]));
+    }
+    const float g = __fdiv_rn(s, (float)n);
+    if (a.gout) a.gout[x] = g;
+    adamw_elem(g, th, m, v, a.c);
+    a.master[x] = th;
+    a.exp_avg[x] = m;
+    a.exp_avg_sq[x] = v;
+    const uint16_t p = ss::f32_to_bf16(th);
+    a.shards[x] = p;
+    const int goff = n * a.w;
     for (int j = 0; j < a.n_out; ++j) static_cast<uint16_t*>(tab.p[goff + j * a.w + slot])[k] = p;
 }
 
@@ -791,13 +825,30 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
                 add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
         } else if (has) {  // the vector meets a segment end: element by element
-            for (int i = 0; i < 8; ++i) {
-                const int64_t x = f + i;
+            if constexpr (NR > 0) {
+                // the entry of element f + i: the last one starting at or before it
                 int c;
-                const ss::PmEntry ex = lookup(mp, x, c);
-                if (x >= ex.packed_off && x < ex.packed_off + ex.len)
-                    step_scalar<true>(a, tab, ex.param - a.param_base, x,
-                                      ex.param_off + (x - ex.packed_off));
+                ss::PmEntry e = lookup(mp, f, c);
+                const float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+                const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int64_t x = f + i;
+                    while (c + 1 < a.M && mp.pm[c + 1].packed_off <= x) e = mp.pm[++c];
+                    if (x >= e.packed_off && x < e.packed_off + e.len)
+                        step_elem<NR>(a, tab, e.param - a.param_base, x,
+                                      e.param_off + (x - e.packed_off), th[i], mm[i], vv[i]);
+                }
+            } else {  // N > 8: one element at a time, with fewer registers
+                for (int i = 0; i < 8; ++i) {
+                    const int64_t x = f + i;
+                    int c;
+                    const ss::PmEntry ex = lookup(mp, x, c);
+                    if (x >= ex.packed_off && x < ex.packed_off + ex.len)
+                        step_scalar<true>(a, tab, ex.param - a.param_base, x,
+                                          ex.param_off + (x - ex.packed_off));
+                }
             }
         }
         const int nkey = __shfl_down_sync(kAll, key, 1);
@@ -954,6 +1005,7 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     a.gout = s->reduced_grad_out;
     a.N = N;
     a.n_out = s->n_out;
+    a.M = (int)plan->pm.size();
     a.c = make_coef(hp);
     const int per_param = (unpacked ? N : 0) + s->n_out;
     if (per_param > kTab) return SS_EINVAL;
