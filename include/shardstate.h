@@ -348,14 +348,10 @@ typedef struct {
 
 /* Per launch the pointer table holds (N if rank_param_grads else 0) + n_out
  * entries per parameter within 2048 slots; more parameters are split into
- * launches over consecutive parameters.  With rank_param_grads, N > 8 and a
- * misaligned plan or pointer, the step runs in two passes per chunk of at most
- * 8M vectors. The first pass writes the fp32 sum of ranks 0..7, and the
- * second adds the rest. The sums sit in a scratch of up to 256 MiB, taken with
- * cudaMallocAsync on `stream` and released with cudaFreeAsync before the call
- * returns; its failure returns SS_ECUDA. Every other form allocates nothing.  Errors: SS_EINVAL (including both or
- * neither gradient source, fp32 plans, (N + n_out) > 2048), SS_EALIGN,
- * SS_ENODEVICE, SS_ECUDA. */
+ * launches over consecutive parameters.  Every form runs in one pass and
+ * allocates nothing.  Errors: SS_EINVAL (including both or neither gradient
+ * source, fp32 plans, (N + n_out) > 2048), SS_EALIGN, SS_ENODEVICE,
+ * SS_ECUDA. */
 int fsdp_sharded_step(const ss_plan* plan, const ss_step* step, int group, ss_stream_t stream);
 
 /*

@@ -11,7 +11,8 @@
 // fused_step_flat_kernel and, for the copy-in, its rounds form
 // fused_step_flat_rounds_kernel when the runs are all whole 16-byte vectors;
 // fused_step_flat_any_kernel (packed gradients) and
-// fused_step_flat_copyin_kernel (per-parameter gradients) at any alignment.
+// fused_step_copyin_staged_kernel (per-parameter gradients, staged through
+// shared memory) at any alignment.
 // Per-parameter pointers ride in the kernel parameters; when a call's
 // parameters need more than one table, each window of parameters runs over
 // the packed ranges its segments form.  That lets one pass
