@@ -782,6 +782,30 @@ def _time_stream(fn, K: int, warmup: int = 3):
     return sum(ms) / len(ms), min(ms)
 
 
+def _time_back_to_back(fn, steps: int = 2000, reps: int = 5, warmup: int = 50):
+    """Per-call time (ms) of fn() issued `steps` times back to back between two
+    CUDA events on the current stream, as the median and min over `reps`
+    batches: the rate a loop of launch-bound steps runs at (host issue and GPU
+    work overlap; an event per call would add its own host time to every
+    call)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    per = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per.append(a.elapsed_time(b) / steps)
+    _LAST_TIMES[:] = per
+    return statistics.median(per), min(per)
+
+
 def _time_cpu(fn, seconds: float):
     t0 = time.perf_counter()
     reps = 0
@@ -1025,23 +1049,27 @@ def _rows_block4096(ss, peak, K):
 
 def _rows_small(ss, peak, want, awkward_scale=1.0):
     # -- config 1: tiny MLP, launch-bound -------------------------------------
+    # Each row is the per-step time of 2000 steps issued back to back between
+    # two CUDA events (median of 5 such batches): the rate a training loop of
+    # tiny steps runs at.
     if "tiny" in want:
         ps1 = W.tiny_mlp()
         st1 = Step(ss, ps1, 1)
+        P1, T1 = st1.info["unpadded_numel"], st1.info["total_numel"]
+        one_pass_bytes = (2 * 2 + 26) * T1 + 2 * P1
+        timing = "2000 steps back to back between two CUDA events, median of 5 batches"
 
         def step1():
             st1.rs_adamw()
             st1.all_gather()
-        ms, mn = _time_stream(step1, 200, warmup=20)
-        by = step_bytes(2, st1.info["total_numel"], st1.info["unpadded_numel"], 1)
-        _row("step on the tiny MLP (16,640 params, N=2): latency, two calls",
-             st1.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
-             extra={"us_per_step": ms * 1e3})
-        ms, mn = _time_stream(lambda: st1.fused_step(), 200, warmup=20)
+        ms, mn = _time_back_to_back(step1)
+        by = step_bytes(2, T1, P1, 1)
+        _row("step on the tiny MLP (16,640 params, N=2): latency, two calls", P1, "params/s", ms,
+             mn, by["step"], peak, extra={"us_per_step": ms * 1e3, "timing": timing})
+        ms, mn = _time_back_to_back(lambda: st1.fused_step())
         _row("step on the tiny MLP (16,640 params, N=2): latency, one fsdp_sharded_step call",
-             st1.info["unpadded_numel"], "params/s", ms, mn,
-             (2 * 2 + 26) * st1.info["total_numel"] + 2 * st1.info["unpadded_numel"], peak,
-             extra={"us_per_step": ms * 1e3})
+             P1, "params/s", ms, mn, one_pass_bytes, peak,
+             extra={"us_per_step": ms * 1e3, "timing": timing})
         # the same call with its arguments marshalled once (ss.ShardedStep)
         call = ss.ShardedStep(st1.plan, st1.master, st1.m, st1.v, st1.shards, st1.next_hp(),
                               rank_grads=st1._grads_arr, params_out=st1._outs_arr, n_out=1,
@@ -1051,41 +1079,35 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
         def prepared():
             step_no[0] += 1
             call(step_no[0])
-        ms, mn = _time_stream(prepared, 200, warmup=20)
+        ms, mn = _time_back_to_back(prepared)
         _row("step on the tiny MLP (16,640 params, N=2): latency, one prepared fsdp_sharded_step "
-             "call (ss.ShardedStep)", st1.info["unpadded_numel"], "params/s", ms, mn,
-             (2 * 2 + 26) * st1.info["total_numel"] + 2 * st1.info["unpadded_numel"], peak,
-             extra={"us_per_step": ms * 1e3})
+             "call (ss.ShardedStep)", P1, "params/s", ms, mn, one_pass_bytes, peak,
+             extra={"us_per_step": ms * 1e3, "timing": timing})
         del call
-        # the same two C-ABI calls captured once in a CUDA graph and replayed:
-        # the launch-bound step without host-side call overhead (the AdamW step
-        # count is frozen in the captured arguments, which does not change the
-        # work done)
-        g = torch.cuda.CUDAGraph()
+        # the same C-ABI calls captured once in a CUDA graph and replayed (the
+        # AdamW step count is frozen in the captured arguments, which does not
+        # change the work done): two calls, then the one-pass kernel
         s_ = torch.cuda.Stream()
         s_.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s_):
-            step1()
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g, stream=s_):
-                step1()
+        graphs = []
+        for fn in (step1, lambda: st1.fused_step()):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s_):
+                fn()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=s_):
+                    fn()
+            graphs.append(g)
         torch.cuda.current_stream().wait_stream(s_)
-        ms, mn = _time_stream(lambda: g.replay(), 500, warmup=20)
-        _row("step on the tiny MLP (16,640 params, N=2): replayed from a CUDA graph",
-             st1.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
-             extra={"us_per_step": ms * 1e3})
-        # one kernel: fsdp_sharded_step with the all-gather written in the same pass
-        g1 = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(s_):
-            st1.fused_step()
-            torch.cuda.synchronize()
-            with torch.cuda.graph(g1, stream=s_):
-                st1.fused_step()
-        torch.cuda.current_stream().wait_stream(s_)
-        ms, mn = _time_stream(lambda: g1.replay(), 500, warmup=20)
+        ms, mn = _time_back_to_back(lambda: graphs[0].replay())
+        _row("step on the tiny MLP (16,640 params, N=2): two calls replayed from a CUDA graph",
+             P1, "params/s", ms, mn, by["step"], peak,
+             extra={"us_per_step": ms * 1e3, "timing": timing})
+        ms, mn = _time_back_to_back(lambda: graphs[1].replay())
         _row("step on the tiny MLP (16,640 params, N=2): one-pass kernel replayed from a graph",
-             st1.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
-             extra={"us_per_step": ms * 1e3})
+             P1, "params/s", ms, mn, one_pass_bytes, peak,
+             extra={"us_per_step": ms * 1e3, "timing": timing})
+        del graphs
 
     # -- config 3: awkward sizes, N=7 ------------------------------------------
     for kind in ((W.FLAT_ORIG_FALSE, W.FLAT_ORIG_TRUE) if "awkward" in want else ()):

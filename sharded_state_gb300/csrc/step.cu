@@ -54,9 +54,18 @@ constexpr int kFlatRounds = 4;    // most rounds per warp of the aligned flat co
 struct RankPtrs {
     const void* p[SS_MAX_WORLD];
 };
-struct PtrTab {
-    void* p[kTab];
+template <int S>
+struct PtrTabT {
+    void* p[S];
 };
+using PtrTab = PtrTabT<kTab>;
+// The table of small launches (see fsdp_sharded_step): 2 KiB of kernel
+// parameters instead of 16 KiB, which a launch pays for on the host.
+constexpr int kTabSmall = 256;
+using PtrTabSmall = PtrTabT<kTabSmall>;
+// Launches of at most this many vectors with a table that fits kTabSmall slots
+// take the small form of the flat kernel.
+constexpr int64_t kSmallVecs = (int64_t)2 * 3 * 152 * 256;
 struct AdamCoef {
     float decay, b1, omb1, b2, omb2, step_size, inv_sqrt_bc2, eps;
 };
@@ -90,8 +99,8 @@ struct StepArgs {
 
 // Table layout: UNPACKED gradients tab[r*w + slot] for r < N, then outputs
 // tab[goff + j*w + slot] with goff = (UNPACKED ? N*w : 0).
-template <bool UNPACKED>
-__device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const PtrTab& tab, int r,
+template <bool UNPACKED, class Tab>
+__device__ __forceinline__ const uint16_t* grad_ptr(const StepArgs& a, const Tab& tab, int r,
                                                     int slot, int64_t f, int64_t k) {
     if (UNPACKED) return static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k;
     return static_cast<const uint16_t*>(a.packed_grads.p[r]) + f;
@@ -133,8 +142,8 @@ __device__ __forceinline__ void add_rank(float (&s)[8], uint4 x) {
 // Ranks 8 .. n-1 (N > 8) added to s in rank order, 8 loads in flight at a
 // time in w (free once the first 8 ranks are summed).  ANY: the
 // per-parameter gradients may sit at any 2-byte offset.
-template <bool UNPACKED, bool ANY = false>
-__device__ __forceinline__ void add_ranks_beyond_8(const StepArgs& a, const PtrTab& tab, int slot,
+template <bool UNPACKED, bool ANY = false, class Tab>
+__device__ __forceinline__ void add_ranks_beyond_8(const StepArgs& a, const Tab& tab, int slot,
                                                    int64_t f, int64_t k, int n,
                                                    uint4 (&w)[kMaxVec], float (&s)[8]) {
     for (int r0 = kMaxVec; r0 < n; r0 += kMaxVec) {
@@ -312,16 +321,35 @@ __device__ __forceinline__ ss::PmEntry lookup(const SegMap& mp, int64_t f, int& 
 // inside the block; only then a binary search over the few segments that
 // start in the block follows.  A pad vector is read (state, packed
 // gradients) but nothing is stored.
-template <int NR, bool UNPACKED>
+// SMALL (launches of a few waves, whose time is mostly launch and latency):
+// a 256-slot pointer table, and the kernel is launched with programmatic
+// stream serialisation.  It lets the next launch on the stream start at once
+// and looks its segment up -- the plan's map, which no kernel writes --
+// before it waits (griddepcontrol.wait) for the grid before it on the stream
+// to complete; only then does it touch state, gradients or outputs.  So
+// back-to-back steps overlap one's launch and lookup with the previous one's
+// end.  Without a programmatic predecessor the wait returns at once.
+template <int NR, bool UNPACKED, bool SMALL = false>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
-                       int64_t vbeg, int64_t nvec, StepArgs a, PtrTab tab) {
+                       int64_t vbeg, int64_t nvec, StepArgs a,
+                       PtrTabT<SMALL ? kTabSmall : kTab> tab) {
+    if (SMALL) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    if (q >= nvec) return;
+    if (q >= nvec) {
+        if (SMALL) asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
     const int64_t f = vbeg + 8 * q;
     const int64_t B = f / ss::kMapBlock;
     int m = __ldg(pm_block + B);
     const int n = NR > 0 ? NR : a.N;
+    ss::PmEntry e;
+    if (SMALL) {  // the segment first, then the wait for the previous grid
+        e = pm[m];
+        locate(SegMap{pm, pm_block, 0}, B, f, m, e);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     uint4 w[kMaxVec];
     if (!UNPACKED) {
 #pragma unroll
@@ -331,17 +359,19 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
     const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
     const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
-    ss::PmEntry e = pm[m];
-    if (f < e.packed_off || f >= e.packed_off + e.len) {  // a segment starts inside the block
-        int hi = __ldg(pm_block + B + 1);
-        while (m < hi) {
-            const int mid = (m + hi + 1) >> 1;
-            if (pm[mid].packed_off <= f)
-                m = mid;
-            else
-                hi = mid - 1;
-        }
+    if (!SMALL) {
         e = pm[m];
+        if (f < e.packed_off || f >= e.packed_off + e.len) {  // a segment starts inside the block
+            int hi = __ldg(pm_block + B + 1);
+            while (m < hi) {
+                const int mid = (m + hi + 1) >> 1;
+                if (pm[mid].packed_off <= f)
+                    m = mid;
+                else
+                    hi = mid - 1;
+            }
+            e = pm[m];
+        }
     }
     const int64_t rel = f - e.packed_off;
     if (rel < 0 || rel >= e.len) return;  // a pad vector
@@ -439,18 +469,20 @@ FlatRoundsKern pick_flat_rounds(int N) {
 }
 
 using FlatKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, StepArgs, PtrTab);
+using FlatKernSmall = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, StepArgs,
+                               PtrTabSmall);
 
-template <bool U>
-FlatKern pick_flat(int N) {
+template <bool U, bool SMALL = false>
+auto pick_flat(int N) {
     switch (N) {
-        case 2: return fused_step_flat_kernel<2, U>;
-        case 3: return fused_step_flat_kernel<3, U>;
-        case 4: return fused_step_flat_kernel<4, U>;
-        case 5: return fused_step_flat_kernel<5, U>;
-        case 6: return fused_step_flat_kernel<6, U>;
-        case 7: return fused_step_flat_kernel<7, U>;
-        case 8: return fused_step_flat_kernel<8, U>;
-        default: return fused_step_flat_kernel<0, U>;
+        case 2: return fused_step_flat_kernel<2, U, SMALL>;
+        case 3: return fused_step_flat_kernel<3, U, SMALL>;
+        case 4: return fused_step_flat_kernel<4, U, SMALL>;
+        case 5: return fused_step_flat_kernel<5, U, SMALL>;
+        case 6: return fused_step_flat_kernel<6, U, SMALL>;
+        case 7: return fused_step_flat_kernel<7, U, SMALL>;
+        case 8: return fused_step_flat_kernel<8, U, SMALL>;
+        default: return fused_step_flat_kernel<0, U, SMALL>;
     }
 }
 
@@ -1017,7 +1049,8 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         a.param_base = wa;
         a.w = wb - wa;
         a.congruent = 1;
-        std::memset(&tab, 0, sizeof tab);
+        // only the slots the kernels read: per_param per parameter of the window
+        std::memset(&tab, 0, sizeof(void*) * (size_t)std::min(kTab, per_param * (wb - wa)));
         for (int i = wa; i < wb; ++i) {
             for (int r = 1; unpacked && r < N; ++r)
                 if (plan->numel[i] > 0 &&
@@ -1038,6 +1071,27 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         if (!gen && rlo % 8 == 0 && rhi % 8 == 0) {
             // everything aligned: one thread per packed vector
             const int64_t nvec = (rhi - rlo) / 8;
+            if (nvec <= kSmallVecs && per_param * a.w <= kTabSmall) {
+                // a launch of a few waves: the small table, and programmatic
+                // stream serialisation so that it may start while the grid
+                // before it on the stream finishes
+                PtrTabSmall ts;
+                std::memcpy(ts.p, tab.p, sizeof ts.p);
+                const auto fs = unpacked ? pick_flat<true, true>(N) : pick_flat<false, true>(N);
+                cudaLaunchConfig_t cfg;
+                std::memset(&cfg, 0, sizeof cfg);
+                cfg.gridDim = dim3((unsigned)((nvec + kThreads - 1) / kThreads));
+                cfg.blockDim = dim3(kThreads);
+                cfg.stream = st;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                const cudaError_t le = cudaLaunchKernelEx(&cfg, fs, (const ss::PmEntry*)plan->d_pm,
+                                                          (const int*)plan->d_pm_block, rlo, nvec, a, ts);
+                return le == cudaSuccess ? ss::check_launch() : ss::cuda_fail(le);
+            }
             FlatRoundsKern fr = unpacked && kFlatRounds > 0 ? pick_flat_rounds(N) : nullptr;
             if (fr) {
                 // rounds of 32 vectors per warp, as many as keep kCopyinWaves
