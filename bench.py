@@ -818,11 +818,15 @@ def _time_cpu(fn, seconds: float):
 
 
 def _row(name, unit_count, unit, ms, ms_min, nbytes, peak, cpu=None, extra=None):
-    gbs = nbytes / (ms / 1e3) / 1e9
-    d = {"row": name, "value": unit_count / (ms / 1e3), "unit": unit, "ms": ms, "ms_min": ms_min,
-         "ms_median": statistics.median(_LAST_TIMES) if _LAST_TIMES else None,
+    """One row: value and roofline from the median of the timed calls (a host
+    stall between two launches lands in one call's events and would move the
+    mean); the mean (`ms`) and the minimum beside it."""
+    med = statistics.median(_LAST_TIMES) if _LAST_TIMES else ms
+    gbs = nbytes / (med / 1e3) / 1e9
+    d = {"row": name, "value": unit_count / (med / 1e3), "unit": unit, "ms": ms, "ms_min": ms_min,
+         "ms_median": med,
          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                      "frac": gbs / peak, "algorithmic_bytes": nbytes}}
+                      "frac": gbs / peak, "algorithmic_bytes": nbytes, "from": "median"}}
     if cpu is not None:
         d["cpu_baseline"] = cpu
     if extra:

@@ -43,6 +43,17 @@ struct PtrTab {
     void* p[CAP];
 };
 
+// Pad tiles a pack launch zeroes besides its data tiles: CTAs ndata .. ndata
+// + n - 1 of the grid take pad tiles lo .. lo + n - 1 (none when n == 0), so
+// a pack is one launch.
+struct PadTiles {
+    const ss::Tile* tiles;
+    const ss::Seg* segs;
+    int64_t lo;
+    int64_t n;
+    int64_t ndata;
+};
+
 // Aligned 16-byte vectors q in [0, nvec) of dv <- the 16 source bytes at
 // sv + 16q, where sv sits sh = sv mod 16 bytes past a boundary (sh != 0).
 // Vector q is rebuilt from the aligned source blocks q and q + 1, block b
@@ -216,11 +227,26 @@ __device__ __forceinline__ void cta_zero(unsigned char* dst, int64_t nelem) {
 // DIR 0: all-gather + unpack (packed -> params); DIR 1: pack (params -> packed).
 // DIR 2: all-gather + unpack with n_out > 1 replicas; DIR 3: the same for a
 // plan and replicas all 16-byte aligned (no realigning code).
+// One pad tile of a pack launch (CTA-cooperative).
+template <int E>
+__device__ __forceinline__ void zero_pad_tile(const PadTiles& pz, int64_t j, unsigned char* packed) {
+    constexpr int64_t T = ss::kTileBytes / E;
+    const ss::Tile tl = pz.tiles[pz.lo + j];
+    const ss::Seg sg = pz.segs[tl.seg];
+    const int64_t off = (int64_t)tl.idx * T;
+    const int64_t len = sg.len - off < T ? sg.len - off : T;
+    cta_zero<E>(packed + (sg.packed_off + off) * E, len);
+}
+
 template <int E, int CAP, int DIR>
 __global__ void __launch_bounds__(kThreads, DIR >= 2 ? 2 : 5)
 tile_copy_kernel(const ss::PmEntry* __restrict__ ext, int64_t t_lo, unsigned char* packed,
-                 PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out) {
+                 PtrTab<CAP> tab, int param_base, int ptr_stride, int n_out, PadTiles pz) {
     constexpr int64_t T = ss::kTileBytes / E;
+    if (DIR == 1 && (int64_t)blockIdx.x >= pz.ndata) {
+        zero_pad_tile<E>(pz, (int64_t)blockIdx.x - pz.ndata, packed);
+        return;
+    }
     const ss::PmEntry sg = ext[t_lo + blockIdx.x];  // the tile's segment, tile index in reserved
     const int slot = sg.param - param_base;
     // The segment's tile starts are moved back by u elements, u = how far the
@@ -283,9 +309,13 @@ tile_copy_kernel(const ss::PmEntry* __restrict__ ext, int64_t t_lo, unsigned cha
 template <int E, int CAP, int DIR>
 __global__ void __launch_bounds__(kThreads, 8)
 tile_copy_fast_kernel(const ss::PmEntry* __restrict__ ext, int64_t t_lo, unsigned char* packed,
-                      PtrTab<CAP> tab, int param_base) {
+                      PtrTab<CAP> tab, int param_base, PadTiles pz) {
     constexpr int64_t T = ss::kTileBytes / E;
     constexpr int kV = ss::kTileBytes / 16 / kThreads;  // vectors per thread
+    if (DIR == 1 && (int64_t)blockIdx.x >= pz.ndata) {
+        zero_pad_tile<E>(pz, (int64_t)blockIdx.x - pz.ndata, packed);
+        return;
+    }
     const ss::PmEntry sg = ext[t_lo + blockIdx.x];  // the tile's segment, tile index in reserved
     const int64_t off = (int64_t)sg.reserved * T;
     const int nv = (int)((sg.len - off < T ? sg.len - off : T) * E / 16);
@@ -319,10 +349,12 @@ zero_tile_kernel(const ss::Tile* __restrict__ tiles, int64_t t_lo, const ss::Seg
     cta_zero<E>(packed + (sg.packed_off + off) * E, len);
 }
 
+// Most CTAs per launch of the tile kernels.
+constexpr int64_t kMaxGrid = (int64_t)1 << 30;
+
 // Launch one CTA per tile of [t_lo, t_hi), in chunks that respect the grid limit.
 template <typename Launch>
 int for_tile_chunks(int64_t t_lo, int64_t t_hi, Launch launch) {
-    constexpr int64_t kMaxGrid = (int64_t)1 << 30;
     for (int64_t t = t_lo; t < t_hi; t += kMaxGrid) {
         const int64_t n = t_hi - t < kMaxGrid ? t_hi - t : kMaxGrid;
         launch(t, (unsigned)n);
@@ -337,12 +369,19 @@ int for_tile_chunks(int64_t t_lo, int64_t t_hi, Launch launch) {
 // 0.823 ms for the 1.2B all-gather).
 template <int CAP>
 int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed,
-                  void* const* ptrs, int n_out, cudaStream_t st) {
+                  void* const* ptrs, int n_out, cudaStream_t st, PadTiles* pads) {
     const int s_lo = p->param_seg[a], s_hi = p->param_seg[b];
-    if (s_hi <= s_lo) return SS_OK;
     const ss::PmEntry* tiles = p->d_data_tiles_ext;
     const int64_t t_lo = p->data_seg_tile[s_lo];
-    const int64_t t_hi = p->data_seg_tile[s_hi];
+    const int64_t t_hi = s_hi > s_lo ? p->data_seg_tile[s_hi] : t_lo;
+    // pad tiles ride with this launch when it is one grid (dir 1 only)
+    PadTiles pz{nullptr, nullptr, 0, 0, (int64_t)1 << 62};
+    if (pads && pads->n > 0 && (t_hi - t_lo) + pads->n <= kMaxGrid) {
+        pz = *pads;
+        pz.ndata = t_hi - t_lo;
+        pads->n = 0;  // taken
+    }
+    if (t_hi <= t_lo && pz.n == 0) return SS_OK;
     PtrTab<CAP> tab;
     std::memset(&tab, 0, sizeof tab);
     const int w = b - a;
@@ -353,56 +392,64 @@ int launch_window(const ss_plan* p, int dir, int a, int b, unsigned char* packed
             ptrs_aligned &= p->numel[i] == 0 || ss::aligned(tab.p[j * w + (i - a)], 16);
         }
     const bool all_aligned = p->vec_aligned && ptrs_aligned;
-    if (all_aligned && n_out == 1) {
-        return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
+    const PadTiles none{nullptr, nullptr, 0, 0, (int64_t)1 << 62};
+    // a grid of data tiles [t, t + grid) (pad tiles after them when pz.n > 0)
+    auto launch = [&](int64_t t, unsigned grid, const PadTiles& z) {
+        if (all_aligned && n_out == 1) {
             if (p->eb == 2) {
                 if (dir == 0)
-                    tile_copy_fast_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
+                    tile_copy_fast_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, z);
                 else
-                    tile_copy_fast_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
+                    tile_copy_fast_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, z);
             } else {
                 if (dir == 0)
-                    tile_copy_fast_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
+                    tile_copy_fast_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, z);
                 else
-                    tile_copy_fast_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a);
+                    tile_copy_fast_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, z);
             }
-        });
-    }
-    return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
+            return;
+        }
         if (p->eb == 2) {
             if (dir == 0 && n_out > 1 && all_aligned)
-                tile_copy_kernel<2, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
+                tile_copy_kernel<2, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out, z);
             else if (dir == 0 && n_out > 1)
-                tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
+                tile_copy_kernel<2, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out, z);
             else if (dir == 0)
-                tile_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
+                tile_copy_kernel<2, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1, z);
             else
-                tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
+                tile_copy_kernel<2, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1, z);
         } else {
             if (dir == 0 && n_out > 1 && all_aligned)
-                tile_copy_kernel<4, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
+                tile_copy_kernel<4, CAP, 3><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out, z);
             else if (dir == 0 && n_out > 1)
-                tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out);
+                tile_copy_kernel<4, CAP, 2><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, n_out, z);
             else if (dir == 0)
-                tile_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
+                tile_copy_kernel<4, CAP, 0><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1, z);
             else
-                tile_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1);
+                tile_copy_kernel<4, CAP, 1><<<grid, kThreads, 0, st>>>(tiles, t, packed, tab, a, w, 1, z);
         }
-    });
+    };
+    if (pz.n > 0) {  // one grid: the data tiles, then the pad tiles
+        launch(t_lo, (unsigned)(pz.ndata + pz.n), pz);
+        return ss::check_launch();
+    }
+    return for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) { launch(t, grid, none); });
 }
 
 // Run the segment copy for params [pa, pb), windowing the pointer table.
+// pads (pack only, nullable): pad tiles to zero in the same launch as the
+// last window's data tiles when they fit one grid; left with n > 0 otherwise.
 int run_segments(const ss_plan* p, int dir, int pa, int pb, unsigned char* packed,
-                 void* const* ptrs, int n_out, cudaStream_t st) {
+                 void* const* ptrs, int n_out, cudaStream_t st, PadTiles* pads) {
     const int n_ptr = (pb - pa) * n_out;
     if (n_ptr <= kTabSmall)
-        return launch_window<kTabSmall>(p, dir, pa, pb, packed, ptrs, n_out, st);
+        return launch_window<kTabSmall>(p, dir, pa, pb, packed, ptrs, n_out, st, pads);
     if (n_ptr <= kTabBig)
-        return launch_window<kTabBig>(p, dir, pa, pb, packed, ptrs, n_out, st);
+        return launch_window<kTabBig>(p, dir, pa, pb, packed, ptrs, n_out, st, pads);
     const int w = kTabBig / n_out;
     for (int a = pa; a < pb; a += w) {
         int b = a + w < pb ? a + w : pb;
-        int rc = launch_window<kTabBig>(p, dir, a, b, packed, ptrs, n_out, st);
+        int rc = launch_window<kTabBig>(p, dir, a, b, packed, ptrs, n_out, st, b == pb ? pads : nullptr);
         if (rc) return rc;
     }
     return SS_OK;
@@ -446,14 +493,19 @@ int fsdp_pack(const ss_plan* plan, const void* const* params, void* packed, int 
     int rc = check_param_ptrs(plan, pa, pb, const_cast<void* const*>(params), 1);
     if (rc) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    rc = run_segments(plan, 1, pa, pb, static_cast<unsigned char*>(packed),
-                      const_cast<void* const*>(params), 1, st);
-    if (rc) return rc;
-    // pads of the selected groups
+    // pads of the selected groups: zeroed by the data launch's extra CTAs
     const int ga = group < 0 ? 0 : group, gb = group < 0 ? plan->G : group + 1;
     const int z_lo = plan->group_zero[ga], z_hi = plan->group_zero[gb];
+    PadTiles pads{plan->d_zero_tiles, plan->d_zero, 0, 0, 0};
     if (z_hi > z_lo) {
-        const int64_t t_lo = plan->zero_seg_tile[z_lo], t_hi = plan->zero_seg_tile[z_hi];
+        pads.lo = plan->zero_seg_tile[z_lo];
+        pads.n = plan->zero_seg_tile[z_hi] - pads.lo;
+    }
+    rc = run_segments(plan, 1, pa, pb, static_cast<unsigned char*>(packed),
+                      const_cast<void* const*>(params), 1, st, &pads);
+    if (rc) return rc;
+    if (pads.n > 0) {  // too many tiles for one grid: the pads in launches of their own
+        const int64_t t_lo = pads.lo, t_hi = pads.lo + pads.n;
         unsigned char* pk = static_cast<unsigned char*>(packed);
         rc = for_tile_chunks(t_lo, t_hi, [&](int64_t t, unsigned grid) {
             if (plan->eb == 2)
@@ -479,7 +531,7 @@ int fsdp_all_gather_unpack(const ss_plan* plan, const void* param_shards, void* 
     int rc = check_param_ptrs(plan, pa, pb, params_out, n_out);
     if (rc) return rc;
     return run_segments(plan, 0, pa, pb, static_cast<unsigned char*>(const_cast<void*>(param_shards)),
-                        params_out, n_out, reinterpret_cast<cudaStream_t>(stream));
+                        params_out, n_out, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 }  // extern "C"
