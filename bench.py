@@ -664,7 +664,8 @@ def _oracle_step(ps: W.ParamSet, cfg: dict, t: int, groups=None) -> int:
 
 def _oracle_sample_text(ps: W.ParamSet, cfg: dict) -> str:
     if cfg["whole"]:
-        return (f"the whole workload per step: all {len(cfg['groups'])} groups, "
+        ng = len(cfg["groups"])
+        return (f"the whole workload per step: {'all %d groups' % ng if ng > 1 else 'its one group'}, "
                 f"{cfg['params']:,} params, each group with its own optimizer state; "
                 f"inputs drawn on the host once per group shape")
     return (f"group 0 only ({cfg['params']:,} params) per step: the whole workload's state "
@@ -817,6 +818,25 @@ def _time_cpu(fn, seconds: float):
     return (time.perf_counter() - t0) / reps, reps
 
 
+def _oracle_pair(fn, seconds: float, units: int, unit: str, sample: str) -> dict:
+    """A row's oracle baseline: fn (the oracle on `units` units of the row's
+    work) timed on all the host's threads, then on one thread for half as
+    long; the all-thread figure is the row's cpu_baseline value."""
+    import oracle
+    cores = _host_cores()
+    used = cores if oracle.has_openmp() else 1
+    oracle.set_threads(cores)
+    t_all, reps = _time_cpu(fn, seconds)
+    oracle.set_threads(1)
+    try:
+        t_one, reps1 = _time_cpu(fn, seconds / 2)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": units / t_all, "unit": unit, "cores": used, "kind": "oracle",
+            "sample": f"{sample}, {reps} reps; one thread: {units / t_one:.4g} {unit}",
+            "single_thread": {"value": units / t_one, "unit": unit, "cores": 1, "reps": reps1}}
+
+
 def _row(name, unit_count, unit, ms, ms_min, nbytes, peak, cpu=None, extra=None):
     """One row: value and roofline from the median of the timed calls (a host
     stall between two launches lands in one call's events and would move the
@@ -851,9 +871,9 @@ def run_rows(args):
     if "llama" in want:
         _rows_llama(args, ss, oracle, peak, used, K, bits)
     if "block4096" in want:
-        _rows_block4096(ss, peak, K)
+        _rows_block4096(ss, peak, K, args.cpu_seconds)
     if want & {"tiny", "awkward", "awkward_large"}:
-        _rows_small(ss, peak, want, args.awkward_scale)
+        _rows_small(ss, peak, want, args.awkward_scale, args.cpu_seconds)
     if "awkward_n16" in want:
         _rows_awkward_wide(ss, peak, args.awkward_scale)
     if "ddp" in want:
@@ -892,31 +912,29 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     # oracle: pack of block group 0 of one rank
     g0 = ps.groups[0]
     sample = [bits(t) for t in grad_params[:g0]]
-    t_cpu, reps = _time_cpu(lambda: oracle.pack(ps.layout, N, 2, d0[:g0], inner[:g0], sample),
-                            args.cpu_seconds / 4)
     p0 = sum(ps.numels()[:g0])
+    cpu = _oracle_pair(lambda: oracle.pack(ps.layout, N, 2, d0[:g0], inner[:g0], sample),
+                       args.cpu_seconds / 4, p0, "params/s",
+                       f"block group 0 ({p0:,} params) of one rank, oracle packs")
     _row(f"a2 pack (one rank's gradients, {tag} model, N=8)", P, "params/s", ms, mn, 4 * P, peak,
-         {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
-          "sample": f"block group 0 ({p0:,} params), {reps} packs"})
+         cpu)
     del grad_params
 
     del packed
     rs_ms, rs_mn = _time_stream(lambda: st.rs_adamw(), K)
     smp = _oracle_group0_from_step(st)
-    t_cpu, reps = _time_cpu(lambda: _oracle_step(ps, smp, 10_000), args.cpu_seconds / 2)
+    cpu = _oracle_pair(lambda: _oracle_step(ps, smp, 10_000), args.cpu_seconds / 2, p0,
+                       "params/s", "block group 0, oracle RS+AdamW+AG steps")
     _row(f"a3 reduce-scatter + AdamW ({tag} model, N=8)", P, "params/s", rs_ms, rs_mn,
-         (2 * N + 26) * total, peak,
-         {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
-          "sample": f"block group 0, {reps} oracle RS+AdamW+AG steps"})
+         (2 * N + 26) * total, peak, cpu)
     ag_ms, ag_mn = _time_stream(lambda: st.all_gather(), K)
     g0p = ps.groups[0]
     shards0 = bits(st.shards[:N * ss.fsdp_plan_group(st.plan, 0)["shard_numel"]])
-    t_cpu, reps = _time_cpu(lambda: oracle.all_gather_unpack(ps.layout, N, 2, d0[:g0p],
-                                                             inner[:g0p], shards0),
-                            args.cpu_seconds / 4)
+    cpu = _oracle_pair(lambda: oracle.all_gather_unpack(ps.layout, N, 2, d0[:g0p], inner[:g0p],
+                                                        shards0),
+                       args.cpu_seconds / 4, p0, "params/s", "block group 0, oracle unpacks")
     _row(f"a4 all-gather + unpack, n_out=1 ({tag} model, N=8)", P, "params/s", ag_ms, ag_mn, 4 * P,
-         peak, {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
-                "sample": f"block group 0, {reps} oracle unpacks"})
+         peak, cpu)
     ms, mn = _time_stream(lambda: st.fused_step(), K)
     _row(f"one-pass step: packed grads -> RS+AdamW -> shards + unpacked params ({tag}, N=8)", P,
          "params/s", ms, mn, (2 * N + 28) * P, peak)
@@ -966,18 +984,19 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     ms, mn = _time_stream(accumulate_step, max(K // 4, 5))
     acc_bytes = (2 * N + 4) + 2 * (2 * N + 8) + (2 * N + 30)
 
+    g0 = smp["groups"][0]  # block group 0, copied from the device above
+
     def oracle_accumulate():
         acc = None
         for _ in range(kmic):
-            acc = oracle.accumulate(N, smp["shard_numel"], smp["grads"], acc)
+            acc = oracle.accumulate(N, g0["shard_numel"], g0["grads"], acc)
         g = oracle.accumulated_grad(acc, kmic)
-        oracle.adamw(g, smp["master"], smp["m"], smp["v"], lr=1e-3, beta1=0.9, beta2=0.999,
+        oracle.adamw(g, g0["master"], g0["m"], g0["v"], lr=1e-3, beta1=0.9, beta2=0.999,
                      eps=1e-8, weight_decay=0.01, step=20_000)
-    t_cpu, reps = _time_cpu(oracle_accumulate, args.cpu_seconds / 4)
+    cpu = _oracle_pair(oracle_accumulate, args.cpu_seconds / 4, p0, "params/s",
+                       f"block group 0, oracle optimizer steps of {kmic} micro-batches")
     _row(f"gradient accumulation: {kmic} micro-batches per optimizer step ({tag}, N=8)", P,
-         "params/s", ms, mn, acc_bytes * total, peak,
-         {"value": p0 / t_cpu, "unit": "params/s", "cores": used, "kind": "oracle",
-          "sample": f"block group 0, {reps} oracle optimizer steps of {kmic} micro-batches"},
+         "params/s", ms, mn, acc_bytes * total, peak, cpu,
          extra={"micro_batches": kmic, "ms_per_micro_batch": ms / kmic})
     del accum
     # F4: AdamW without fp32 master weights (bf16 shard updated in place)
@@ -1031,7 +1050,7 @@ def _rows_llama(args, ss, oracle, peak, used, K, bits):
     torch.cuda.empty_cache()
 
 
-def _rows_block4096(ss, peak, K):
+def _rows_block4096(ss, peak, K, cpu_seconds):
     # -- config 2: one 4096 block ---------------------------------------------
     ps2 = W.llama_block_4096()
     st2 = Step(ss, ps2, 1)
@@ -1045,13 +1064,17 @@ def _rows_block4096(ss, peak, K):
     _row("step on one Llama block, hidden 4096 (202M params, N=8): two calls", P2, "params/s", ms,
          mn, by["step"], peak)
     ms, mn = _time_stream(lambda: st2.fused_step(), K)
+    cfg2 = _oracle_config(ps2)
+    cpu = _oracle_pair(lambda: _oracle_step(ps2, cfg2, 10_000), cpu_seconds, cfg2["params"],
+                       "params/s", _oracle_sample_text(ps2, cfg2) + "; oracle RS+AdamW+AG steps")
+    del cfg2
     _row("step on one Llama block, hidden 4096 (202M params, N=8): one pass", P2, "params/s", ms,
-         mn, (2 * 8 + 26) * total2 + 2 * P2, peak)
+         mn, (2 * 8 + 26) * total2 + 2 * P2, peak, cpu)
     del st2
     torch.cuda.empty_cache()
 
 
-def _rows_small(ss, peak, want, awkward_scale=1.0):
+def _rows_small(ss, peak, want, awkward_scale=1.0, cpu_seconds=4.0):
     # -- config 1: tiny MLP, launch-bound -------------------------------------
     # Each row is the per-step time of 2000 steps issued back to back between
     # two CUDA events (median of 5 such batches): the rate a training loop of
@@ -1084,8 +1107,11 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
             step_no[0] += 1
             call(step_no[0])
         ms, mn = _time_back_to_back(prepared)
+        cfg1 = _oracle_config(ps1)
+        cpu = _oracle_pair(lambda: _oracle_step(ps1, cfg1, 10_000), cpu_seconds, cfg1["params"],
+                           "params/s", _oracle_sample_text(ps1, cfg1) + "; oracle RS+AdamW+AG steps")
         _row("step on the tiny MLP (16,640 params, N=2): latency, one prepared fsdp_sharded_step "
-             "call (ss.ShardedStep)", P1, "params/s", ms, mn, one_pass_bytes, peak,
+             "call (ss.ShardedStep)", P1, "params/s", ms, mn, one_pass_bytes, peak, cpu,
              extra={"us_per_step": ms * 1e3, "timing": timing})
         del call
         # the same C-ABI calls captured once in a CUDA graph and replayed (the
@@ -1123,8 +1149,11 @@ def _rows_small(ss, peak, want, awkward_scale=1.0):
             st3.all_gather()
         ms, mn = _time_stream(step3, 100, warmup=10)
         by = step_bytes(7, st3.info["total_numel"], st3.info["unpadded_numel"], 1)
+        cfg3 = _oracle_config(ps3)
+        cpu = _oracle_pair(lambda: _oracle_step(ps3, cfg3, 10_000), cpu_seconds, cfg3["params"],
+                           "params/s", _oracle_sample_text(ps3, cfg3) + "; oracle RS+AdamW+AG steps")
         _row(f"step on 200 awkward params ({W.LAYOUT_NAMES[kind]}, N=7)",
-             st3.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak,
+             st3.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak, cpu,
              extra={"us_per_step": ms * 1e3})
 
     # -- the same awkward shapes scaled up until they are bandwidth-bound:
@@ -1216,10 +1245,9 @@ def _rows_ddp(args, ss, oracle, peak, used, K, bits):
     outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for n in ds.numels]
     Pd = sum(ds.numels)
     small = [[bits(grads[r][t]) for t in range(40)] for r in range(ds.world_size)]
-    t_cpu, reps = _time_cpu(lambda: oracle.ddp_average(small), args.cpu_seconds / 4)
     psmall = sum(ds.numels[:40])
-    cpu = {"value": psmall / t_cpu, "unit": "elements/s", "cores": used, "kind": "oracle",
-           "sample": f"first 40 tensors ({psmall:,} elements, N=8), {reps} averages"}
+    cpu = _oracle_pair(lambda: oracle.ddp_average(small), args.cpu_seconds / 4, psmall,
+                       "elements/s", f"first 40 tensors ({psmall:,} elements, N=8), oracle averages")
     import ctypes
     T = len(ds.numels)
     flat_arr = ss.ptr_array([g for rank in grads for g in rank])
@@ -1241,6 +1269,22 @@ def _rows_ddp(args, ss, oracle, peak, used, K, bits):
              "elements/s", ms, mn, (2 * ds.world_size + 2) * Pd, peak, cpu,
              extra={"bucket_cap_bytes": cap, "buckets": nb})
         cpu = None
+    # the allocation-free entry point on the same list at the 25 MiB cap: its
+    # table goes to the library's fixed device array instead of a
+    # stream-ordered allocation
+    cap = 25 << 20
+
+    def ddp_noalloc():
+        st_ = ss.lib().ddp_bucket_pack_average_noalloc(ds.world_size, T, numels_arr, flat_arr, cap,
+                                                       outs_arr, ctypes.byref(nb_out), sp)
+        if st_ != 0:
+            raise RuntimeError(f"ddp_bucket_pack_average_noalloc: {ss.ss_strerror(st_)}")
+    for name, fn in (("ddp_bucket_pack_average", lambda: ddp_call(cap)),
+                     ("ddp_bucket_pack_average_noalloc", ddp_noalloc)):
+        ms, mn = _time_stream(fn, max(K // 10, 5))
+        _row(f"a5 DDP bucketed average through {name}, cap {cap} B ({len(ds.numels)} grads, N=8)",
+             Pd, "elements/s", ms, mn, (2 * ds.world_size + 2) * Pd, peak,
+             extra={"bucket_cap_bytes": cap, "entry_point": name})
 
 
 def main():
