@@ -681,6 +681,7 @@ def cpu_baseline(st: Step, ps: W.ParamSet, args) -> dict:
     oracle.set_threads(cores)
     used = cores if oracle.has_openmp() else 1
     cfg = _oracle_config(ps)
+    _oracle_step(ps, cfg, 999)  # untimed: touches the freshly allocated host memory once
     t0 = time.perf_counter()
     reps, params = 0, 0
     while True:
