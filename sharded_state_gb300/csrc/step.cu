@@ -41,6 +41,7 @@
 
 #include "device_utils.cuh"
 #include "internal.h"
+#include "segmap.cuh"
 
 namespace {
 
@@ -211,18 +212,6 @@ __device__ __forceinline__ uint4 adam_vec(const StepArgs& a, int64_t f, const fl
     return p;
 }
 
-// Store bytes [lo, hi) of the 16-byte value v to blk + lo (blk 16-byte
-// aligned, lo and hi even), two bytes at a time.
-__device__ __forceinline__ void st_bytes(unsigned char* blk, uint4 v, int lo, int hi) {
-#pragma unroll
-    for (int b = 0; b < 16; b += 2) {
-        if (b >= lo && b < hi) {
-            const uint32_t w = b < 4 ? v.x : b < 8 ? v.y : b < 12 ? v.z : v.w;
-            *reinterpret_cast<uint16_t*>(blk + b) = (uint16_t)(w >> ((b & 2) * 8));
-        }
-    }
-}
-
 template <bool UNPACKED>
 __device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab, int slot,
                                             int64_t f, int64_t k) {
@@ -275,41 +264,6 @@ __device__ __forceinline__ void step_elem(const StepArgs& a, const PtrTab& tab, 
     for (int j = 0; j < a.n_out; ++j) static_cast<uint16_t*>(tab.p[goff + j * a.w + slot])[k] = p;
 }
 
-// The plan's packed segment map on the device.
-struct SegMap {
-    const ss::PmEntry* __restrict__ pm;  // data segments by packed offset
-    const int* __restrict__ pm_block;    // per kMapBlock block: last entry at or before it
-    int M;                               // entries (where a kernel needs them)
-};
-
-// The map entry of packed element f in block B = f / kMapBlock, given the
-// block's first candidate m = pm_block[B] and e = pm[m]: unless e's segment
-// holds f, a binary search over the entries that start inside the block for
-// the last one that starts at or before f (m stays pm_block[B] when none
-// does: f lies before the first segment).  m and e are updated.
-__device__ __forceinline__ void locate(const SegMap& mp, int64_t B, int64_t f, int& m,
-                                       ss::PmEntry& e) {
-    if (f >= e.packed_off && f < e.packed_off + e.len) return;
-    int hi = __ldg(mp.pm_block + B + 1);
-    while (m < hi) {
-        const int mid = (m + hi + 1) >> 1;
-        if (mp.pm[mid].packed_off <= f)
-            m = mid;
-        else
-            hi = mid - 1;
-    }
-    e = mp.pm[m];
-}
-
-// The map entry of packed element f (its index in m).
-__device__ __forceinline__ ss::PmEntry lookup(const SegMap& mp, int64_t f, int& m) {
-    const int64_t B = f / ss::kMapBlock;
-    m = __ldg(mp.pm_block + B);
-    ss::PmEntry e = mp.pm[m];
-    locate(mp, B, f, m, e);
-    return e;
-}
-
 // Flat form of the one-pass step, for plans whose runs are all whole 16-byte
 // vectors with 16-byte aligned per-parameter pointers: thread q of the grid
 // takes packed elements f = vbeg + 8q .. f + 7, as the reduce-scatter kernel
@@ -347,7 +301,7 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     ss::PmEntry e;
     if (SMALL) {  // the segment first, then the wait for the previous grid
         e = pm[m];
-        locate(SegMap{pm, pm_block, 0}, B, f, m, e);
+        ss::locate(ss::SegMap{pm, pm_block, 0}, B, f, m, e);
         asm volatile("griddepcontrol.wait;" ::: "memory");
     }
     uint4 w[kMaxVec];
@@ -402,7 +356,7 @@ template <int NR>  // 2..8
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_rounds_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
                               int64_t vbeg, int64_t nvec, int iters, StepArgs a, PtrTab tab) {
-    const SegMap mp{pm, pm_block, 0};
+    const ss::SegMap mp{pm, pm_block, 0};
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     constexpr int n = NR;
@@ -416,7 +370,7 @@ fused_step_flat_rounds_kernel(const ss::PmEntry* __restrict__ pm, const int* __r
         const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
         if (hslot < 0 || f + 8 > hend) {  // leaves the last segment: look it up
             int m;
-            const ss::PmEntry e = lookup(mp, f, m);
+            const ss::PmEntry e = ss::lookup(mp, f, m);
             hslot = -1;
             if (f >= e.packed_off && f < e.packed_off + e.len) {
                 hend = e.packed_off + e.len;
@@ -496,22 +450,10 @@ auto pick_flat(int N) {
 __device__ __forceinline__ void store_outputs_lane(const StepArgs& a, const PtrTab& tab, int goff,
                                                    int slot, int64_t k, uint4 p, uint4 nx,
                                                    bool same_next, bool same_prev) {
-    for (int j = 0; j < a.n_out; ++j) {
-        unsigned char* ob =
-            reinterpret_cast<unsigned char*>(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k);
-        const int sh = (int)(reinterpret_cast<uintptr_t>(ob) & 15u);
-        if (sh == 0) {
-            ss::st_stream_u4(ob, p);
-            continue;
-        }
-        unsigned char* blk = ob - sh + 16;  // the aligned block after this vector's start
-        const uint4 v = ss::realign16(p, nx, 16 - sh);
-        if (same_next)
-            ss::st_stream_u4(blk, v);
-        else
-            st_bytes(blk, v, 0, sh);
-        if (!same_prev) st_bytes(blk - 16, ss::realign16(p, p, 16 - sh), sh, 16);
-    }
+    for (int j = 0; j < a.n_out; ++j)
+        ss::store_realigned(
+            reinterpret_cast<unsigned char*>(static_cast<uint16_t*>(tab.p[goff + j * a.w + slot]) + k), p,
+            nx, same_next, same_prev);
 }
 
 // The call range's elements outside whole packed vectors: [h0, h0 + nh) at
@@ -541,7 +483,7 @@ template <int NR>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
                            int M, int64_t vbeg, int64_t nvec, EdgeElems ed, StepArgs a, PtrTab tab) {
-    const SegMap mp{pm, pm_block, M};
+    const ss::SegMap mp{pm, pm_block, M};
     const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const int n = NR > 0 ? NR : a.N;
@@ -561,7 +503,7 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
         const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
         ss::PmEntry e = mp.pm[m];
-        locate(mp, B, f, m, e);
+        ss::locate(mp, B, f, m, e);
         float s[8];
         sum_ranks<NR>(w, n, s);
         if (NR == 0) add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
@@ -610,7 +552,7 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
             const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
             int m;
-            const ss::PmEntry e = lookup(mp, x, m);
+            const ss::PmEntry e = ss::lookup(mp, x, m);
             if (x >= e.packed_off && x < e.packed_off + e.len)
                 step_scalar<false>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
         }
@@ -765,7 +707,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
                                 int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, EdgeElems ed,
                                 StepArgs a, PtrTab tab) {
     extern __shared__ uint4 stage[];
-    const SegMap mp{pm, pm_block, 0};
+    const ss::SegMap mp{pm, pm_block, 0};
     constexpr unsigned kAll = 0xFFFFFFFFu;
     constexpr int kBufBlocks = kStageBatch * kStageBlocks;  // one batch of ranks
     const int lane = threadIdx.x & 31;
@@ -794,7 +736,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
         }
         if (has && (hkey < 0 || f + 8 > hend)) {  // leaves the last segment: look it up
             int m;
-            const ss::PmEntry e = lookup(mp, f, m);
+            const ss::PmEntry e = ss::lookup(mp, f, m);
             hkey = -1;
             if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
                 hkey = m;
@@ -861,7 +803,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
             if constexpr (NR > 0) {
                 // the entry of element f + i: the last one starting at or before it
                 int c;
-                ss::PmEntry e = lookup(mp, f, c);
+                ss::PmEntry e = ss::lookup(mp, f, c);
                 const float th[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
                 const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
                 const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -877,7 +819,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
                 for (int i = 0; i < 8; ++i) {
                     const int64_t x = f + i;
                     int c;
-                    const ss::PmEntry ex = lookup(mp, x, c);
+                    const ss::PmEntry ex = ss::lookup(mp, x, c);
                     if (x >= ex.packed_off && x < ex.packed_off + ex.len)
                         step_scalar<true>(a, tab, ex.param - a.param_base, x,
                                           ex.param_off + (x - ex.packed_off));
@@ -900,7 +842,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
         if (i < 8 ? i < ed.nh : i - 8 < ed.nt) {
             const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
             int c;
-            const ss::PmEntry ex = lookup(mp, x, c);
+            const ss::PmEntry ex = ss::lookup(mp, x, c);
             if (x >= ex.packed_off && x < ex.packed_off + ex.len)
                 step_scalar<true>(a, tab, ex.param - a.param_base, x, ex.param_off + (x - ex.packed_off));
         }
