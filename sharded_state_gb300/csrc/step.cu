@@ -338,7 +338,7 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     }
     float s[8];
     sum_ranks<NR>(w, n, s);
-    if (NR == 0) add_ranks_beyond_8<UNPACKED>(a, tab, slot, f, k, n, w, s);
+    if (NR == 0 || NR > kMaxVec) add_ranks_beyond_8<UNPACKED>(a, tab, slot, f, k, n, w, s);
     const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
     const int goff = UNPACKED ? n * a.w : 0;
     for (int j = 0; j < a.n_out; ++j)
@@ -506,7 +506,7 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         ss::locate(mp, B, f, m, e);
         float s[8];
         sum_ranks<NR>(w, n, s);
-        if (NR == 0) add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
+        if (NR == 0 || NR > kMaxVec) add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
         if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
             key = m;
@@ -566,7 +566,7 @@ constexpr int kStageBlocks = 33;
 constexpr int kStageBatch = 8;
 constexpr int kStagedWarps = kThreads / 32;
 
-__host__ __device__ constexpr int staged_bufs(int NR) { return NR > 0 ? 1 : 2; }
+__host__ __device__ constexpr int staged_bufs(int NR) { return NR > 0 && NR <= kStageBatch ? 1 : 2; }
 __host__ __device__ constexpr int staged_smem_bytes(int NR) {
     return kStagedWarps * staged_bufs(NR) * kStageBatch * kStageBlocks * 16;
 }
@@ -616,7 +616,7 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
                                            const uint4* wst, float (&s)[8], Pre prefetch_next) {
     constexpr int kBufBlocks = kStageBatch * kStageBlocks;
     const int n = NR > 0 ? NR : a.N;
-    const int nbat = NR > 0 ? 1 : (n + kStageBatch - 1) / kStageBatch;
+    const int nbat = (n + kStageBatch - 1) / kStageBatch;
     auto run = [&](int r) {
         return reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(tab.p[r * a.w + slot0]) +
                                                       k0);
@@ -640,10 +640,10 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
     };
     __syncwarp();  // every lane has read the last round's buffers
     issue(0);
-    if (NR == 0 && nbat > 1) issue(1);
+    if (nbat > 1) issue(1);
     prefetch_next();
     for (int b = 0; b < nbat; ++b) {
-        if (NR == 0 && b + 1 < nbat)
+        if (b + 1 < nbat)
             ss::cp_async_wait<1>();
         else
             ss::cp_async_wait<0>();
@@ -674,7 +674,7 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
                 }
             }
         }
-        if (NR == 0 && b + 2 < nbat) {
+        if (b + 2 < nbat) {
             __syncwarp();  // every lane has read the buffer it refills
             issue(b + 2);
         }
@@ -800,7 +800,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
                 add_rank(s, ss::ld_any16(static_cast<const uint16_t*>(tab.p[r * a.w + slot]) + k));
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
         } else if (has) {  // the vector meets a segment end: element by element
-            if constexpr (NR > 0) {
+            if constexpr (NR > 0 && NR <= kMaxVec) {
                 // the entry of element f + i: the last one starting at or before it
                 int c;
                 ss::PmEntry e = ss::lookup(mp, f, c);
@@ -863,6 +863,9 @@ StagedKern pick_staged(int N, int* smem) {
         case 6: k = fused_step_copyin_staged_kernel<6>; break;
         case 7: k = fused_step_copyin_staged_kernel<7>; break;
         case 8: k = fused_step_copyin_staged_kernel<8>; break;
+        // N = 16 unrolled: both rank batches known at compile time (0.89 -> 0.93
+        // of measured on the 218M-param misaligned set)
+        case 16: k = fused_step_copyin_staged_kernel<16>; break;
         default: k = fused_step_copyin_staged_kernel<0>; break;
     }
     *smem = N <= kStageBatch ? staged_smem_bytes(1) : staged_smem_bytes(0);
