@@ -260,6 +260,43 @@ def test_prepared_step_equals_the_call(ss):
                        rank_grads=packed, params_out=outs_b, n_out=1)(0)  # step 0: EINVAL
 
 
+def test_small_launches_between_dependent_work(ss):
+    """The small one-pass form lets the next launch on the stream start early
+    and waits for its predecessor before touching memory.  Here every step's
+    gradients are made by torch kernels from the previous step's gathered
+    parameters, with no synchronisation anywhere, so each step kernel sits
+    between kernels that produce its inputs and consume its outputs; four
+    steps of that chain equal, bit for bit, the same chain through the
+    two-call path (pack, RS+AdamW, all-gather: launches without early start)."""
+    ps = W.tiny_mlp(2, W.FLAT_ORIG_TRUE)
+    su = Setup(ss, ps)
+    N = su.N
+    results = []
+    for mode in ("two_calls", "one_pass"):
+        shards, master, m, v = _state(ss, su)
+        outs = [p.clone() for p in su.params]
+        packed = [torch.empty(su.total, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+        torch.cuda.synchronize()
+        for step in (1, 2, 3, 4):
+            # rank r's gradient of each parameter, from the gathered parameters
+            grads = [[(o.float() * (0.01 * (r + 1)) - 1e-3 * step).to(torch.bfloat16) for o in outs]
+                     for r in range(N)]
+            hp = ss.adamw_params(step=step, **_hp(step))
+            if mode == "two_calls":
+                for r in range(N):
+                    ss.fsdp_pack(su.plan, grads[r], packed[r])
+                ss.fsdp_reduce_scatter_adamw(su.plan, packed, master, m, v, shards, hp)
+                ss.fsdp_all_gather_unpack(su.plan, shards, outs)
+            else:
+                ss.fsdp_sharded_step(su.plan, master, m, v, shards, hp,
+                                     rank_param_grads=[g for rank in grads for g in rank],
+                                     params_out=outs, n_out=1)
+        torch.cuda.synchronize()
+        results.append([to_np(t) for t in [shards, master, m, v] + outs])
+    for x, y in zip(*results):
+        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
 ORACLE_STATE_CASES = [
     ("small_llama_N8", W.llama_1b2(world_size=8, layers=2, hidden=48, ffn=136, vocab=96)),
     ("awkward1d_false_N7", W.awkward_1d(7, W.FLAT_ORIG_FALSE, torch.bfloat16, count=80)),
