@@ -504,6 +504,23 @@ def test_pack_more_than_2048_params(ss):
         np.testing.assert_array_equal(to_np(o), p)
 
 
+def test_pack_windows_with_pads(ss):
+    """More parameters than one pointer table, so pack runs in parameter
+    windows, and pads in most rank chunks (PER_PARAM_DIM0, N = 3, dim 0 not a
+    multiple of 3): the pad tiles ride with the last window's launch, and
+    every one must be zeroed over a buffer of NaN sentinels."""
+    shapes = [(1 + (13 * i) % 11, 1 + i % 3) for i in range(2300)]
+    ps = W.ParamSet([f"p{i}" for i in range(2300)], shapes, [1000, 1300], 3, W.PER_PARAM_DIM0,
+                    torch.bfloat16, seed=9)
+    su = Setup(ss, ps)
+    assert su.info.pad_numel > 1000
+    packed, whole = guarded(su.total, torch.bfloat16)
+    ss.fsdp_pack(su.plan, su.params, packed)
+    torch.cuda.synchronize()
+    assert guards_intact(whole)
+    np.testing.assert_array_equal(to_np(packed), su.oracle_pack(su.params_np()))
+
+
 def test_one_group_shorthand_matches_create(ss):
     ps = W.awkward_2d(5)
     d0, inner = ps.dim0_inner()
