@@ -1156,6 +1156,23 @@ def _rows_small(ss, peak, want, awkward_scale=1.0, cpu_seconds=4.0):
         _row(f"step on 200 awkward params ({W.LAYOUT_NAMES[kind]}, N=7)",
              st3.info["unpadded_numel"], "params/s", ms, mn, by["step"], peak, cpu,
              extra={"us_per_step": ms * 1e3})
+        # the one pass as a prepared call (ss.ShardedStep), 2000 steps back to back
+        call3 = ss.ShardedStep(st3.plan, st3.master, st3.m, st3.v, st3.shards, st3.next_hp(),
+                               rank_grads=st3._grads_arr, params_out=st3._outs_arr, n_out=1,
+                               stream=torch.cuda.current_stream())
+        step3_no = [st3.t]
+
+        def prepared3():
+            step3_no[0] += 1
+            call3(step3_no[0])
+        ms, mn = _time_back_to_back(prepared3)
+        P3, T3 = st3.info["unpadded_numel"], st3.info["total_numel"]
+        _row(f"step on 200 awkward params ({W.LAYOUT_NAMES[kind]}, N=7): one prepared "
+             "fsdp_sharded_step call (ss.ShardedStep)", P3, "params/s", ms, mn,
+             (2 * 7 + 26) * T3 + 2 * P3, peak,
+             extra={"us_per_step": ms * 1e3,
+                    "timing": "2000 steps back to back between two CUDA events, median of 5 batches"})
+        del call3
 
     # -- the same awkward shapes scaled up until they are bandwidth-bound:
     # odd-sized parameters at odd flat offsets (runs not congruent mod 16 bytes)

@@ -212,8 +212,8 @@ __device__ __forceinline__ uint4 adam_vec(const StepArgs& a, int64_t f, const fl
     return p;
 }
 
-template <bool UNPACKED>
-__device__ __forceinline__ void step_scalar(const StepArgs& a, const PtrTab& tab, int slot,
+template <bool UNPACKED, class Tab>
+__device__ __forceinline__ void step_scalar(const StepArgs& a, const Tab& tab, int slot,
                                             int64_t f, int64_t k) {
     const int n = a.N;
     float s = ss::bf16_to_f32(*grad_ptr<UNPACKED>(a, tab, 0, slot, f, k));
@@ -447,7 +447,8 @@ auto pick_flat(int N) {
 // vector of the same run) when same_next, else only this vector's bytes of
 // it; unless same_prev (the previous vector of the run writes the block
 // before whole), the vector's first 16 - sh bytes go into the block before.
-__device__ __forceinline__ void store_outputs_lane(const StepArgs& a, const PtrTab& tab, int goff,
+template <class Tab>
+__device__ __forceinline__ void store_outputs_lane(const StepArgs& a, const Tab& tab, int goff,
                                                    int slot, int64_t k, uint4 p, uint4 nx,
                                                    bool same_next, bool same_prev) {
     for (int j = 0; j < a.n_out; ++j)
@@ -479,10 +480,12 @@ struct EdgeElems {
 //    segment; pad elements are not stored.
 //  - Threads nvec .. nvec + 15 take the range's edge elements one by one.
 // Lanes never leave before the shuffles, so whole warps take part in them.
-template <int NR>
+template <int NR, bool SMALL = false>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
-                           int M, int64_t vbeg, int64_t nvec, EdgeElems ed, StepArgs a, PtrTab tab) {
+                           int M, int64_t vbeg, int64_t nvec, EdgeElems ed, StepArgs a,
+                           PtrTabT<SMALL ? kTabSmall : kTab> tab) {
+    if (SMALL) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const ss::SegMap mp{pm, pm_block, M};
     const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int lane = threadIdx.x & 31;
@@ -495,6 +498,12 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         const int64_t f = vbeg + 8 * q;
         const int64_t B = f / ss::kMapBlock;
         int m = __ldg(mp.pm_block + B);
+        ss::PmEntry e;
+        if (SMALL) {  // the segment first, then the wait for the previous grid
+            e = mp.pm[m];
+            ss::locate(mp, B, f, m, e);
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+        }
         uint4 w[kMaxVec];
 #pragma unroll
         for (int r = 0; r < kMaxVec; ++r)
@@ -502,8 +511,10 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
         const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
         const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
-        ss::PmEntry e = mp.pm[m];
-        ss::locate(mp, B, f, m, e);
+        if (!SMALL) {
+            e = mp.pm[m];
+            ss::locate(mp, B, f, m, e);
+        }
         float s[8];
         sum_ranks<NR>(w, n, s);
         if (NR == 0 || NR > kMaxVec) add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
@@ -553,6 +564,7 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
             const int64_t x = i < 8 ? ed.h0 + i : ed.t0 + (i - 8);
             int m;
             const ss::PmEntry e = ss::lookup(mp, x, m);
+            if (SMALL) asm volatile("griddepcontrol.wait;" ::: "memory");
             if (x >= e.packed_off && x < e.packed_off + e.len)
                 step_scalar<false>(a, tab, e.param - a.param_base, x, e.param_off + (x - e.packed_off));
         }
@@ -897,16 +909,17 @@ int staged_prepare(StagedKern k, int smem) {
 using FlatAnyKern = void (*)(const ss::PmEntry*, const int*, int, int64_t, int64_t, EdgeElems,
                              StepArgs, PtrTab);
 
-FlatAnyKern pick_flat_any(int N) {
+template <bool SMALL = false>
+auto pick_flat_any(int N) {
     switch (N) {
-        case 2: return fused_step_flat_any_kernel<2>;
-        case 3: return fused_step_flat_any_kernel<3>;
-        case 4: return fused_step_flat_any_kernel<4>;
-        case 5: return fused_step_flat_any_kernel<5>;
-        case 6: return fused_step_flat_any_kernel<6>;
-        case 7: return fused_step_flat_any_kernel<7>;
-        case 8: return fused_step_flat_any_kernel<8>;
-        default: return fused_step_flat_any_kernel<0>;
+        case 2: return fused_step_flat_any_kernel<2, SMALL>;
+        case 3: return fused_step_flat_any_kernel<3, SMALL>;
+        case 4: return fused_step_flat_any_kernel<4, SMALL>;
+        case 5: return fused_step_flat_any_kernel<5, SMALL>;
+        case 6: return fused_step_flat_any_kernel<6, SMALL>;
+        case 7: return fused_step_flat_any_kernel<7, SMALL>;
+        case 8: return fused_step_flat_any_kernel<8, SMALL>;
+        default: return fused_step_flat_any_kernel<0, SMALL>;
     }
 }
 
@@ -1107,6 +1120,27 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                 w0 += cw;
             } while (w0 < nw);
             return SS_OK;
+        }
+        if (nvec + 16 <= kSmallVecs && per_param * a.w <= kTabSmall) {
+            // a launch of a few waves: the small table, and programmatic
+            // stream serialisation (as for the aligned small form)
+            PtrTabSmall ts;
+            std::memcpy(ts.p, tab.p, sizeof ts.p);
+            const auto fs = pick_flat_any<true>(N);
+            cudaLaunchConfig_t cfg;
+            std::memset(&cfg, 0, sizeof cfg);
+            cfg.gridDim = dim3((unsigned)((nvec + 16 + kThreads - 1) / kThreads));
+            cfg.blockDim = dim3(kThreads);
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            const cudaError_t le =
+                cudaLaunchKernelEx(&cfg, fs, (const ss::PmEntry*)plan->d_pm, (const int*)plan->d_pm_block,
+                                   (int)plan->pm.size(), lo8, nvec, ed, a, ts);
+            return le == cudaSuccess ? ss::check_launch() : ss::cuda_fail(le);
         }
         FlatAnyKern ff = pick_flat_any(N);
         constexpr int64_t kChunk = (int64_t)0x7FFFFFF0 * kThreads;  // vectors per launch
