@@ -48,8 +48,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTab = 2048;
 constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
-constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the flat copy-in
-constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) it keeps
+constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the copy-in kernels
+constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) they keep
 constexpr int kFlatRounds = 4;    // most rounds per warp of the aligned flat copy-in
 
 struct RankPtrs {
@@ -141,18 +141,15 @@ __device__ __forceinline__ void add_rank(float (&s)[8], uint4 x) {
 }
 
 // Ranks 8 .. n-1 (N > 8) added to s in rank order, 8 loads in flight at a
-// time in w (free once the first 8 ranks are summed).  ANY: the
-// per-parameter gradients may sit at any 2-byte offset.
-template <bool UNPACKED, bool ANY = false, class Tab>
+// time in w (free once the first 8 ranks are summed).
+template <bool UNPACKED, class Tab>
 __device__ __forceinline__ void add_ranks_beyond_8(const StepArgs& a, const Tab& tab, int slot,
                                                    int64_t f, int64_t k, int n,
                                                    uint4 (&w)[kMaxVec], float (&s)[8]) {
     for (int r0 = kMaxVec; r0 < n; r0 += kMaxVec) {
 #pragma unroll
         for (int j = 0; j < kMaxVec; ++j)
-            if (r0 + j < n)
-                w[j] = ANY ? ss::ld_any16(grad_ptr<UNPACKED>(a, tab, r0 + j, slot, f, k))
-                           : ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r0 + j, slot, f, k));
+            if (r0 + j < n) w[j] = ss::ld_stream_u4(grad_ptr<UNPACKED>(a, tab, r0 + j, slot, f, k));
 #pragma unroll
         for (int j = 0; j < kMaxVec; ++j)
             if (r0 + j < n) add_rank(s, w[j]);
