@@ -1217,6 +1217,15 @@ def _rows_small(ss, peak, want, awkward_scale=1.0, cpu_seconds=4.0):
         ms, mn = _time_stream(lambda: st4.all_gather(), 20)
         _row(f"large awkward ({name}, N=7): all-gather + unpack", P4, "params/s", ms, mn, 4 * P4,
              peak)
+        # context for the two rows above: torch's own device copy of the same
+        # bytes (P4 bf16 elements read and written), the operation the measured
+        # peak is taken with, at this size
+        src = torch.empty(P4, dtype=torch.bfloat16, device="cuda")
+        dst = torch.empty_like(src)
+        ms, mn = _time_stream(lambda: dst.copy_(src), 20)
+        _row(f"large awkward ({name}, N=7): torch copy_ of the same bytes (context)", P4,
+             "params/s", ms, mn, 4 * P4, peak)
+        del src, dst
         # every rank's copy (n_out = N = 7 replicas, separately allocated)
         outs7 = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(7)
                  for n in ps4.numels()]
