@@ -50,7 +50,6 @@ constexpr int kTab = 2048;
 constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
 constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the copy-in kernels
 constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) they keep
-constexpr int kTailScale = 8;     // eighths of a wave per level of shorter warps at the end
 constexpr int kFlatRounds = 4;    // most rounds per warp of the aligned flat copy-in
 
 struct RankPtrs {
@@ -462,18 +461,6 @@ struct EdgeElems {
     int nh, nt;
 };
 
-// Rounds per warp of the staged copy-in: warps below w[0] take `iters`
-// rounds from round gw * iters; the last launch's final warps (levels k =
-// 0..n-1: warps [w[k], w[k+1]), sz[k] rounds each from round r[k]) take
-// fewer, so that the CTAs dispatched last end sooner.
-constexpr int kTailLevels = 3;
-struct WarpRounds {
-    int64_t w[kTailLevels + 1];
-    int64_t r[kTailLevels];
-    int sz[kTailLevels];
-    int n;
-};
-
 // Flat form of the one-pass step for packed gradients at any alignment of the
 // runs and of the per-parameter outputs.  Thread q takes the 8-aligned packed
 // vector f = vbeg + 8q; its gradient and state loads are aligned and go out
@@ -706,11 +693,8 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
 // Flat form of the one-pass step with per-parameter gradients (fused
 // copy-in) at any alignment of the runs and the pointers, for any N, in one
 // pass.  Warp gw takes `iters` rounds of 32 consecutive 8-aligned packed
-// vectors, lane = vector, except the launch's final warps, which take fewer
-// (wr: the CTAs dispatched last end sooner, and the launch's tail with them);
-// a CTA's warps take consecutive rounds, so the CTAs walk HBM in address
-// order and each works in one place.  A lane keeps the segment of its last
-// vector and looks it up in the packed segment map only when it leaves it.  When every
+// vectors, lane = vector; a lane keeps the segment of its last vector and
+// looks it up in the packed segment map only when it leaves it.  When every
 // vector of the round lies in one segment (all but the rounds that meet a
 // segment end), the warp's gradient bytes of rank r are one contiguous run of
 // the rank's tensor: the warp copies the aligned 16-byte blocks covering it
@@ -729,8 +713,8 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
 template <int NR>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
-                                int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, WarpRounds wr,
-                                EdgeElems ed, StepArgs a, PtrTab tab) {
+                                int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, EdgeElems ed,
+                                StepArgs a, PtrTab tab) {
     extern __shared__ uint4 stage[];
     const ss::SegMap mp{pm, pm_block, 0};
     constexpr unsigned kAll = 0xFFFFFFFFu;
@@ -745,16 +729,8 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
     const int64_t fend = vbeg + 8 * nvec;
     int64_t hend = 0, hdelta = 0;  // the lane's last segment: its end and k - f,
     int hslot = 0, hkey = -1;      // its parameter slot and map index (-1: none)
-    int64_t r0 = gw * iters;  // the warp's first round and its count
-    int nr = iters;
-    for (int k = 0; k < wr.n; ++k) {
-        if (gw >= wr.w[k] && gw < wr.w[k + 1]) {
-            r0 = wr.r[k] + (gw - wr.w[k]) * wr.sz[k];
-            nr = wr.sz[k];
-        }
-    }
-    int64_t f = vbeg + 8 * (r0 * 32 + lane);
-    for (int it = gw < nwarps ? nr : 0; it > 0; --it, f += 8 * 32) {
+    int64_t f = vbeg + 8 * (gw * iters * 32 + lane);
+    for (int it = gw < nwarps ? iters : 0; it > 0; --it, f += 8 * 32) {
         if (__shfl_sync(kAll, f, 0) >= fend) break;  // the same for the whole warp
         const bool has = f < fend;
         const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -883,7 +859,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
 }
 
 using StagedKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int,
-                            WarpRounds, EdgeElems, StepArgs, PtrTab);
+                            EdgeElems, StepArgs, PtrTab);
 
 StagedKern pick_staged(int N, int* smem) {
     StagedKern k;
@@ -1128,42 +1104,14 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             const int64_t nw = (nvec + span - 1) / span;
             constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
             int64_t w0 = 0;
-            // warps resident at once (3 CTAs per SM)
-            const int64_t res = 3 * (int64_t)ss::num_sms() * kStagedWarps;
             do {
                 const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
                 const bool last = w0 + cw >= nw;
                 const int64_t cv = last ? nvec - span * w0 : span * cw;
-                // The last launch's final rounds go to shorter-lived warps:
-                // level k (k = 0, 1, 2) takes about kTailScale / 8 of a wave of
-                // warps of iters / 2, iters / 4 and 1 rounds each, so the CTAs
-                // dispatched last end after a fraction of the others' time.
-                WarpRounds wr;
-                std::memset(&wr, 0, sizeof wr);
-                int64_t nwk = cw;  // warps with rounds (the edge warp aside)
-                const int64_t R = (cv + 31) / 32;
-                int64_t tail = 0;
-                for (int k = 0; k < kTailLevels; ++k) tail += res * (iters >> (k + 1)) * kTailScale / 8;
-                if (last && iters >= 8 && R >= 4 * tail + iters) {
-                    const int64_t M = (R - tail) / iters * iters;  // rounds of the full warps
-                    int64_t w = M / iters, r = M;
-                    for (int k = 0; k < kTailLevels; ++k) {
-                        const int sz = k + 1 < kTailLevels ? iters >> (k + 1) : 1;
-                        const int64_t L = k + 1 < kTailLevels ? res * sz * kTailScale / 8 / sz * sz : R - r;
-                        wr.w[k] = w;
-                        wr.r[k] = r;
-                        wr.sz[k] = sz;
-                        w += (L + sz - 1) / sz;
-                        r += L;
-                    }
-                    wr.w[kTailLevels] = w;
-                    wr.n = kTailLevels;
-                    nwk = w;
-                }
-                const int64_t warps = nwk + (last ? 1 : 0);
+                const int64_t warps = cw + (last ? 1 : 0);
                 const unsigned grid = (unsigned)((warps + kStagedWarps - 1) / kStagedWarps);
                 fk<<<grid, kThreads, smem, st>>>(plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv,
-                                                 nwk, iters, wr, last ? ed : none, a, tab);
+                                                 cw, iters, last ? ed : none, a, tab);
                 rc = ss::check_launch();
                 if (rc) return rc;
                 w0 += cw;

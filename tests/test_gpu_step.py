@@ -501,17 +501,29 @@ def test_sharded_step_full_size_copy_in_equals_pack_and_two_calls(ss):
     torch.cuda.empty_cache()
 
 
-def test_sharded_step_copy_in_two_pass_chunks_equal_pack_and_two_calls(ss):
-    """Per-parameter gradients at N = 9 on a misaligned plan of about 80M
-    params: the copy-in runs in two passes (ranks 0..7 summed into fp32
-    scratch, then rank 8 and AdamW) over more than one chunk of 8M vectors,
-    and must equal packing each set and running the two calls bit for bit."""
-    ps = W.awkward_1d(9, W.FLAT_ORIG_FALSE, torch.bfloat16, count=40, max_len=4_500_000)
+LARGE_COPY_IN_CASES = [
+    ("awkward1d_false_N9_80M",
+     lambda: W.awkward_1d(9, W.FLAT_ORIG_FALSE, torch.bfloat16, count=40, max_len=4_500_000)),
+    ("awkward2d_N7_67M", lambda: W.awkward_2d(7, count=200, max_rows=200_000)),
+]
+
+
+@pytest.mark.parametrize("name,make", LARGE_COPY_IN_CASES, ids=[c[0] for c in LARGE_COPY_IN_CASES])
+def test_sharded_step_large_copy_in_equals_pack_and_two_calls(ss, name, make):
+    """Per-parameter gradients on misaligned plans of 67M-87M params (N = 9:
+    the general instance, ranks in two batches; N = 7 PER_PARAM_DIM0: its own
+    instance, with pads in most rank chunks): tens of waves of warps of 8
+    rounds each, and the step must equal packing each set and running the
+    two calls bit for bit (pads, zero in the packed shards, stay zero)."""
+    ps = make()
     su = Setup(ss, ps, make_values=False)
     total, N = su.total, su.N
-    assert total // 8 > (1 << 23) + 248  # more than one chunk
+    assert total >= 30_000_000
     gen = torch.Generator(device="cuda").manual_seed(45)
-    init = (torch.randn(total, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+    # shards packed from parameters, so the pads hold zero as the step expects
+    init = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+    ss.fsdp_pack(su.plan, [(torch.randn(s, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+                           for s in ps.shapes], init)
     sets = [[(torch.randn(s, device="cuda", generator=gen) * 1e-3).to(torch.bfloat16)
              for s in ps.shapes] for _ in range(N)]
     res = []
