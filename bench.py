@@ -67,8 +67,9 @@ def parse_args():
                     help="step: the one-line headline; rows: one JSON line per hot-path row")
     ap.add_argument("--rows", default="all",
                     help="rows mode: comma list of llama,block4096,tiny,awkward,awkward_large,"
-                         "awkward_n16,ddp (default all; awkward_large: only the large awkward "
-                         "sets; awkward_n16: the 1-D awkward set at N = 16)")
+                         "awkward_n16,world_sizes,ddp (default all; awkward_large: only the large "
+                         "awkward sets; awkward_n16: the 1-D awkward set at N = 16; world_sizes: "
+                         "the 1.2B model at N = 2, 4, 16 and 32)")
     ap.add_argument("--step-kind", default="fused", choices=["two_calls", "fused", "copy_in"],
                     help="timed step: the one-pass fsdp_sharded_step from packed gradients "
                          "(default), RS+AdamW then all-gather as two calls, or the one pass "
@@ -888,7 +889,8 @@ def run_rows(args):
     K = max(args.steps, 5)
     bits = lambda t: t.reshape(-1).cpu().view(torch.int16).numpy().view(np.uint16).copy()
     want = set(args.rows.split(",")) if args.rows != "all" else {"llama", "block4096", "tiny",
-                                                                 "awkward", "awkward_n16", "ddp"}
+                                                                 "awkward", "awkward_n16",
+                                                                 "world_sizes", "ddp"}
     if "llama" in want:
         _rows_llama(args, ss, oracle, peak, used, K, bits)
     if "block4096" in want:
@@ -897,6 +899,8 @@ def run_rows(args):
         _rows_small(ss, peak, want, args.awkward_scale, args.cpu_seconds)
     if "awkward_n16" in want:
         _rows_awkward_wide(ss, peak, args.awkward_scale)
+    if "world_sizes" in want:
+        _rows_world_sizes(ss, peak)
     if "ddp" in want:
         _rows_ddp(args, ss, oracle, peak, used, K, bits)
 
@@ -1283,6 +1287,23 @@ def _rows_awkward_wide(ss, peak, awkward_scale=1.0):
          "params/s", ms, mn, (2 * N + 2) * P + 26 * tot, peak)
     del rank_sets, flat_pg, st
     torch.cuda.empty_cache()
+
+
+def _rows_world_sizes(ss, peak):
+    # -- the 1.2B model at other world sizes: N = 2 and 4 (unrolled
+    # instances), 16 (its own instance) and 32 (the general instance)
+    for N in (2, 4, 16, 32):
+        ps = W.llama_1b2(world_size=N)
+        st = Step(ss, ps, 1)
+        P, tot = st.info["unpadded_numel"], st.info["total_numel"]
+        ms, mn = _time_stream(lambda: st.rs_adamw(), 20)
+        _row(f"1.2B model, N={N}: RS + AdamW", P, "params/s", ms, mn, (2 * N + 26) * tot, peak,
+             extra={"world_size": N})
+        ms, mn = _time_stream(lambda: st.fused_step(), 20)
+        _row(f"1.2B model, N={N}: one-pass step", P, "params/s", ms, mn, (2 * N + 26) * tot + 2 * P,
+             peak, extra={"world_size": N})
+        del st
+        torch.cuda.empty_cache()
 
 
 def _rows_ddp(args, ss, oracle, peak, used, K, bits):

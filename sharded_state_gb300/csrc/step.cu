@@ -307,9 +307,19 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
         for (int r = 0; r < kMaxVec; ++r)
             if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f);
     }
-    const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
-    const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
-    const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+    // N > 8 (the general instance): the state is loaded after the ranks are
+    // summed, so that its registers are not held across the rank batches
+    constexpr bool kRanksFirst = NR == 0;
+    float4 t0, t1, m0, m1, v0, v1;
+    auto load_state = [&]() {
+        t0 = ss::ld_rw_f4(a.master + f);
+        t1 = ss::ld_rw_f4(a.master + f + 4);
+        m0 = ss::ld_rw_f4(a.exp_avg + f);
+        m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
+        v0 = ss::ld_rw_f4(a.exp_avg_sq + f);
+        v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
+    };
+    if (!kRanksFirst) load_state();
     if (!SMALL) {
         e = pm[m];
         if (f < e.packed_off || f >= e.packed_off + e.len) {  // a segment starts inside the block
@@ -336,6 +346,7 @@ fused_step_flat_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict
     float s[8];
     sum_ranks<NR>(w, n, s);
     if (NR == 0 || NR > kMaxVec) add_ranks_beyond_8<UNPACKED>(a, tab, slot, f, k, n, w, s);
+    if (kRanksFirst) load_state();
     const uint4 p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
     const int goff = UNPACKED ? n * a.w : 0;
     for (int j = 0; j < a.n_out; ++j)
@@ -505,6 +516,12 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
 #pragma unroll
         for (int r = 0; r < kMaxVec; ++r)
             if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f);
+        float s[8];
+        constexpr bool kRanksFirst = NR == 0 || NR > kMaxVec;  // the ranks summed before the state loads
+        if (kRanksFirst) {
+            sum_ranks<NR>(w, n, s);
+            add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
+        }
         const float4 t0 = ss::ld_rw_f4(a.master + f), t1 = ss::ld_rw_f4(a.master + f + 4);
         const float4 m0 = ss::ld_rw_f4(a.exp_avg + f), m1 = ss::ld_rw_f4(a.exp_avg + f + 4);
         const float4 v0 = ss::ld_rw_f4(a.exp_avg_sq + f), v1 = ss::ld_rw_f4(a.exp_avg_sq + f + 4);
@@ -512,9 +529,10 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
             e = mp.pm[m];
             ss::locate(mp, B, f, m, e);
         }
-        float s[8];
-        sum_ranks<NR>(w, n, s);
-        if (NR == 0 || NR > kMaxVec) add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
+        if (!kRanksFirst) {
+            sum_ranks<NR>(w, n, s);
+            if (NR == 0 || NR > kMaxVec) add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
+        }
         if (f >= e.packed_off && f + 8 <= e.packed_off + e.len) {
             p = adam_vec(a, f, s, n, t0, t1, m0, m1, v0, v1);
             key = m;
@@ -909,6 +927,7 @@ using FlatAnyKern = void (*)(const ss::PmEntry*, const int*, int, int64_t, int64
 template <bool SMALL = false>
 auto pick_flat_any(int N) {
     switch (N) {
+        case 1: return fused_step_flat_any_kernel<1, SMALL>;
         case 2: return fused_step_flat_any_kernel<2, SMALL>;
         case 3: return fused_step_flat_any_kernel<3, SMALL>;
         case 4: return fused_step_flat_any_kernel<4, SMALL>;
@@ -916,6 +935,7 @@ auto pick_flat_any(int N) {
         case 6: return fused_step_flat_any_kernel<6, SMALL>;
         case 7: return fused_step_flat_any_kernel<7, SMALL>;
         case 8: return fused_step_flat_any_kernel<8, SMALL>;
+        case 16: return fused_step_flat_any_kernel<16, SMALL>;
         default: return fused_step_flat_any_kernel<0, SMALL>;
     }
 }
