@@ -437,6 +437,7 @@ using FlatKernSmall = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t,
 template <bool U, bool SMALL = false>
 auto pick_flat(int N) {
     switch (N) {
+        case 1: return fused_step_flat_kernel<1, U, SMALL>;
         case 2: return fused_step_flat_kernel<2, U, SMALL>;
         case 3: return fused_step_flat_kernel<3, U, SMALL>;
         case 4: return fused_step_flat_kernel<4, U, SMALL>;
@@ -517,7 +518,10 @@ fused_step_flat_any_kernel(const ss::PmEntry* __restrict__ pm, const int* __rest
         for (int r = 0; r < kMaxVec; ++r)
             if (r < n) w[r] = ss::ld_stream_u4(static_cast<const uint16_t*>(a.packed_grads.p[r]) + f);
         float s[8];
-        constexpr bool kRanksFirst = NR == 0 || NR > kMaxVec;  // the ranks summed before the state loads
+        // N > 8: the ranks are summed before the state is loaded, so that the
+        // state's registers are not held across the rank batches (without
+        // it the general instance spills)
+        constexpr bool kRanksFirst = NR == 0 || NR > kMaxVec;
         if (kRanksFirst) {
             sum_ranks<NR>(w, n, s);
             add_ranks_beyond_8<false>(a, tab, 0, f, 0, n, w, s);
