@@ -58,7 +58,16 @@ CASES = [("tiny_mlp", W.tiny_mlp(2, W.FLAT_ORIG_TRUE)),
          # every 2048-element block, so the flat kernel's binary search runs
          ("tiny_params_N4", W.ParamSet([f"t{i}" for i in range(500)],
                                        [(1 + (7 * i) % 9, 8) for i in range(500)],
-                                       [500], 4, W.PER_PARAM_DIM0, torch.bfloat16, seed=13))]
+                                       [500], 4, W.PER_PARAM_DIM0, torch.bfloat16, seed=13)),
+         # 4.3M-8.9M params: more vectors than a small launch takes, so the
+         # large forms of the N = 1, N = 16 and general instances run
+         ("awkward1d_false_N1_large",
+          W.awkward_1d(1, W.FLAT_ORIG_FALSE, torch.bfloat16, count=30, max_len=300_000)),
+         ("awkward1d_false_N16_large",
+          W.awkward_1d(16, W.FLAT_ORIG_FALSE, torch.bfloat16, count=30, max_len=300_000)),
+         ("awkward1d_true_N17_large",
+          W.awkward_1d(17, W.FLAT_ORIG_TRUE, torch.bfloat16, count=30, max_len=300_000)),
+         ("llama_N1_large", W.llama_1b2(world_size=1, layers=2, hidden=512, ffn=1536, vocab=2048))]
 
 
 def _state(ss, su):
