@@ -198,12 +198,11 @@ using DdpKernel = void (*)(const int64_t*, const void* const*, int, int, int);
 // while the previous bucket's kernel on the stream is still finishing.
 cudaError_t launch_bucket(DdpKernel fn, unsigned grid, cudaStream_t st, const int64_t* prefix,
                           const void* const* ptrs, int N, int o_lo, int o_hi) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[1] = {};
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;

@@ -1057,12 +1057,11 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                 PtrTabSmall ts;
                 std::memcpy(ts.p, tab.p, sizeof ts.p);
                 const auto fs = unpacked ? pick_flat<true, true>(N) : pick_flat<false, true>(N);
-                cudaLaunchConfig_t cfg;
-                std::memset(&cfg, 0, sizeof cfg);
+                cudaLaunchConfig_t cfg = {};
                 cfg.gridDim = dim3((unsigned)((nvec + kThreads - 1) / kThreads));
                 cfg.blockDim = dim3(kThreads);
                 cfg.stream = st;
-                cudaLaunchAttribute attr[1];
+                cudaLaunchAttribute attr[1] = {};
                 attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
                 attr[0].val.programmaticStreamSerializationAllowed = 1;
                 cfg.attrs = attr;
@@ -1148,12 +1147,11 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             PtrTabSmall ts;
             std::memcpy(ts.p, tab.p, sizeof ts.p);
             const auto fs = pick_flat_any<true>(N);
-            cudaLaunchConfig_t cfg;
-            std::memset(&cfg, 0, sizeof cfg);
+            cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)((nvec + 16 + kThreads - 1) / kThreads));
             cfg.blockDim = dim3(kThreads);
             cfg.stream = st;
-            cudaLaunchAttribute attr[1];
+            cudaLaunchAttribute attr[1] = {};
             attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
