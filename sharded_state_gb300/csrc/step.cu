@@ -714,9 +714,11 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
 
 // Flat form of the one-pass step with per-parameter gradients (fused
 // copy-in) at any alignment of the runs and the pointers, for any N, in one
-// pass.  Warp gw takes `iters` rounds of 32 consecutive 8-aligned packed
-// vectors, lane = vector; a lane keeps the segment of its last vector and
-// looks it up in the packed segment map only when it leaves it.  When every
+// pass.  A CTA takes 8 * iters rounds of 32 consecutive 8-aligned packed
+// vectors, lane = vector, and its warp wib every 8th of them from round wib,
+// so that the CTA's warps read neighbouring runs at once; a lane keeps the
+// segment of its last vector and looks it up in the packed segment map only
+// when it leaves it.  When every
 // vector of the round lies in one segment (all but the rounds that meet a
 // segment end), the warp's gradient bytes of rank r are one contiguous run of
 // the rank's tensor: the warp copies the aligned 16-byte blocks covering it
@@ -751,8 +753,12 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
     const int64_t fend = vbeg + 8 * nvec;
     int64_t hend = 0, hdelta = 0;  // the lane's last segment: its end and k - f,
     int hslot = 0, hkey = -1;      // its parameter slot and map index (-1: none)
-    int64_t f = vbeg + 8 * (gw * iters * 32 + lane);
-    for (int it = gw < nwarps ? iters : 0; it > 0; --it, f += 8 * 32) {
+    // the CTA's 8 * iters rounds, interleaved: warp wib takes rounds wib,
+    // wib + 8, ... of them, so the CTA's warps read neighbouring 512-byte runs
+    // of each rank at once (4 KiB together) rather than runs 8 rounds apart
+    constexpr int64_t kStride = 8 * 32 * kStagedWarps;  // elements between a warp's rounds
+    int64_t f = vbeg + 8 * (((int64_t)blockIdx.x * kStagedWarps * iters + wib) * 32 + lane);
+    for (int it = iters; it > 0; --it, f += kStride) {
         if (__shfl_sync(kAll, f, 0) >= fend) break;  // the same for the whole warp
         const bool has = f < fend;
         const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -785,12 +791,12 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
             const int nl = __popc(__ballot_sync(kAll, has));  // lanes 0..nl-1 hold vectors
             const int64_t k0 = __shfl_sync(kAll, k, 0);
             const int slot0 = __shfl_sync(kAll, slot, 0);
-            // the lane's next vector, 32 on: its state and (when it stays in
-            // this segment) its first batch's gradient lines into L2 while
-            // this round computes, so the next round's copies wait for L2
-            // rather than DRAM
+            // the lane's next vector, 8 rounds on: its state and (when it
+            // stays in this segment) its first batch's gradient lines into L2
+            // while this round computes, so the next round's copies wait for
+            // L2 rather than DRAM
             auto prefetch_next = [&]() {
-                const int64_t fn = f + 8 * 32;
+                const int64_t fn = f + kStride;
                 if (it > 1 && fn < fend) {
                     ss::prefetch_l2(a.master + fn);
                     ss::prefetch_l2(a.exp_avg + fn);
