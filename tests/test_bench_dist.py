@@ -141,3 +141,38 @@ def test_host_stall_detection():
     assert bench.host_stall([8.7] * 199 + [4550.0])            # a multi-second stall
     assert bench.host_stall([0.44, 4550.0, 0.44])
     assert not bench.host_stall([0.02] * 99 + [0.5])           # 25x, but under 1 ms
+
+
+def _run_reference_line(monkeypatch, budget_s):
+    import argparse
+    import contextlib
+    import io
+    import json
+
+    import workloads as W
+    ps = W.llama_1b2(world_size=8, layers=3, hidden=48, ffn=136, vocab=96)  # 4 groups
+    monkeypatch.setattr(bench, "make_workload", lambda name: ps)
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", budget_s)
+    args = argparse.Namespace(workload="small", steps=2, warmup=2, n_out=1, step_kind="fused")
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.run_reference(args, 1, 0)
+    return json.loads(buf.getvalue().strip().splitlines()[-1]), ps
+
+
+def test_reference_arm_runs_the_whole_workload_within_its_budget(monkeypatch):
+    out, ps = _run_reference_line(monkeypatch, 1e9)
+    assert out["impl"] == "reference" and out["steps"] == 2 and out["warmup"] == 2
+    assert out["cpu_baseline"]["sample"].startswith("the whole workload per step: all 4 groups")
+    assert out["value"] > 0 and out["e2e"]["value"] == out["value"]
+
+
+def test_reference_arm_cuts_to_a_prefix_of_groups_past_its_budget(monkeypatch):
+    """When the first warm-up step says the warm-up and timed steps would
+    take longer than REFERENCE_BUDGET_S, each step runs a prefix of the
+    groups, the sample says how many, and the line still times K steps."""
+    out, ps = _run_reference_line(monkeypatch, 0.0)
+    assert out["steps"] == 2
+    sample = out["cpu_baseline"]["sample"]
+    first = ps.numels()[:ps.groups[0]]
+    assert sample.startswith(f"the first 1 of 4 groups per step ({sum(first):,} params)"), sample
