@@ -1080,7 +1080,7 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             if (fr) {
                 // rounds of 32 vectors per warp, as many as keep kCopyinWaves
                 // waves of CTAs (at most kFlatRounds)
-                int64_t it = nvec / ((int64_t)kThreads * kCopyinWaves * 3 * 152);
+                int64_t it = nvec / ((int64_t)kThreads * kCopyinWaves * 3 * ss::num_sms());
                 const int iters = (int)(it < 1 ? 1 : it > kFlatRounds ? kFlatRounds : it);
                 const int64_t span = 32 * (int64_t)iters;  // vectors per warp
                 const int64_t nw = (nvec + span - 1) / span;
@@ -1127,7 +1127,7 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             int rc = staged_prepare(fk, smem);
             if (rc) return rc;
             const int64_t per_round = 32 * (int64_t)kStagedWarps;  // vectors per CTA round
-            int64_t it = nvec / (per_round * kCopyinWaves * 3 * 152);
+            int64_t it = nvec / (per_round * kCopyinWaves * 3 * ss::num_sms());
             const int iters = (int)(it < 1 ? 1 : it > kCopyinIters ? kCopyinIters : it);
             const int64_t span = 32 * (int64_t)iters;  // vectors per warp
             const int64_t nw = (nvec + span - 1) / span;
