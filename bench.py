@@ -68,8 +68,9 @@ def parse_args():
     ap.add_argument("--rows", default="all",
                     help="rows mode: comma list of llama,block4096,tiny,awkward,awkward_large,"
                          "awkward_n16,world_sizes,ddp (default all; awkward_large: only the large "
-                         "awkward sets; awkward_n16: the 1-D awkward set at N = 16; world_sizes: "
-                         "the 1.2B model at N = 2, 4, 16 and 32)")
+                         "awkward sets; awkward_n16: the 1-D awkward set at N = 16 and 800 "
+                         "per-parameter-layout params in one group; world_sizes: the 1.2B model "
+                         "at N = 2, 4, 16 and 32)")
     ap.add_argument("--step-kind", default="fused", choices=["two_calls", "fused", "copy_in"],
                     help="timed step: the one-pass fsdp_sharded_step from packed gradients "
                          "(default), RS+AdamW then all-gather as two calls, or the one pass "
@@ -1285,6 +1286,23 @@ def _rows_awkward_wide(ss, peak, awkward_scale=1.0):
     ms, mn = _time_stream(lambda: st.fused_step(param_grads=flat_pg), 20)
     _row(f"large awkward (flat_orig_false, N={N}): one-pass step with fused copy-in", P,
          "params/s", ms, mn, (2 * N + 2) * P + 26 * tot, peak)
+    del rank_sets, flat_pg, st
+    torch.cuda.empty_cache()
+    # -- 800 PER_PARAM_DIM0 parameters in one group at N = 7: with per-parameter
+    # gradients the pointers (8 per parameter) overflow one table, so the call
+    # runs in parameter windows, each window's data in 7 runs (one per shard)
+    ps = W.awkward_2d(7, count=800, max_rows=int(100_000 * awkward_scale))
+    st = Step(ss, ps, 1)
+    P, tot = st.info["unpadded_numel"], st.info["total_numel"]
+    ms, mn = _time_stream(lambda: st.fused_step(), 20)
+    _row(f"large awkward (per_param_dim0, 800 params in one group, {P:,} params, N=7): one-pass step",
+         P, "params/s", ms, mn, (2 * 7 + 26) * tot + 2 * P, peak)
+    rank_sets = list(st._rank_grad_iter("cuda"))
+    flat_pg = ss.ptr_array([g for rank in rank_sets for g in rank])
+    ms, mn = _time_stream(lambda: st.fused_step(param_grads=flat_pg), 20)
+    _row("large awkward (per_param_dim0, 800 params in one group, N=7): one-pass step with fused "
+         "copy-in (4 parameter windows x 7 runs)", P, "params/s", ms, mn, (2 * 7 + 2) * P + 26 * tot,
+         peak)
     del rank_sets, flat_pg, st
     torch.cuda.empty_cache()
 

@@ -49,7 +49,8 @@ constexpr int kThreads = 256;
 constexpr int kTab = 2048;
 constexpr int kMaxVec = 8;  // gradient vectors kept in flight per thread (ranks 0..7)
 constexpr int kCopyinIters = 8;   // most rounds of vectors per warp in the copy-in kernels
-constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) they keep
+constexpr int kCopyinWaves = 16;  // fewest waves of CTAs (3 per SM) the aligned copy-in keeps
+constexpr int kCopyinMinWaves = 2;  // fewest waves of CTAs the staged copy-in keeps
 constexpr int kFlatRounds = 4;    // most rounds per warp of the aligned flat copy-in
 
 struct RankPtrs {
@@ -737,9 +738,14 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
 template <int NR>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
-                                int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, EdgeElems ed,
-                                StepArgs a, PtrTab tab) {
+                                int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, int pdl,
+                                EdgeElems ed, StepArgs a, PtrTab tab) {
     extern __shared__ uint4 stage[];
+    // pdl bit 0: the call's next staged launch (another window's runs) may
+    // start once every CTA here has; bit 1: this launch ends only after the
+    // one before it (programmatic dependent launch: the launches touch
+    // disjoint elements, and a following kernel still sees both done)
+    if (pdl & 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const ss::SegMap mp{pm, pm_block, 0};
     constexpr unsigned kAll = 0xFFFFFFFFu;
     constexpr int kBufBlocks = kStageBatch * kStageBlocks;  // one batch of ranks
@@ -884,9 +890,10 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
                 step_scalar<true>(a, tab, ex.param - a.param_base, x, ex.param_off + (x - ex.packed_off));
         }
     }
+    if (pdl & 2) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-using StagedKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int,
+using StagedKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int, int,
                             EdgeElems, StepArgs, PtrTab);
 
 StagedKern pick_staged(int N, int* smem) {
@@ -1049,6 +1056,7 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                 tab.p[goff + j * a.w + (i - wa)] = s->params_out[(size_t)j * n + i];
         }
     };
+    bool staged_launched = false;  // a staged copy-in launch of this call is queued
     // The step over packed range [rlo, rhi), whose data segments all belong to
     // the parameters in the pointer table.
     auto run = [&](int64_t rlo, int64_t rhi) -> int {
@@ -1120,14 +1128,14 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         const EdgeElems none{0, 0, 0, 0};
         if (unpacked) {
             // rounds of 32 vectors per warp, as many rounds per warp as keep
-            // kCopyinWaves waves of CTAs (at most kCopyinIters), and one
-            // extra warp for the edges
+            // 2 waves of CTAs (at most kCopyinIters), and one extra warp for
+            // the edges
             int smem = 0;
             const StagedKern fk = pick_staged(N, &smem);
             int rc = staged_prepare(fk, smem);
             if (rc) return rc;
             const int64_t per_round = 32 * (int64_t)kStagedWarps;  // vectors per CTA round
-            int64_t it = nvec / (per_round * kCopyinWaves * 3 * ss::num_sms());
+            int64_t it = nvec / (per_round * kCopyinMinWaves * 3 * ss::num_sms());
             const int iters = (int)(it < 1 ? 1 : it > kCopyinIters ? kCopyinIters : it);
             const int64_t span = 32 * (int64_t)iters;  // vectors per warp
             const int64_t nw = (nvec + span - 1) / span;
@@ -1139,10 +1147,26 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
                 const int64_t cv = last ? nvec - span * w0 : span * cw;
                 const int64_t warps = cw + (last ? 1 : 0);
                 const unsigned grid = (unsigned)((warps + kStagedWarps - 1) / kStagedWarps);
-                fk<<<grid, kThreads, smem, st>>>(plan->d_pm, plan->d_pm_block, lo8 + 8 * span * w0, cv,
-                                                 cw, iters, last ? ed : none, a, tab);
-                rc = ss::check_launch();
+                // launches after a call's first staged one may start while it
+                // ends (programmatic dependent launch); each ends only after
+                // the one before it
+                const int pdl = staged_launched ? 3 : 1;
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(grid);
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = (size_t)smem;
+                cfg.stream = st;
+                cudaLaunchAttribute attr[1] = {};
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = staged_launched ? 1 : 0;
+                const cudaError_t le = cudaLaunchKernelEx(&cfg, fk, (const ss::PmEntry*)plan->d_pm,
+                                                          (const int*)plan->d_pm_block, lo8 + 8 * span * w0, cv,
+                                                          cw, iters, pdl, last ? ed : none, a, tab);
+                rc = le == cudaSuccess ? ss::check_launch() : ss::cuda_fail(le);
                 if (rc) return rc;
+                staged_launched = true;
                 w0 += cw;
             } while (w0 < nw);
             return SS_OK;

@@ -514,6 +514,11 @@ LARGE_COPY_IN_CASES = [
     ("awkward1d_false_N9_80M",
      lambda: W.awkward_1d(9, W.FLAT_ORIG_FALSE, torch.bfloat16, count=40, max_len=4_500_000)),
     ("awkward2d_N7_67M", lambda: W.awkward_2d(7, count=200, max_rows=200_000)),
+    # 800 parameters in one group: 8 pointers each overflow the 2048-slot
+    # table, so the call runs in parameter windows, each window's data in 7
+    # runs (one per rank shard): 28 launches, chained by programmatic
+    # dependent launch
+    ("awkward2d_N7_800params_windows", lambda: W.awkward_2d(7, count=800, max_rows=40_000)),
 ]
 
 
