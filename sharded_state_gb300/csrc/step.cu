@@ -733,13 +733,29 @@ __device__ __forceinline__ void staged_sum(const StepArgs& a, const PtrTab& tab,
 // straight from global memory (ld_any16) and run the others element by
 // element.  Every block read holds at least one byte of the run, so no load
 // leaves the gradient tensor's 16-byte blocks.  Outputs as in
-// fused_step_flat_any_kernel; the range's edge elements run on lanes 0..15 of
-// warp nwarps.
+// fused_step_flat_any_kernel.  One launch takes all the runs of one pointer
+// table (StagedRuns: with the per-parameter layout a window of parameters
+// cut out of a group is one run per rank shard); each run has its own CTAs,
+// and its edge elements run on lanes 0..15 of the warp after its rounds'.
+// The runs of one staged copy-in launch: a parameter window's runs of the
+// packed index (at most kMaxRuns), run i its whole vectors [vbeg[i], vbeg[i] +
+// 8 * nvec[i]), taken by nwarps[i] warps of `iters` rounds, and its edge
+// elements ed[i] (on the warp after them); run i takes CTAs [cta0[i],
+// cta0[i + 1]).
+constexpr int kMaxRuns = 64;
+struct StagedRuns {
+    int64_t vbeg[kMaxRuns];
+    int64_t nvec[kMaxRuns];
+    int64_t nwarps[kMaxRuns];
+    int64_t cta0[kMaxRuns + 1];
+    EdgeElems ed[kMaxRuns];
+    int n;
+};
+
 template <int NR>
 __global__ void __launch_bounds__(kThreads, 3)
 fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* __restrict__ pm_block,
-                                int64_t vbeg, int64_t nvec, int64_t nwarps, int iters, int pdl,
-                                EdgeElems ed, StepArgs a, PtrTab tab) {
+                                StagedRuns runs, int iters, int pdl, StepArgs a, PtrTab tab) {
     extern __shared__ uint4 stage[];
     // pdl bit 0: the call's next staged launch (another window's runs) may
     // start once every CTA here has; bit 1: this launch ends only after the
@@ -751,7 +767,12 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
     constexpr int kBufBlocks = kStageBatch * kStageBlocks;  // one batch of ranks
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    const int64_t gw = (int64_t)blockIdx.x * kStagedWarps + wib;
+    int ri = 0;  // the CTA's run
+    while (ri + 1 < runs.n && (int64_t)blockIdx.x >= runs.cta0[ri + 1]) ++ri;
+    const int64_t cb = (int64_t)blockIdx.x - runs.cta0[ri];  // the CTA's place in its run
+    const int64_t vbeg = runs.vbeg[ri], nvec = runs.nvec[ri], nwarps = runs.nwarps[ri];
+    const EdgeElems ed = runs.ed[ri];
+    const int64_t gw = cb * kStagedWarps + wib;
     const int n = NR > 0 ? NR : a.N;
     const uint4* wst = stage + (size_t)wib * staged_bufs(NR) * kBufBlocks;
     const uint32_t wst_s = (uint32_t)__cvta_generic_to_shared(wst);
@@ -763,7 +784,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
     // wib + 8, ... of them, so the CTA's warps read neighbouring 512-byte runs
     // of each rank at once (4 KiB together) rather than runs 8 rounds apart
     constexpr int64_t kStride = 8 * 32 * kStagedWarps;  // elements between a warp's rounds
-    int64_t f = vbeg + 8 * (((int64_t)blockIdx.x * kStagedWarps * iters + wib) * 32 + lane);
+    int64_t f = vbeg + 8 * ((cb * kStagedWarps * iters + wib) * 32 + lane);
     for (int it = iters; it > 0; --it, f += kStride) {
         if (__shfl_sync(kAll, f, 0) >= fend) break;  // the same for the whole warp
         const bool has = f < fend;
@@ -893,8 +914,7 @@ fused_step_copyin_staged_kernel(const ss::PmEntry* __restrict__ pm, const int* _
     if (pdl & 2) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-using StagedKern = void (*)(const ss::PmEntry*, const int*, int64_t, int64_t, int64_t, int, int,
-                            EdgeElems, StepArgs, PtrTab);
+using StagedKern = void (*)(const ss::PmEntry*, const int*, StagedRuns, int, int, StepArgs, PtrTab);
 
 StagedKern pick_staged(int N, int* smem) {
     StagedKern k;
@@ -1057,6 +1077,51 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
         }
     };
     bool staged_launched = false;  // a staged copy-in launch of this call is queued
+    // The staged copy-in's runs of the current pointer table, launched
+    // together by staged_flush: rounds of 32 vectors per warp, as many rounds
+    // per warp as keep kCopyinMinWaves waves of CTAs over all the runs (at
+    // most kCopyinIters), each run's CTAs after the last run's, and one extra
+    // warp per run for its edge elements.  Launches after a call's first may
+    // start while the one before ends (programmatic dependent launch); each
+    // ends only after the one before it.
+    StagedRuns staged;
+    staged.n = 0;
+    int64_t staged_vecs = 0;
+    auto staged_flush = [&]() -> int {
+        if (staged.n == 0) return SS_OK;
+        int smem = 0;
+        const StagedKern fk = pick_staged(N, &smem);
+        int rc = staged_prepare(fk, smem);
+        if (rc) return rc;
+        const int64_t per_round = 32 * (int64_t)kStagedWarps;  // vectors per CTA round
+        const int64_t it = staged_vecs / (per_round * kCopyinMinWaves * 3 * ss::num_sms());
+        const int iters = (int)(it < 1 ? 1 : it > kCopyinIters ? kCopyinIters : it);
+        const int64_t span = 32 * (int64_t)iters;  // vectors per warp
+        staged.cta0[0] = 0;
+        for (int i = 0; i < staged.n; ++i) {
+            staged.nwarps[i] = (staged.nvec[i] + span - 1) / span;
+            staged.cta0[i + 1] = staged.cta0[i] + (staged.nwarps[i] + 1 + kStagedWarps - 1) / kStagedWarps;
+        }
+        if (staged.cta0[staged.n] > 0x7FFFFFFF) return SS_EOVERFLOW;
+        const int pdl = staged_launched ? 3 : 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)staged.cta0[staged.n]);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1] = {};
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = staged_launched ? 1 : 0;
+        const cudaError_t le = cudaLaunchKernelEx(&cfg, fk, (const ss::PmEntry*)plan->d_pm,
+                                                  (const int*)plan->d_pm_block, staged, iters, pdl, a, tab);
+        rc = le == cudaSuccess ? ss::check_launch() : ss::cuda_fail(le);
+        staged_launched = true;
+        staged.n = 0;
+        staged_vecs = 0;
+        return rc;
+    };
     // The step over packed range [rlo, rhi), whose data segments all belong to
     // the parameters in the pointer table.
     auto run = [&](int64_t rlo, int64_t rhi) -> int {
@@ -1126,49 +1191,16 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             ed = EdgeElems{rlo, rhi, (int)(rhi - rlo), 0};
         }
         const EdgeElems none{0, 0, 0, 0};
-        if (unpacked) {
-            // rounds of 32 vectors per warp, as many rounds per warp as keep
-            // 2 waves of CTAs (at most kCopyinIters), and one extra warp for
-            // the edges
-            int smem = 0;
-            const StagedKern fk = pick_staged(N, &smem);
-            int rc = staged_prepare(fk, smem);
-            if (rc) return rc;
-            const int64_t per_round = 32 * (int64_t)kStagedWarps;  // vectors per CTA round
-            int64_t it = nvec / (per_round * kCopyinMinWaves * 3 * ss::num_sms());
-            const int iters = (int)(it < 1 ? 1 : it > kCopyinIters ? kCopyinIters : it);
-            const int64_t span = 32 * (int64_t)iters;  // vectors per warp
-            const int64_t nw = (nvec + span - 1) / span;
-            constexpr int64_t kChunkW = (int64_t)1 << 32;  // warps per launch
-            int64_t w0 = 0;
-            do {
-                const int64_t cw = nw - w0 < kChunkW ? nw - w0 : kChunkW;
-                const bool last = w0 + cw >= nw;
-                const int64_t cv = last ? nvec - span * w0 : span * cw;
-                const int64_t warps = cw + (last ? 1 : 0);
-                const unsigned grid = (unsigned)((warps + kStagedWarps - 1) / kStagedWarps);
-                // launches after a call's first staged one may start while it
-                // ends (programmatic dependent launch); each ends only after
-                // the one before it
-                const int pdl = staged_launched ? 3 : 1;
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(grid);
-                cfg.blockDim = dim3(kThreads);
-                cfg.dynamicSmemBytes = (size_t)smem;
-                cfg.stream = st;
-                cudaLaunchAttribute attr[1] = {};
-                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-                attr[0].val.programmaticStreamSerializationAllowed = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = staged_launched ? 1 : 0;
-                const cudaError_t le = cudaLaunchKernelEx(&cfg, fk, (const ss::PmEntry*)plan->d_pm,
-                                                          (const int*)plan->d_pm_block, lo8 + 8 * span * w0, cv,
-                                                          cw, iters, pdl, last ? ed : none, a, tab);
-                rc = le == cudaSuccess ? ss::check_launch() : ss::cuda_fail(le);
+        if (unpacked) {  // queued: one launch per pointer table (staged_flush)
+            if (staged.n == kMaxRuns) {
+                const int rc = staged_flush();
                 if (rc) return rc;
-                staged_launched = true;
-                w0 += cw;
-            } while (w0 < nw);
+            }
+            const int i = staged.n++;
+            staged.vbeg[i] = lo8;
+            staged.nvec[i] = nvec;
+            staged.ed[i] = ed;
+            staged_vecs += nvec;
             return SS_OK;
         }
         if (nvec + 16 <= kSmallVecs && per_param * a.w <= kTabSmall) {
@@ -1210,7 +1242,8 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
     if (hi <= lo || plan->pm.empty()) return SS_OK;
     if (pb - pa <= wmax) {  // one pointer table: the whole range at once
         fill(pa, pb);
-        return run(lo, hi);
+        const int rc = run(lo, hi);
+        return rc ? rc : staged_flush();
     }
     // More parameters than one pointer table: windows of consecutive
     // parameters, whole groups packed greedily into each (a group larger than
@@ -1261,6 +1294,8 @@ extern "C" int fsdp_sharded_step(const ss_plan* plan, const ss_step* s, int grou
             int rc = run(rl, rh);
             if (rc) return rc;
         }
+        int rc = staged_flush();  // before the next window refills the table
+        if (rc) return rc;
     }
     return SS_OK;
 }
